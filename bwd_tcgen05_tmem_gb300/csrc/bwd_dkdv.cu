@@ -1,0 +1,475 @@
+// bwd_dkdv.cu -- key/value-stationary backward kernel: dK and dV
+// (tcgen05 / TMEM / TMA).
+//
+// One CTA owns 128 key rows of one (sequence, key/value head) and walks every
+// query head of its GQA group and every visible query tile i of BQ rows
+// (TransformerEngine PR #3699: gradients reduced over the GQA group; PR #3510
+// backward chain):
+//   S^T  = K Q_i^T            (SS MMA, K resident)
+//   dP^T = V dO_i^T           (SS MMA, V resident)            [dK]
+//   P^T  = exp(scale S^T - LSE_i),  dS^T = P^T (dP^T - D_i)   (softmax warps)
+//   dV  += P^T dO_i           (TS MMA: P^T from TMEM)         [dV]
+//   dK  += dS^T Q_i           (TS MMA: dS^T from TMEM)        [dK]
+// then dK *= scale.  The group reduction happens in TMEM, in a fixed order:
+// no atomics, bitwise reproducible.
+//
+// MODE selects the accumulators: 3 = dK and dV, 1 = dV only, 2 = dK only
+// (head dim 256 runs one launch of each: both accumulators do not fit in the
+// 512 TMEM columns next to the score tiles).
+//
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// MMA issuer, warp 2 loads LSE_i / D_i into shared memory, warps 4..11 two
+// softmax warpgroups splitting the BQ query columns.
+#include "bwd.h"
+
+namespace attn {
+
+template <int DQK, int DV, int BQ, int MODE>
+struct DkvCfg {
+  static constexpr bool kDV = (MODE & 1) != 0;
+  static constexpr bool kDK = (MODE & 2) != 0;
+  static constexpr int kKSlots = DQK / 64;
+  static constexpr int kVSlots = kDK ? DV / 64 : 0;
+  static constexpr int kResident = (kKSlots + kVSlots) * kSlotBytes;
+  static constexpr int kChunk = BQ * 128;
+  static constexpr int kQCh = DQK / 64;
+  static constexpr int kDoCh = DV / 64;
+  static constexpr int kPerTile = kQCh + kDoCh;
+  static constexpr int kBudget = 232448 - 1024 - (2 * BQ * 8 + 640);
+  static constexpr int kRingRaw = (kBudget - kResident) / kChunk;
+  static constexpr int kRing = kRingRaw > 24 ? 24 : kRingRaw;
+  static constexpr int kSmem = kResident + kRing * kChunk + 1024;
+  static constexpr int kHalf = BQ / 2;
+  // TMEM columns
+  static constexpr int kTS = 0;
+  static constexpr int kTdP = BQ;
+  static constexpr int kTP = kDK ? 2 * BQ : BQ;
+  static constexpr int kTdS = kTP + (kDV ? BQ / 2 : 0);
+  static constexpr int kTAcc = ((kTdS + (kDK ? BQ / 2 : 0)) + 31) / 32 * 32;
+  static constexpr int kTdV = kTAcc;
+  static constexpr int kTdK = kTAcc + (kDV ? DV : 0);
+  static constexpr int kTEnd = kTdK + (kDK ? DQK : 0);
+  static_assert(kTEnd <= 512, "TMEM budget");
+  static_assert(BQ == 64 || BQ == 128, "BQ");
+  static_assert(MODE >= 1 && MODE <= 3, "MODE");
+  // Slots are assigned in load order.  dK-only loads dO(i) before Q(i) (Q is
+  // held for the dK MMA); the other modes load Q(i) first.  The score MMAs of
+  // tile i+1 are issued before the accumulate MMAs of tile i, so the chunks up
+  // to the end of the scores of tile i+1 must not reuse a slot still held by
+  // tile i.
+  static constexpr bool kDoFirst = kDK && !kDV;
+  static constexpr int kNeed = (kDK && kDV) ? 2 * kPerTile
+                               : kDK        ? kPerTile + kQCh
+                                            : kPerTile;
+  static_assert(kRing >= kNeed, "ring too small for the pipeline");
+};
+
+template <int DQK, int DV, int BQ, int MODE, bool BF16, bool G_F32>
+__global__ void __launch_bounds__(384, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ DkvParams p) {
+  using C = DkvCfg<DQK, DV, BQ, MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kKSlots * kSlotBytes;
+  uint8_t* sRing = smem + C::kResident;
+
+  __shared__ uint64_t full_bar[C::kRing], empty_bar[C::kRing];
+  __shared__ uint64_t kv_bar, sdp_full, sc_free, pds_full, acc_done, drain_bar;
+  __shared__ uint64_t ld_full[2], ld_empty[2];
+  __shared__ float s_lse2[2][BQ], s_d[2][BQ];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag, skip_sh;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = blockIdx.x;
+  const int ktile = blockIdx.y;
+  const int b = blockIdx.z;
+  const int tb = p.geo.cu_q ? 0 : b;  // TMA batch coordinate (packed THD tensors have one)
+  const int grp = p.hq / p.hkv;
+
+  const Seq sq = load_seq(p.geo, b);
+  const int k0 = ktile * kBlockM;
+  if (k0 >= sq.lk) return;
+  if (threadIdx.x == 0) skip_sh = (p.status && *(volatile int*)p.status) ? 1 : 0;
+  __syncthreads();
+  if (skip_sh) return;
+  long long i0, i1;
+  query_range(sq, k0, min(k0 + kBlockM, sq.lk) - 1, i0, i1);
+  const int qt0 = (i1 >= i0) ? (int)(i0 / BQ) : 0;
+  const int n_qt = (i1 >= i0) ? (int)(i1 / BQ) - qt0 + 1 : 0;
+  const int n_it = n_qt * grp;  // iterations: head-major over the group, then query tiles
+
+  Abort ab{&abort_flag, p.status};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < C::kRing; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(&kv_bar, 1);
+    mbar_init(&sdp_full, 1);
+    mbar_init(&sc_free, 256);
+    mbar_init(&pds_full, 256);
+    mbar_init(&acc_done, 1);
+    mbar_init(&drain_bar, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ld_full[s], 32);
+      mbar_init(&ld_empty[s], 256);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  // chunk index of (iteration, which, c): Q chunks first, then dO chunks
+  auto q_idx = [&](int it, int c) {
+    return (uint32_t)(it * C::kPerTile + (C::kDoFirst ? C::kDoCh : 0) + c);
+  };
+  auto do_idx = [&](int it, int c) {
+    return (uint32_t)(it * C::kPerTile + (C::kDoFirst ? 0 : C::kQCh) + c);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one_lane() && n_it > 0) {
+      int c1, c2, c3;
+      map_coords(p.ok, 0, g, sq.k_start + k0, tb, c1, c2, c3);
+      mbar_arrive_tx(&kv_bar, (C::kKSlots + C::kVSlots) * kSlotBytes);
+      for (int c = 0; c < C::kKSlots; ++c)
+        tma_load_4d(sK + c * kSlotBytes, &p.tm_k, &kv_bar, c * 64, c1, c2, c3);
+      if (C::kDK) {
+        map_coords(p.ov, 0, g, sq.k_start + k0, tb, c1, c2, c3);
+        for (int c = 0; c < C::kVSlots; ++c)
+          tma_load_4d(sV + c * kSlotBytes, &p.tm_v, &kv_bar, c * 64, c1, c2, c3);
+      }
+      uint32_t cnt = 0;
+      bool ok = true;
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int h = g * grp + it / n_qt;
+        const int qrow = sq.q_start + (qt0 + it % n_qt) * BQ;
+        for (int which = 0; which < 2 && ok; ++which) {
+          const bool is_do = (which == 1) != C::kDoFirst;
+          const CUtensorMap* m = is_do ? &p.tm_do : &p.tm_q;
+          int d1, d2, d3;
+          map_coords(is_do ? p.odo : p.oq, 0, h, qrow, tb, d1, d2, d3);
+          const int nch = is_do ? C::kDoCh : C::kQCh;
+          for (int c = 0; c < nch; ++c, ++cnt) {
+            const int slot = cnt % C::kRing;
+            if (!mbar_wait(&empty_bar[slot], ((cnt / C::kRing) & 1u) ^ 1u, ab)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_tx(&full_bar[slot], C::kChunk);
+            tma_load_4d(sRing + slot * C::kChunk, m, &full_bar[slot], c * 64, d1, d2, d3);
+          }
+        }
+      }
+      mbar_wait_quiet(&kv_bar, 0, kWaitLimitNs);
+      const uint32_t first = cnt > (uint32_t)C::kRing ? cnt - C::kRing : 0u;
+      for (uint32_t c = first; c < cnt; ++c)
+        mbar_wait_quiet(&full_bar[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one_lane() && n_it > 0) {
+      const uint32_t idesc_s = make_idesc(128, BQ, BF16, false, false);
+      const uint32_t idesc_a = make_idesc(128, 64, BF16, false, true);
+      bool ok = mbar_wait(&kv_bar, 0, ab);
+      tc_fence_after();
+      auto wait_chunk = [&](uint32_t idx) -> uint32_t {
+        const uint32_t slot = idx % C::kRing;
+        if (!mbar_wait(&full_bar[slot], (idx / C::kRing) & 1u, ab)) {
+          ok = false;
+          return 0u;
+        }
+        tc_fence_after();
+        return smem_u32(sRing + slot * C::kChunk);
+      };
+      auto issue_scores = [&](int it) {
+        for (int c = 0; c < C::kQCh && ok; ++c) {
+          const uint32_t qb = wait_chunk(q_idx(it, c));
+          if (!ok) return;
+          const uint32_t ka = smem_u32(sK + c * kSlotBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + C::kTS, make_sdesc(ka + k * 32, 16, 1024),
+                   make_sdesc(qb + k * 32, 16, 1024), idesc_s, (c | k) ? 1u : 0u);
+          if (!C::kDK) mma_commit(&empty_bar[q_idx(it, c) % C::kRing]);
+        }
+        if (C::kDK) {
+          for (int c = 0; c < C::kDoCh && ok; ++c) {
+            const uint32_t db = wait_chunk(do_idx(it, c));
+            if (!ok) return;
+            const uint32_t va = smem_u32(sV + c * kSlotBytes);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + C::kTdP, make_sdesc(va + k * 32, 16, 1024),
+                     make_sdesc(db + k * 32, 16, 1024), idesc_s, (c | k) ? 1u : 0u);
+            if (!C::kDV) mma_commit(&empty_bar[do_idx(it, c) % C::kRing]);
+          }
+        }
+        if (ok) mma_commit(&sdp_full);
+      };
+      auto issue_acc = [&](int it) {
+        if (C::kDV) {
+          for (int c = 0; c < C::kDoCh && ok; ++c) {
+            const uint32_t db = wait_chunk(do_idx(it, c));  // already complete when dK
+            if (!ok) return;
+#pragma unroll
+            for (int k = 0; k < BQ / 16; ++k)
+              mma_ts(tmem + C::kTdV + c * 64, tmem + C::kTP + k * 8,
+                     make_sdesc(db + k * 2048, 16, 1024), idesc_a, (it > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&empty_bar[do_idx(it, c) % C::kRing]);
+          }
+        }
+        if (C::kDK) {
+          for (int c = 0; c < C::kQCh && ok; ++c) {
+            const uint32_t qb = wait_chunk(q_idx(it, c));
+            if (!ok) return;
+#pragma unroll
+            for (int k = 0; k < BQ / 16; ++k)
+              mma_ts(tmem + C::kTdK + c * 64, tmem + C::kTdS + k * 8,
+                     make_sdesc(qb + k * 2048, 16, 1024), idesc_a, (it > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&empty_bar[q_idx(it, c) % C::kRing]);
+          }
+        }
+        if (ok) mma_commit(&acc_done);
+      };
+      if (ok) issue_scores(0);
+      for (int it = 0; it < n_it && ok; ++it) {
+        if (it + 1 < n_it) {
+          if (!mbar_wait(&sc_free, it & 1u, ab)) break;
+          issue_scores(it + 1);
+          if (!ok) break;
+        }
+        if (!mbar_wait(&pds_full, it & 1u, ab)) break;
+        tc_fence_after();
+        issue_acc(it);
+      }
+      mma_commit(&drain_bar);
+      mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ LSE / D loader
+    bool ok = true;
+    for (int it = 0; it < n_it && ok; ++it) {
+      const int st = it & 1;
+      if (!mbar_wait_warp(&ld_empty[st], ((it >> 1) & 1u) ^ 1u, ab)) break;
+      const int h = g * grp + it / n_qt;
+      const int q0 = (qt0 + it % n_qt) * BQ;
+      for (int t = lane; t < BQ; t += 32) {
+        const int i = q0 + t;
+        float l2 = INFINITY, dd = 0.0f;
+        if (i < sq.lq) {
+          const int64_t tok = (int64_t)sq.q_start + i;
+          l2 = p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + tok] * 1.4426950408889634f;
+          dd = p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok];
+          if (l2 == -INFINITY) l2 = INFINITY;  // keyless query row: masked anyway
+        }
+        s_lse2[st][t] = l2;
+        s_d[st][t] = dd;
+      }
+      mbar_arrive(&ld_full[st]);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / dS
+    const int wq = (warp - 4) & 3;
+    const int wg = (warp - 4) >> 2;
+    const int r = wq * 32 + lane;
+    const int j = k0 + r;  // key row within the sequence
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const int col0 = wg * C::kHalf;
+    const float sl2 = p.scale_log2;
+    // query rows that see key j: [vis_lo, vis_hi]
+    const long long vis_lo = (long long)j - sq.off - sq.R;
+    long long vis_hi = (long long)j - sq.off + sq.L;
+    if (vis_hi > sq.lq - 1) vis_hi = sq.lq - 1;
+    const long long krow_last = min(k0 + kBlockM, sq.lk) - 1;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it & 1;
+      const int q0 = (qt0 + it % n_qt) * BQ;
+      if (!mbar_wait_warp(&sdp_full, it & 1u, ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[C::kHalf], dp[C::kHalf];
+#pragma unroll
+      for (int c = 0; c < C::kHalf / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_off + C::kTS + col0 + c * 32, rr);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(rr[t]);
+        if constexpr (C::kDK) {
+          tmem_ld32(tmem + lane_off + C::kTdP + col0 + c * 32, rr);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) dp[c * 32 + t] = __uint_as_float(rr[t]);
+        }
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sc_free);
+      if (!mbar_wait_warp(&ld_full[st], (it >> 1) & 1u, ab)) {
+        ok = false;
+        break;
+      }
+      const int c0 = q0 + col0;  // first query row of this warpgroup's columns
+      const bool full_tile = ((long long)(c0 + C::kHalf - 1) <= sq.lq - 1) &&
+                             ((long long)c0 >= krow_last - sq.off - sq.R) &&
+                             ((long long)(c0 + C::kHalf - 1) <= (long long)k0 - sq.off + sq.L);
+      const long long lo = vis_lo - c0, hi = vis_hi - c0;
+      uint32_t pp[C::kHalf / 2], pd[C::kHalf / 2];
+#pragma unroll
+      for (int t = 0; t < C::kHalf; t += 2) {
+        float e0 = ex2(fmaf(s[t], sl2, -s_lse2[st][col0 + t]));
+        float e1 = ex2(fmaf(s[t + 1], sl2, -s_lse2[st][col0 + t + 1]));
+        if (!full_tile) {
+          if (t < lo || t > hi) e0 = 0.0f;
+          if (t + 1 < lo || t + 1 > hi) e1 = 0.0f;
+        }
+        if constexpr (C::kDV) pp[t / 2] = Pack<BF16>::two(e0, e1);
+        if constexpr (C::kDK)
+          pd[t / 2] = Pack<BF16>::two(e0 * (dp[t] - s_d[st][col0 + t]),
+                                      e1 * (dp[t + 1] - s_d[st][col0 + t + 1]));
+      }
+      mbar_arrive(&ld_empty[st]);
+      if (it > 0 && !mbar_wait_warp(&acc_done, (it - 1) & 1u, ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < C::kHalf / 32; ++c) {
+        uint32_t w16[16];
+        if constexpr (C::kDV) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) w16[t] = pp[c * 16 + t];
+          tmem_st16(tmem + lane_off + C::kTP + col0 / 2 + c * 16, w16);
+        }
+        if constexpr (C::kDK) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) w16[t] = pd[c * 16 + t];
+          tmem_st16(tmem + lane_off + C::kTdS + col0 / 2 + c * 16, w16);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&pds_full);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && n_it > 0) ok = mbar_wait_warp(&acc_done, (n_it - 1) & 1u, ab);
+    if (ok) {
+      tc_fence_after();
+      const bool valid = j < sq.lk;
+      const int64_t tok = (int64_t)sq.k_start + j;
+      auto store = [&](void* base, int64_t sb, int64_t st_, int64_t sh, int tcol, int D,
+                       float mul) {
+        char* row = (char*)base + ((int64_t)b * sb + tok * st_ + (int64_t)g * sh) * (G_F32 ? 4 : 2);
+        const int half = D / 2;
+        for (int c = 0; c < half / 32; ++c) {
+          const int col = wg * half + c * 32;
+          uint32_t rr[32];
+          if (n_it > 0) {
+            tmem_ld32(tmem + lane_off + tcol + col, rr);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) rr[t] = 0u;
+          }
+          if (!valid) continue;
+          if (G_F32) {
+            float4* dst = reinterpret_cast<float4*>(row + col * 4);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              float4 w = make_float4(__uint_as_float(rr[4 * t]) * mul,
+                                     __uint_as_float(rr[4 * t + 1]) * mul,
+                                     __uint_as_float(rr[4 * t + 2]) * mul,
+                                     __uint_as_float(rr[4 * t + 3]) * mul);
+              if (p.accum) {  // sum into the caller's FP32 gradient
+                const float4 old = dst[t];
+                w.x += old.x;
+                w.y += old.y;
+                w.z += old.z;
+                w.w += old.w;
+              }
+              dst[t] = w;
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(row + col * 2);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              uint4 v;
+              v.x = Pack<BF16>::two(__uint_as_float(rr[8 * t + 0]) * mul,
+                                    __uint_as_float(rr[8 * t + 1]) * mul);
+              v.y = Pack<BF16>::two(__uint_as_float(rr[8 * t + 2]) * mul,
+                                    __uint_as_float(rr[8 * t + 3]) * mul);
+              v.z = Pack<BF16>::two(__uint_as_float(rr[8 * t + 4]) * mul,
+                                    __uint_as_float(rr[8 * t + 5]) * mul);
+              v.w = Pack<BF16>::two(__uint_as_float(rr[8 * t + 6]) * mul,
+                                    __uint_as_float(rr[8 * t + 7]) * mul);
+              dst[t] = v;
+            }
+          }
+        }
+      };
+      if (C::kDV) store(p.dv, p.sdv_b, p.sdv_t, p.sdv_h, C::kTdV, DV, 1.0f);
+      if (C::kDK) store(p.dk, p.sdk_b, p.sdk_t, p.sdk_h, C::kTdK, DQK, p.scale);
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK, int DV, int BQ, int MODE, bool BF16, bool G_F32>
+static cudaError_t launch_dkv_t(const DkvParams& p, cudaStream_t st) {
+  using C = DkvCfg<DQK, DV, BQ, MODE>;
+  auto k = attn_bwd_dkdv_kernel<DQK, DV, BQ, MODE, BF16, G_F32>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)p.hkv, (unsigned)p.n_ktiles, (unsigned)p.batch);
+  k<<<grid, 384, C::kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DQK, int DV, int BQ, int MODE>
+static cudaError_t launch_dkv_d(const DkvParams& p, bool bf16, bool gf32, cudaStream_t st) {
+  if (bf16)
+    return gf32 ? launch_dkv_t<DQK, DV, BQ, MODE, true, true>(p, st)
+                : launch_dkv_t<DQK, DV, BQ, MODE, true, false>(p, st);
+  return gf32 ? launch_dkv_t<DQK, DV, BQ, MODE, false, true>(p, st)
+              : launch_dkv_t<DQK, DV, BQ, MODE, false, false>(p, st);
+}
+
+// Query-tile rows streamed by the dK/dV kernel(s) and the launches needed.
+// Returns the number of launches (0 if unsupported); bq[i] / mode[i] describe each.
+int dkv_plan(int dqk, int dv, int* bq, int* mode) {
+  if (dqk == 64 && dv == 64) { bq[0] = 128; mode[0] = 3; return 1; }
+  if (dqk == 128 && dv == 128) { bq[0] = 64; mode[0] = 3; return 1; }
+  if (dqk == 192 && dv == 128) { bq[0] = 64; mode[0] = 3; return 1; }
+  if (dqk == 256 && dv == 256) { bq[0] = 128; mode[0] = 1; bq[1] = 64; mode[1] = 2; return 2; }
+  return 0;
+}
+
+cudaError_t launch_dkv(const DkvParams& p, int dqk, int dv, int mode, bool bf16, bool gf32,
+                       cudaStream_t st) {
+  if (dqk == 64 && dv == 64 && mode == 3) return launch_dkv_d<64, 64, 128, 3>(p, bf16, gf32, st);
+  if (dqk == 128 && dv == 128 && mode == 3) return launch_dkv_d<128, 128, 64, 3>(p, bf16, gf32, st);
+  if (dqk == 192 && dv == 128 && mode == 3) return launch_dkv_d<192, 128, 64, 3>(p, bf16, gf32, st);
+  if (dqk == 256 && dv == 256 && mode == 1) return launch_dkv_d<256, 256, 128, 1>(p, bf16, gf32, st);
+  if (dqk == 256 && dv == 256 && mode == 2) return launch_dkv_d<256, 256, 64, 2>(p, bf16, gf32, st);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace attn

@@ -1,0 +1,380 @@
+// bwd_dq.cu -- query-stationary backward kernel: dQ (tcgen05 / TMEM / TMA).
+//
+// For 128 query rows of one (sequence, query head) and every visible key tile
+// j (TransformerEngine PR #3510 / PR #3699 backward chain):
+//   S  = Q K_j^T          (SS MMA, Q resident in shared memory)
+//   dP = dO V_j^T         (SS MMA, dO resident)
+//   P  = exp(scale S - LSE),  dS = P (dP - D)      (softmax warps, FP32)
+//   dQ += dS K_j          (TS MMA: dS from TMEM, K_j chunk MN-major)
+// and finally dQ *= scale.  No atomics: every dQ element is written once, so
+// the result is bitwise reproducible.
+//
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// MMA issuer, warps 4..11 two softmax warpgroups; warpgroup w owns key
+// columns [w*BKV/2, (w+1)*BKV/2) of every tile (the backward needs no row
+// reduction, so splitting columns is free).  The softmax signals "scores
+// consumed" right after loading S/dP so the next tile's S/dP MMAs overlap the
+// exponentials.
+// TMEM: S [0,BKV)  dP [BKV,2BKV)  dS [2BKV, 2.5BKV) (16-bit, 2 per column)
+//       dQ [kTdQ, kTdQ + DQK).
+#include "bwd.h"
+
+namespace attn {
+
+template <int DQK, int DV, int BKV>
+struct DqCfg {
+  static constexpr int kQSlots = DQK / 64;
+  static constexpr int kDoSlots = DV / 64;
+  static constexpr int kChunk = BKV * 128;
+  static constexpr int kResident = (kQSlots + kDoSlots) * kSlotBytes;
+  static constexpr int kBudget = 232448 - 1024 - 1024;
+  static constexpr int kRingRaw = (kBudget - kResident) / kChunk;
+  static constexpr int kRing = kRingRaw > 24 ? 24 : kRingRaw;
+  static constexpr int kKCh = DQK / 64;
+  static constexpr int kVCh = DV / 64;
+  static constexpr int kTdP = BKV;
+  static constexpr int kTdS = 2 * BKV;
+  static constexpr int kTdQ = ((5 * BKV / 2) + 31) / 32 * 32;
+  static constexpr int kSmem = kResident + kRing * kChunk + 1024;
+  static constexpr int kHalf = BKV / 2;  // columns per softmax warpgroup
+  static_assert(kTdQ + DQK <= 512, "TMEM budget");
+  // Slots are assigned in load order (V(j) then K(j)); K(j) stays held until
+  // dQ(j) is issued, after the score MMAs of tile j+1.  Those need the chunks
+  // up to the end of tile j+1, which reuse slots of tile j's K only if
+  // kRing < (chunks per tile) + kKCh.
+  static constexpr int kPerTile = kKCh + kVCh;
+  static_assert(kRing >= kPerTile + kKCh, "ring too small for the pipeline");
+  static_assert(BKV == 64 || BKV == 128, "BKV");
+};
+
+template <int DQK, int DV, int BKV, bool BF16, bool G_F32>
+__global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_constant__ DqParams p) {
+  using C = DqCfg<DQK, DV, BKV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem;
+  uint8_t* sDo = smem + C::kQSlots * kSlotBytes;
+  uint8_t* sRing = smem + C::kResident;
+
+  __shared__ uint64_t full_bar[C::kRing], empty_bar[C::kRing];
+  __shared__ uint64_t q_bar, sdp_full, sc_free, ds_full, dq_done, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag, skip_sh;
+
+  const int warp = threadIdx.x >> 5;
+  const int h = blockIdx.x;
+  const int tile = p.n_qtiles - 1 - blockIdx.y;
+  const int b = blockIdx.z;
+  const int tb = p.geo.cu_q ? 0 : b;  // TMA batch coordinate (packed THD tensors have one)
+  const int g = h / (p.hq / p.hkv);
+
+  const Seq sq = load_seq(p.geo, b);
+  const int q0 = tile * kBlockM;
+  if (q0 >= sq.lq) return;
+  if (threadIdx.x == 0) skip_sh = (p.status && *(volatile int*)p.status) ? 1 : 0;
+  __syncthreads();
+  if (skip_sh) return;
+  long long j0, j1;
+  key_range(sq, q0, min(q0 + kBlockM, sq.lq) - 1, j0, j1);
+  const int kt0 = (j1 >= j0) ? (int)(j0 / BKV) : 0;
+  const int n_kv = (j1 >= j0) ? (int)(j1 / BKV) - kt0 + 1 : 0;
+
+  Abort ab{&abort_flag, p.status};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < C::kRing; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(&q_bar, 1);
+    mbar_init(&sdp_full, 1);
+    mbar_init(&sc_free, 256);
+    mbar_init(&ds_full, 256);
+    mbar_init(&dq_done, 1);
+    mbar_init(&drain_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one_lane() && n_kv > 0) {
+      int c1, c2, c3;
+      map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
+      mbar_arrive_tx(&q_bar, (C::kQSlots + C::kDoSlots) * kSlotBytes);
+      for (int c = 0; c < C::kQSlots; ++c)
+        tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
+      map_coords(p.odo, 0, h, sq.q_start + q0, tb, c1, c2, c3);
+      for (int c = 0; c < C::kDoSlots; ++c)
+        tma_load_4d(sDo + c * kSlotBytes, &p.tm_do, &q_bar, c * 64, c1, c2, c3);
+      uint32_t cnt = 0;
+      bool ok = true;
+      for (int jt = 0; jt < n_kv && ok; ++jt) {
+        const int krow = sq.k_start + (kt0 + jt) * BKV;
+        for (int which = 0; which < 2 && ok; ++which) {  // V(j) first, then K(j)
+          const bool is_k = which == 1;
+          const CUtensorMap* m = is_k ? &p.tm_k : &p.tm_v;
+          int d1, d2, d3;
+          map_coords(is_k ? p.ok : p.ov, 0, g, krow, tb, d1, d2, d3);
+          const int nch = is_k ? C::kKCh : C::kVCh;
+          for (int c = 0; c < nch; ++c, ++cnt) {
+            const int slot = cnt % C::kRing;
+            if (!mbar_wait(&empty_bar[slot], ((cnt / C::kRing) & 1u) ^ 1u, ab)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_tx(&full_bar[slot], C::kChunk);
+            tma_load_4d(sRing + slot * C::kChunk, m, &full_bar[slot], c * 64, d1, d2, d3);
+          }
+        }
+      }
+      mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
+      const uint32_t first = cnt > (uint32_t)C::kRing ? cnt - C::kRing : 0u;
+      for (uint32_t c = first; c < cnt; ++c)
+        mbar_wait_quiet(&full_bar[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one_lane() && n_kv > 0) {
+      const uint32_t idesc_s = make_idesc(128, BKV, BF16, false, false);
+      const uint32_t idesc_q = make_idesc(128, 64, BF16, false, true);
+      bool ok = true;
+      auto wait_chunk = [&](uint32_t idx) -> uint32_t {
+        const uint32_t slot = idx % C::kRing;
+        if (!mbar_wait(&full_bar[slot], (idx / C::kRing) & 1u, ab)) {
+          ok = false;
+          return 0u;
+        }
+        tc_fence_after();
+        return smem_u32(sRing + slot * C::kChunk);
+      };
+      // chunk index of tile jt: V chunks first, then K chunks
+      auto v_idx = [&](int jt, int c) { return (uint32_t)(jt * C::kPerTile + c); };
+      auto k_idx = [&](int jt, int c) { return (uint32_t)(jt * C::kPerTile + C::kVCh + c); };
+      ok = mbar_wait(&q_bar, 0, ab);
+      tc_fence_after();
+      auto issue_scores = [&](int jt) {
+        for (int c = 0; c < C::kVCh && ok; ++c) {
+          const uint32_t vb = wait_chunk(v_idx(jt, c));
+          if (!ok) return;
+          const uint32_t da = smem_u32(sDo + c * kSlotBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + C::kTdP, make_sdesc(da + k * 32, 16, 1024),
+                   make_sdesc(vb + k * 32, 16, 1024), idesc_s, (c | k) ? 1u : 0u);
+          mma_commit(&empty_bar[v_idx(jt, c) % C::kRing]);
+        }
+        for (int c = 0; c < C::kKCh && ok; ++c) {
+          const uint32_t kb = wait_chunk(k_idx(jt, c));
+          if (!ok) return;
+          const uint32_t qa = smem_u32(sQ + c * kSlotBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem, make_sdesc(qa + k * 32, 16, 1024), make_sdesc(kb + k * 32, 16, 1024),
+                   idesc_s, (c | k) ? 1u : 0u);
+        }
+        if (ok) mma_commit(&sdp_full);
+      };
+      auto issue_dq = [&](int jt) {
+        for (int c = 0; c < C::kKCh; ++c) {
+          const uint32_t slot = k_idx(jt, c) % C::kRing;  // held since the S MMA of tile jt
+          const uint32_t kb = smem_u32(sRing + slot * C::kChunk);
+#pragma unroll
+          for (int k = 0; k < BKV / 16; ++k)
+            mma_ts(tmem + C::kTdQ + c * 64, tmem + C::kTdS + k * 8,
+                   make_sdesc(kb + k * 2048, 16, 1024), idesc_q, (jt > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&empty_bar[slot]);
+        }
+        mma_commit(&dq_done);
+      };
+      if (ok) issue_scores(0);
+      for (int jt = 0; jt < n_kv && ok; ++jt) {
+        if (jt + 1 < n_kv) {
+          if (!mbar_wait(&sc_free, jt & 1u, ab)) break;
+          issue_scores(jt + 1);
+          if (!ok) break;
+        }
+        if (!mbar_wait(&ds_full, jt & 1u, ab)) break;
+        tc_fence_after();
+        issue_dq(jt);
+      }
+      mma_commit(&drain_bar);
+      mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / dS
+    const int wq = (warp - 4) & 3;
+    const int wg = (warp - 4) >> 2;
+    const int r = wq * 32 + (threadIdx.x & 31);
+    const int i = q0 + r;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const int col0 = wg * C::kHalf;
+    const float sl2 = p.scale_log2;
+    const int64_t tok = (int64_t)sq.q_start + i;
+    float lse2 = INFINITY, Dr = 0.0f;
+    if (i < sq.lq) {
+      lse2 = p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + tok] * 1.4426950408889634f;
+      Dr = p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok];
+      if (lse2 == -INFINITY) lse2 = INFINITY;  // keyless row: every key is masked anyway
+    }
+    const long long vis_lo = (long long)i + sq.off - sq.L;
+    long long vis_hi = (long long)i + sq.off + sq.R;
+    if (vis_hi > sq.lk - 1) vis_hi = sq.lk - 1;
+    const long long rows_last = min(q0 + kBlockM, sq.lq) - 1;
+    bool ok = true;
+    for (int jt = 0; jt < n_kv; ++jt) {
+      const int k0 = (kt0 + jt) * BKV;
+      if (!mbar_wait_warp(&sdp_full, jt & 1u, ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[C::kHalf], dp[C::kHalf];
+#pragma unroll
+      for (int c = 0; c < C::kHalf / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_off + col0 + c * 32, rr);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(rr[t]);
+        tmem_ld32(tmem + lane_off + C::kTdP + col0 + c * 32, rr);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) dp[c * 32 + t] = __uint_as_float(rr[t]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sc_free);
+      const int c0 = k0 + col0;  // first key of this warpgroup's columns
+      const bool full_tile = (c0 + C::kHalf - 1 <= sq.lk - 1) &&
+                             ((long long)c0 >= rows_last + sq.off - sq.L) &&
+                             ((long long)(c0 + C::kHalf - 1) <= (long long)q0 + sq.off + sq.R);
+      uint32_t pk[C::kHalf / 2];
+      const long long lo = vis_lo - c0, hi = vis_hi - c0;
+#pragma unroll
+      for (int t = 0; t < C::kHalf; t += 2) {
+        float e0 = ex2(fmaf(s[t], sl2, -lse2));
+        float e1 = ex2(fmaf(s[t + 1], sl2, -lse2));
+        if (!full_tile) {
+          if (t < lo || t > hi) e0 = 0.0f;
+          if (t + 1 < lo || t + 1 > hi) e1 = 0.0f;
+        }
+        pk[t / 2] = Pack<BF16>::two(e0 * (dp[t] - Dr), e1 * (dp[t + 1] - Dr));
+      }
+      if (jt > 0 && !mbar_wait_warp(&dq_done, (jt - 1) & 1u, ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < C::kHalf / 32; ++c) {
+        uint32_t w16[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) w16[t] = pk[c * 16 + t];
+        tmem_st16(tmem + lane_off + C::kTdS + col0 / 2 + c * 16, w16);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ds_full);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && n_kv > 0) ok = mbar_wait_warp(&dq_done, (n_kv - 1) & 1u, ab);
+    if (ok) {
+      tc_fence_after();
+      const bool valid = i < sq.lq;
+      char* row = (char*)p.dq +
+                  ((int64_t)b * p.sdq_b + tok * p.sdq_t + (int64_t)h * p.sdq_h) * (G_F32 ? 4 : 2);
+      constexpr int kCols = DQK / 2;  // dQ columns stored by this warpgroup
+#pragma unroll
+      for (int c = 0; c < kCols / 32; ++c) {
+        const int col = wg * kCols + c * 32;
+        uint32_t rr[32];
+        if (n_kv > 0) {
+          tmem_ld32(tmem + lane_off + C::kTdQ + col, rr);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) rr[t] = 0u;
+        }
+        if (valid) {
+          if (G_F32) {
+            float4* dst = reinterpret_cast<float4*>(row + col * 4);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              float4 w = make_float4(__uint_as_float(rr[4 * t]) * p.scale,
+                                     __uint_as_float(rr[4 * t + 1]) * p.scale,
+                                     __uint_as_float(rr[4 * t + 2]) * p.scale,
+                                     __uint_as_float(rr[4 * t + 3]) * p.scale);
+              if (p.accum) {  // sum into the caller's FP32 gradient
+                const float4 old = dst[t];
+                w.x += old.x;
+                w.y += old.y;
+                w.z += old.z;
+                w.w += old.w;
+              }
+              dst[t] = w;
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(row + col * 2);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              uint4 v;
+              v.x = Pack<BF16>::two(__uint_as_float(rr[8 * t + 0]) * p.scale,
+                                    __uint_as_float(rr[8 * t + 1]) * p.scale);
+              v.y = Pack<BF16>::two(__uint_as_float(rr[8 * t + 2]) * p.scale,
+                                    __uint_as_float(rr[8 * t + 3]) * p.scale);
+              v.z = Pack<BF16>::two(__uint_as_float(rr[8 * t + 4]) * p.scale,
+                                    __uint_as_float(rr[8 * t + 5]) * p.scale);
+              v.w = Pack<BF16>::two(__uint_as_float(rr[8 * t + 6]) * p.scale,
+                                    __uint_as_float(rr[8 * t + 7]) * p.scale);
+              dst[t] = v;
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK, int DV, int BKV, bool BF16, bool G_F32>
+static cudaError_t launch_dq_t(const DqParams& p, cudaStream_t st) {
+  using C = DqCfg<DQK, DV, BKV>;
+  auto k = attn_bwd_dq_kernel<DQK, DV, BKV, BF16, G_F32>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)p.hq, (unsigned)p.n_qtiles, (unsigned)p.batch);
+  k<<<grid, 384, C::kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DQK, int DV, int BKV>
+static cudaError_t launch_dq_d(const DqParams& p, bool bf16, bool gf32, cudaStream_t st) {
+  if (bf16)
+    return gf32 ? launch_dq_t<DQK, DV, BKV, true, true>(p, st)
+                : launch_dq_t<DQK, DV, BKV, true, false>(p, st);
+  return gf32 ? launch_dq_t<DQK, DV, BKV, false, true>(p, st)
+              : launch_dq_t<DQK, DV, BKV, false, false>(p, st);
+}
+
+// Rows of the key/value tile streamed by the dQ kernel for a head-dim pair.
+int dq_block_kv(int dqk, int dv) { return (dqk >= 256 || dv >= 256) ? 64 : 128; }
+
+cudaError_t launch_dq(const DqParams& p, int dqk, int dv, bool bf16, bool gf32, cudaStream_t st) {
+  if (dqk == 64 && dv == 64) return launch_dq_d<64, 64, 128>(p, bf16, gf32, st);
+  if (dqk == 128 && dv == 128) return launch_dq_d<128, 128, 128>(p, bf16, gf32, st);
+  if (dqk == 192 && dv == 128) return launch_dq_d<192, 128, 128>(p, bf16, gf32, st);
+  if (dqk == 256 && dv == 256) return launch_dq_d<256, 256, 64>(p, bf16, gf32, st);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace attn

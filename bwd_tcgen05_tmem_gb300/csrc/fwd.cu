@@ -1,0 +1,389 @@
+// fwd.cu -- fused attention forward on tcgen05 / TMEM / TMA (sm_103a).
+//
+// Computes O = softmax(scale * Q K^T + mask) V and the natural-log LSE per
+// query row with an online (running-maximum) softmax over key tiles
+// (TransformerEngine PR #3527: the forward saves a natural-log logsumexp in
+// FP32; PR #3510: causal FP16/BF16 attention on Blackwell).
+//
+// One CTA owns 128 query rows of one (sequence, query head) and, for head dim
+// 512, one half of the value columns.  Warp roles (256 threads):
+//   warp 0      TMA producer: Q once, then K/V 64-column chunks through a ring
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warps 4..7  softmax: one TMEM lane (= query row) per thread; rescales O
+//               in TMEM when the running maximum grows, writes P (16-bit)
+//               into TMEM, and runs the epilogue.
+// TMEM columns: S buffers [0,128) and [128,256) (P overwrites the first 64
+// columns of its S buffer), O accumulator [256, 256 + DV_CTA).
+// MMAs: S = Q K^T   SS, both K-major (128 x 128 x DQK)
+//       O += P V    TS, A = P from TMEM, B = V chunk (MN-major), N = 64 each.
+#include "kcommon.cuh"
+
+namespace attn {
+
+template <int DQK, int DV_CTA, bool BF16, bool O_F32>
+struct FwdCfg {
+  static constexpr int kQSlots = DQK / 64;
+  static constexpr int kRing = kMaxSlots - kQSlots;
+  static constexpr int kVChunks = DV_CTA / 64;
+  static constexpr int kKChunks = DQK / 64;
+  static constexpr int kSmem = (kQSlots + kRing) * kSlotBytes + 1024;
+  static constexpr int kTmemO = 256;
+  static_assert(DQK % 64 == 0 && DV_CTA % 64 == 0 && DV_CTA <= 256, "head dim");
+  static_assert(kRing >= 2, "ring");
+};
+
+template <int DQK, int DV_CTA, bool BF16, bool O_F32>
+__global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<DQK, DV_CTA, BF16, O_F32>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::kQSlots * kSlotBytes;
+
+  __shared__ uint64_t full_bar[C::kRing], empty_bar[C::kRing];
+  __shared__ uint64_t q_bar, s_full[2], p_full[2], o_done, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag, skip_sh;
+
+  const int warp = threadIdx.x >> 5;
+  const int split = blockIdx.x % p.n_split;
+  const int h = blockIdx.x / p.n_split;
+  const int tile = p.n_qtiles - 1 - blockIdx.y;
+  const int b = blockIdx.z;
+  const int tb = p.geo.cu_q ? 0 : b;  // TMA batch coordinate (packed THD tensors have one)
+  const int g = h / (p.hq / p.hkv);
+
+  const Seq sq = load_seq(p.geo, b);
+  const int q0 = tile * kBlockM;
+  if (q0 >= sq.lq) return;  // tile past the end of this sequence (uniform)
+  // a failed device check (cu_seqlens) or an earlier abort stops every CTA
+  if (threadIdx.x == 0) skip_sh = (p.status && *(volatile int*)p.status) ? 1 : 0;
+  __syncthreads();
+  if (skip_sh) return;
+  long long j0, j1;
+  key_range(sq, q0, min(q0 + kBlockM, sq.lq) - 1, j0, j1);
+  const int kt0 = (j1 >= j0) ? (int)(j0 / kBlockN) : 0;
+  const int n_kv = (j1 >= j0) ? (int)(j1 / kBlockN) - kt0 + 1 : 0;
+
+  Abort ab{&abort_flag, p.status};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < C::kRing; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(&q_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+    }
+    mbar_init(&o_done, 1);
+    mbar_init(&drain_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one_lane() && n_kv > 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      int c1, c2, c3;
+      map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
+      mbar_arrive_tx(&q_bar, C::kQSlots * kSlotBytes);
+      for (int c = 0; c < C::kQSlots; ++c)
+        tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
+      uint32_t cnt = 0;
+      bool ok = true;
+      // consumption order: K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1)
+      auto load_chunks = [&](bool is_v, int jt) {
+        const int krow = sq.k_start + (kt0 + jt) * kBlockN;
+        int d1, d2, d3;
+        if (is_v)
+          map_coords(p.ov, 0, g, krow, tb, d1, d2, d3);
+        else
+          map_coords(p.ok, 0, g, krow, tb, d1, d2, d3);
+        const int nch = is_v ? C::kVChunks : C::kKChunks;
+        const int col0 = is_v ? split * DV_CTA : 0;
+        for (int c = 0; c < nch && ok; ++c, ++cnt) {
+          const int slot = cnt % C::kRing;
+          const uint32_t ph = (cnt / C::kRing) & 1u;
+          if (!mbar_wait(&empty_bar[slot], ph ^ 1u, ab)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_tx(&full_bar[slot], kSlotBytes);
+          tma_load_4d(sRing + slot * kSlotBytes, is_v ? &p.tm_v : &p.tm_k, &full_bar[slot],
+                      col0 + c * 64, d1, d2, d3);
+        }
+      };
+      load_chunks(false, 0);
+      for (int jt = 0; jt < n_kv && ok; ++jt) {
+        if (jt + 1 < n_kv) load_chunks(false, jt + 1);
+        load_chunks(true, jt);
+      }
+      // let every copy still in flight land before the CTA can exit
+      mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
+      const uint32_t first = cnt > (uint32_t)C::kRing ? cnt - C::kRing : 0u;
+      for (uint32_t c = first; c < cnt; ++c)
+        mbar_wait_quiet(&full_bar[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one_lane() && n_kv > 0) {
+      const uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
+      const uint32_t idesc_o = make_idesc(128, 64, BF16, false, true);
+      uint32_t cnt = 0;
+      bool ok = mbar_wait(&q_bar, 0, ab);
+      tc_fence_after();
+      auto issue_s = [&](int jt) {
+        const uint32_t d = tmem + (uint32_t)((jt & 1) * 128);
+        for (int c = 0; c < C::kKChunks && ok; ++c, ++cnt) {
+          const int slot = cnt % C::kRing;
+          if (!mbar_wait(&full_bar[slot], (cnt / C::kRing) & 1u, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sQ + c * kSlotBytes);
+          const uint32_t kb = smem_u32(sRing + slot * kSlotBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(d, make_sdesc(qa + k * 32, 16, 1024), make_sdesc(kb + k * 32, 16, 1024),
+                   idesc_s, (c | k) ? 1u : 0u);
+          mma_commit(&empty_bar[slot]);
+        }
+        if (ok) mma_commit(&s_full[jt & 1]);
+      };
+      auto issue_pv = [&](int jt) {
+        if (!mbar_wait(&p_full[jt & 1], (jt >> 1) & 1u, ab)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        const uint32_t pa = tmem + (uint32_t)((jt & 1) * 128);
+        for (int c = 0; c < C::kVChunks && ok; ++c, ++cnt) {
+          const int slot = cnt % C::kRing;
+          if (!mbar_wait(&full_bar[slot], (cnt / C::kRing) & 1u, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vb = smem_u32(sRing + slot * kSlotBytes);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + C::kTmemO + c * 64, pa + k * 8, make_sdesc(vb + k * 2048, 16, 1024),
+                   idesc_o, (jt > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&empty_bar[slot]);
+        }
+        if (ok) mma_commit(&o_done);
+      };
+      if (ok) issue_s(0);
+      for (int jt = 0; jt < n_kv && ok; ++jt) {
+        if (jt + 1 < n_kv) {
+          // S buffer (jt+1)&1 last held P(jt-1): wait until PV(jt-1) has read it
+          if (jt >= 1 && !mbar_wait(&o_done, (jt - 1) & 1u, ab)) break;
+          issue_s(jt + 1);
+        }
+        if (ok) issue_pv(jt);
+      }
+      mma_commit(&drain_bar);
+      mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int wq = warp - 4;
+    const int r = wq * 32 + (threadIdx.x & 31);
+    const int i = q0 + r;  // query row within the sequence
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.0f;
+    const long long vis_lo = (long long)i + sq.off - sq.L;  // first visible key
+    long long vis_hi = (long long)i + sq.off + sq.R;        // last visible key
+    if (vis_hi > sq.lk - 1) vis_hi = sq.lk - 1;
+    // rows that see every key of a tile need no per-element mask; decide per tile
+    const long long rows_last = min(q0 + kBlockM, sq.lq) - 1;
+    bool ok = true;
+    for (int jt = 0; jt < n_kv; ++jt) {
+      const int k0 = (kt0 + jt) * kBlockN;
+      if (!mbar_wait_warp(&s_full[jt & 1], (jt >> 1) & 1u, ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sb = tmem + lane_off + (uint32_t)((jt & 1) * 128);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(sb + c * 32, rr);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(rr[t]);
+      }
+      tmem_ld_wait();
+      const bool full_tile = (k0 + kBlockN - 1 <= sq.lk - 1) &&
+                             ((long long)k0 >= rows_last + sq.off - sq.L) &&
+                             ((long long)(k0 + kBlockN - 1) <= (long long)q0 + sq.off + sq.R);
+      if (!full_tile) {
+        const long long lo = vis_lo - k0, hi = vis_hi - k0;
+#pragma unroll
+        for (int t = 0; t < 128; ++t)
+          if (t < lo || t > hi) s[t] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 128; ++t) mx = fmaxf(mx, s[t]);
+      const float m_tile = mx * sl2;
+      const bool grow = m_tile > m_run + 8.0f;
+      const float m_new = grow ? m_tile : m_run;
+      const float alpha = grow ? ex2(m_run - m_new) : 1.0f;
+      m_run = m_new;
+      const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
+      float rs = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float e0 = ex2(fmaf(s[c * 32 + 2 * t], sl2, neg_m));
+          const float e1 = ex2(fmaf(s[c * 32 + 2 * t + 1], sl2, neg_m));
+          rs += e0 + e1;
+          pk[t] = Pack<BF16>::two(e0, e1);
+        }
+        tmem_st16(sb + c * 16, pk);
+      }
+      l_run = l_run * alpha + rs;
+      // rescale O rows whose maximum grew (after PV(jt-1) has finished)
+      if (__any_sync(0xffffffffu, grow && jt > 0)) {
+        if (!mbar_wait_warp(&o_done, (jt - 1) & 1u, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < DV_CTA / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_off + C::kTmemO + c * 32, rr);
+          tmem_ld_wait();
+          uint32_t lo16[16], hi16[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            lo16[t] = __float_as_uint(__uint_as_float(rr[t]) * alpha);
+            hi16[t] = __float_as_uint(__uint_as_float(rr[16 + t]) * alpha);
+          }
+          tmem_st16(tmem + lane_off + C::kTmemO + c * 32, lo16);
+          tmem_st16(tmem + lane_off + C::kTmemO + c * 32 + 16, hi16);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[jt & 1]);
+    }
+    // ------------------------------------------------------------ epilogue
+    // PV(n-2) may still be in flight here (the rescale wait is conditional), so
+    // complete the phases in order: a parity wait cannot tell phase n-1 from n-3.
+    if (ok && n_kv > 1) ok = mbar_wait_warp(&o_done, (n_kv - 2) & 1u, ab);
+    if (ok && n_kv > 0) ok = mbar_wait_warp(&o_done, (n_kv - 1) & 1u, ab);
+    if (ok) {
+      tc_fence_after();
+      const bool valid = i < sq.lq;
+      const bool keyless = !(l_run > 0.0f);
+      const float inv_l = keyless ? 0.0f : 1.0f / l_run;
+      const int64_t tok = (int64_t)sq.q_start + i;
+      if (valid && split == 0)
+        p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + tok] =
+            keyless ? -INFINITY : (m_run + __log2f(l_run)) * 0.69314718055994530942f;
+      char* orow = (char*)p.o +
+                   ((int64_t)b * p.so_b + tok * p.so_t + (int64_t)h * p.so_h +
+                    (int64_t)split * DV_CTA) *
+                       (O_F32 ? 4 : 2);
+#pragma unroll
+      for (int c = 0; c < DV_CTA / 32; ++c) {
+        uint32_t rr[32];
+        if (n_kv > 0) {
+          tmem_ld32(tmem + lane_off + C::kTmemO + c * 32, rr);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) rr[t] = 0u;
+        }
+        if (valid) {
+          if (O_F32) {
+            float4* dst = reinterpret_cast<float4*>(orow + c * 32 * 4);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              dst[t] = make_float4(__uint_as_float(rr[4 * t]) * inv_l,
+                                   __uint_as_float(rr[4 * t + 1]) * inv_l,
+                                   __uint_as_float(rr[4 * t + 2]) * inv_l,
+                                   __uint_as_float(rr[4 * t + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32 * 2);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              uint4 v;
+              v.x = Pack<BF16>::two(__uint_as_float(rr[8 * t + 0]) * inv_l,
+                                    __uint_as_float(rr[8 * t + 1]) * inv_l);
+              v.y = Pack<BF16>::two(__uint_as_float(rr[8 * t + 2]) * inv_l,
+                                    __uint_as_float(rr[8 * t + 3]) * inv_l);
+              v.z = Pack<BF16>::two(__uint_as_float(rr[8 * t + 4]) * inv_l,
+                                    __uint_as_float(rr[8 * t + 5]) * inv_l);
+              v.w = Pack<BF16>::two(__uint_as_float(rr[8 * t + 6]) * inv_l,
+                                    __uint_as_float(rr[8 * t + 7]) * inv_l);
+              dst[t] = v;
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------- launch
+template <int DQK, int DV_CTA, bool BF16, bool O_F32>
+static cudaError_t launch_fwd_t(const FwdParams& p, dim3 grid, cudaStream_t st) {
+  using C = FwdCfg<DQK, DV_CTA, BF16, O_F32>;
+  auto k = attn_fwd_kernel<DQK, DV_CTA, BF16, O_F32>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, 256, C::kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DQK, int DV_CTA>
+static cudaError_t launch_fwd_d(const FwdParams& p, dim3 grid, bool bf16, bool of32,
+                                cudaStream_t st) {
+  if (bf16)
+    return of32 ? launch_fwd_t<DQK, DV_CTA, true, true>(p, grid, st)
+                : launch_fwd_t<DQK, DV_CTA, true, false>(p, grid, st);
+  return of32 ? launch_fwd_t<DQK, DV_CTA, false, true>(p, grid, st)
+              : launch_fwd_t<DQK, DV_CTA, false, false>(p, grid, st);
+}
+
+// Returns cudaErrorNotSupported for head dims without an instantiation.
+cudaError_t launch_fwd(const FwdParams& p, int dqk, int dv, bool bf16, bool o_f32,
+                       cudaStream_t st) {
+  const int nsplit = dv > 256 ? dv / 256 : 1;
+  if (p.n_split != nsplit) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)(p.hq * nsplit), (unsigned)p.n_qtiles, (unsigned)p.batch);
+  if (dqk == 64 && dv == 64) return launch_fwd_d<64, 64>(p, grid, bf16, o_f32, st);
+  if (dqk == 128 && dv == 128) return launch_fwd_d<128, 128>(p, grid, bf16, o_f32, st);
+  if (dqk == 192 && dv == 128) return launch_fwd_d<192, 128>(p, grid, bf16, o_f32, st);
+  if (dqk == 256 && dv == 256) return launch_fwd_d<256, 256>(p, grid, bf16, o_f32, st);
+  if (dqk == 512 && dv == 512) return launch_fwd_d<512, 256>(p, grid, bf16, o_f32, st);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace attn

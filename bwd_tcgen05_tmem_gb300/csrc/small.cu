@@ -1,0 +1,173 @@
+// small.cu -- the memory-bound kernels of the attention path:
+//   * attn_pre_kernel:   D[b,h,i] = sum_c dO[i,h,c] * O[i,h,c] in FP32
+//                        (TransformerEngine PR #3699: the backward helper chain);
+//   * attn_merge_kernel: LSE-weighted merge of partial results
+//                        (PR #3527: the context-parallel ring correction);
+//   * attn_check_kernel: device validation of cu_seqlens (PR #3699: every
+//                        execution checks the packed-layout metadata on device).
+#include "kcommon.cuh"
+#include "small_params.h"
+
+namespace attn {
+
+// ----------------------------------------------------------------- D = rowsum(dO * O)
+// One warp per (token, head) row; each lane reads 16-byte vectors of O and dO.
+template <bool BF16>
+__global__ void __launch_bounds__(256) attn_pre_kernel(const PreParams p) {
+  if (p.status && *(volatile int*)p.status) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)(p.cu_q ? p.total_q : p.batch * p.seqlen_q) * p.hq;
+  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = warp_id; r < rows; r += nwarps) {
+    const int h = (int)(r % p.hq);
+    const int64_t t = r / p.hq;  // token (dense: b*S + i)
+    int b;
+    int64_t tok;
+    if (p.cu_q) {
+      // binary search for the sequence that owns token t
+      int lo = 0, hi = p.batch;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.cu_q[mid] <= t) lo = mid; else hi = mid;
+      }
+      b = lo;
+      tok = t;
+    } else {
+      b = (int)(t / p.seqlen_q);
+      tok = t % p.seqlen_q;
+    }
+    const uint16_t* orow = (const uint16_t*)p.o + (int64_t)b * p.so_b * (p.cu_q ? 0 : 1) +
+                           tok * p.so_t + (int64_t)h * p.so_h;
+    const uint16_t* drow = (const uint16_t*)p.dout + (int64_t)b * p.sdo_b * (p.cu_q ? 0 : 1) +
+                           tok * p.sdo_t + (int64_t)h * p.sdo_h;
+    float acc = 0.0f;
+    for (int c = lane * 8; c < p.dv; c += 256) {
+      const uint4 ov = *reinterpret_cast<const uint4*>(orow + c);
+      const uint4 dv = *reinterpret_cast<const uint4*>(drow + c);
+      const uint16_t* oe = reinterpret_cast<const uint16_t*>(&ov);
+      const uint16_t* de = reinterpret_cast<const uint16_t*>(&dv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(Pack<BF16>::to_f(oe[e]), Pack<BF16>::to_f(de[e]), acc);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok] = acc;
+  }
+}
+
+cudaError_t launch_pre(const PreParams& p, bool bf16, int num_sms, cudaStream_t st) {
+  const int64_t rows = (int64_t)(p.cu_q ? p.total_q : p.batch * p.seqlen_q) * p.hq;
+  int64_t blocks = (rows + 7) / 8;
+  const int64_t cap = (int64_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (bf16)
+    attn_pre_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(p);
+  else
+    attn_pre_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------- LSE merge
+// One warp per (row, head); each lane owns 4 consecutive value columns per step.
+__global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ MergeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t total = p.rows * p.heads;
+  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t w = warp_id; w < total; w += nwarps) {
+    const int64_t r = w / p.heads;
+    const int h = (int)(w % p.heads);
+    // maximum over the parts covering this row
+    float m = -INFINITY;
+    for (int q = 0; q < p.n; ++q) {
+      const int64_t lr = r - p.row0[q];
+      if (lr < 0 || lr >= p.nrows[q]) continue;
+      m = fmaxf(m, p.lse[q][(int64_t)h * p.nrows[q] + lr]);
+    }
+    float sum = 0.0f;
+    if (m != -INFINITY) {
+      for (int q = 0; q < p.n; ++q) {
+        const int64_t lr = r - p.row0[q];
+        if (lr < 0 || lr >= p.nrows[q]) continue;
+        const float l = p.lse[q][(int64_t)h * p.nrows[q] + lr];
+        if (l != -INFINITY) sum += __expf(l - m);
+      }
+    }
+    const float lse = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
+    if (lane == 0) p.lse_out[(int64_t)h * p.rows + r] = lse;
+    for (int c = lane * 4; c < p.dv; c += 128) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (m != -INFINITY) {
+        for (int q = 0; q < p.n; ++q) {
+          const int64_t lr = r - p.row0[q];
+          if (lr < 0 || lr >= p.nrows[q]) continue;
+          const float l = p.lse[q][(int64_t)h * p.nrows[q] + lr];
+          if (l == -INFINITY) continue;
+          const float a = __expf(l - lse);
+          const float4 v =
+              *reinterpret_cast<const float4*>(p.o[q] + (lr * p.heads + h) * (int64_t)p.dv + c);
+          acc.x = fmaf(a, v.x, acc.x);
+          acc.y = fmaf(a, v.y, acc.y);
+          acc.z = fmaf(a, v.z, acc.z);
+          acc.w = fmaf(a, v.w, acc.w);
+        }
+      }
+      const int64_t off = (r * p.heads + h) * (int64_t)p.dv + c;
+      if (p.out_kind == 2) {
+        *reinterpret_cast<float4*>((float*)p.o_out + off) = acc;
+      } else {
+        uint2 pk;
+        if (p.out_kind == 0) {
+          pk.x = Pack<true>::two(acc.x, acc.y);
+          pk.y = Pack<true>::two(acc.z, acc.w);
+        } else {
+          pk.x = Pack<false>::two(acc.x, acc.y);
+          pk.y = Pack<false>::two(acc.z, acc.w);
+        }
+        *reinterpret_cast<uint2*>((uint16_t*)p.o_out + off) = pk;
+      }
+    }
+  }
+}
+
+cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t st) {
+  const int64_t total = p.rows * p.heads;
+  int64_t blocks = (total + 7) / 8;
+  const int64_t cap = (int64_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  attn_merge_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------- cu_seqlens check
+// Single block.  Sets *status = DEV_BAD_SEQLENS unless, for both q and k:
+// cu[0] == 0, cu non-decreasing, every length <= the declared maximum and
+// cu[batch] == the declared total.
+__global__ void __launch_bounds__(256) attn_check_kernel(const CheckParams p) {
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  int local = 0;
+  for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
+    const int lq = p.cu_q[b + 1] - p.cu_q[b];
+    const int lk = p.cu_k[b + 1] - p.cu_k[b];
+    if (lq < 0 || lq > p.max_q || lk < 0 || lk > p.max_k) local = 1;
+  }
+  if (threadIdx.x == 0) {
+    if (p.cu_q[0] != 0 || p.cu_k[0] != 0) local = 1;
+    if (p.cu_q[p.batch] != p.total_q || p.cu_k[p.batch] != p.total_k) local = 1;
+  }
+  if (local) atomicOr(&bad, 1);
+  __syncthreads();
+  if (threadIdx.x == 0 && bad) atomicExch(p.status, DEV_BAD_SEQLENS);
+}
+
+cudaError_t launch_check(const CheckParams& p, cudaStream_t st) {
+  attn_check_kernel<<<1, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

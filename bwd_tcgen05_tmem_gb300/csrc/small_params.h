@@ -1,0 +1,44 @@
+// small_params.h -- parameter blocks and launchers of the memory-bound kernels
+// (D preprocess, LSE merge, cu_seqlens check) defined in small.cu.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+struct PreParams {
+  const void* o;
+  const void* dout;
+  float* d;             // D in the LSE layout
+  const int32_t* cu_q;  // null: dense
+  int64_t so_b, so_t, so_h, sdo_b, sdo_t, sdo_h;
+  int64_t d_sb, d_sh;   // D index = b*d_sb + h*d_sh + token
+  int batch, seqlen_q, total_q, hq, dv;
+  int* status;
+};
+
+constexpr int kMaxParts = 64;
+struct MergeParams {
+  const float* o[kMaxParts];
+  const float* lse[kMaxParts];
+  int64_t row0[kMaxParts], nrows[kMaxParts];
+  int n;
+  int64_t rows;
+  int heads, dv;
+  void* o_out;
+  float* lse_out;
+  int out_kind;  // 0 bf16, 1 fp16, 2 fp32
+};
+
+struct CheckParams {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int batch, max_q, max_k, total_q, total_k;
+  int* status;
+};
+
+cudaError_t launch_pre(const PreParams& p, bool bf16, int num_sms, cudaStream_t st);
+cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t st);
+cudaError_t launch_check(const CheckParams& p, cudaStream_t st);
+
+}  // namespace attn

@@ -1,0 +1,181 @@
+/*
+ * attn.h -- C ABI of libattn.so: fused causal scaled-dot-product attention
+ * (forward, backward, LSE merge) for NVIDIA GB300 (sm_103a).
+ *
+ * Sources for the operations (web pages on Blackwell attention backends):
+ *  - TransformerEngine PR #3527, "cuDNN FROST attention backend for head_dim in
+ *    (256, 512], with context parallelism": forward with a natural-log FP32
+ *    log-sum-exp; graphs built from each tensor's actual strides; output
+ *    buffers owned by the caller; unsupported configurations refused rather
+ *    than approximated; k/v stride agreement and GQA divisibility checks;
+ *    sliding window (left, right) with -1 unbounded and a causal mask pinning
+ *    the right bound to the diagonal; top-left / bottom-right causal alignment;
+ *    the stream bound per call; a context-parallel ring merging partial
+ *    results through LSE differences.
+ *  - TransformerEngine PR #3699, "cuDNN FROST D128/D256 backward dispatch":
+ *    the backward helper chain (the D = rowsum(dO * O) preprocess, gradient
+ *    reductions over GQA groups), per-execution device checks of cu_seqlens,
+ *    pointers / stream / workspace bound per call, exactly zero dQ on rows
+ *    that see no key.
+ *  - TransformerEngine PR #3149, "FA4 for context parallelism": packed THD
+ *    tensors addressed through cu_seqlens.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no memory and keeps no state between calls (except a
+ *    thread-local error string and a cached driver entry point).
+ *  - Work is enqueued on `stream`; calls return once it is enqueued.
+ *  - A problem the host can see (bad shape, stride, alignment, dtype, head
+ *    dim, workspace) is returned at once and nothing is launched.
+ *  - A problem only the device can see (inconsistent cu_seqlens, a wait that
+ *    exceeded its time limit) is written to the status word at the start of
+ *    the workspace; the kernels then stop early and leave the outputs
+ *    undefined.  attn_query_status() reads it.  No kernel ever traps.
+ *  - Element strides are given as {batch, token, head}; the head-dim axis is
+ *    contiguous.  Q/K/V/O/dO/dQ/dK/dV may each have their own strides.
+ *  - Dense layout (cu_seqlens NULL): tensors are [batch][seqlen][heads][d].
+ *    Varlen THD layout (cu_seqlens set): tensors are [total][heads][d] and
+ *    sequence b owns rows [cu_seqlens[b], cu_seqlens[b+1]); the batch stride
+ *    is ignored.
+ *  - LSE is FP32 natural log.  Default layout [batch][heads_q][seqlen_q]
+ *    (dense) or [heads_q][total_q] (THD); stride_lse overrides it.
+ *  - A query row that sees no key gets O = 0, LSE = -inf and dQ = 0.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent shape */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid request this library refuses (head dim, dtype mix) */
+  ATTN_ERR_ALIGNMENT = 3,    /* pointer or stride not 16-byte aligned as required */
+  ATTN_ERR_WORKSPACE = 4,    /* workspace missing or smaller than *_workspace_size() */
+  ATTN_ERR_BAD_METADATA = 5, /* device check: cu_seqlens inconsistent (status word) */
+  ATTN_ERR_TIMEOUT = 6,      /* device wait exceeded its time limit (status word) */
+  ATTN_ERR_CUDA = 7          /* a CUDA runtime call failed; see attn_last_error() */
+} attn_status_t;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1, ATTN_FP32 = 2 } attn_dtype_t;
+
+typedef struct {
+  attn_dtype_t dtype;      /* Q, K, V, dO: ATTN_BF16 or ATTN_FP16 */
+  attn_dtype_t o_dtype;    /* O: == dtype, or ATTN_FP32 (partials for attn_lse_merge) */
+  attn_dtype_t grad_dtype; /* dQ, dK, dV: == dtype, or ATTN_FP32 */
+  int batch;               /* dense: batch size; THD: number of sequences */
+  int seqlen_q, seqlen_k;  /* dense: sequence lengths; THD: maximum lengths */
+  const int32_t* cu_seqlens_q; /* device [batch+1] prefix sums, or NULL for dense */
+  const int32_t* cu_seqlens_k; /* device [batch+1]; must be set iff cu_seqlens_q is */
+  int total_q, total_k;    /* THD: rows of the packed tensors (== cu_seqlens[batch]) */
+  int heads_q, heads_kv;   /* heads_q % heads_kv == 0; query head h uses kv head h/(hq/hkv) */
+  int d_qk, d_v;           /* (64,64) (128,128) (192,128) (256,256) (512,512) */
+  int64_t stride_q[3], stride_k[3], stride_v[3], stride_o[3]; /* {batch, token, head} */
+  int64_t stride_do[3], stride_dq[3], stride_dk[3], stride_dv[3];
+  int64_t stride_lse[2];   /* {batch, head} in elements; {0, 0} = default layout */
+  int causal;              /* 1: key j visible only if j <= i + off */
+  int bottom_right;        /* off = seqlen_k - seqlen_q (per sequence) if 1, else 0 */
+  int window_left;         /* visible only if j >= i + off - window_left; -1 unbounded */
+  int window_right;        /* visible only if j <= i + off + window_right; -1 unbounded */
+  float softmax_scale;     /* > 0, typically 1/sqrt(d_qk) */
+  int accumulate;          /* attn_bwd with grad_dtype FP32 only: 1 adds the gradients
+                              into dq/dk/dv instead of overwriting them (used to sum
+                              the partial gradients of a context-parallel ring) */
+} attn_params_t;
+
+/* Bytes of workspace attn_fwd / attn_bwd need for `p` (always >= 256: the
+ * status word lives at offset 0).  The workspace must be 256-byte aligned. */
+size_t attn_fwd_workspace_size(const attn_params_t* p);
+size_t attn_bwd_workspace_size(const attn_params_t* p);
+
+/*
+ * Forward (PR #3527): O = softmax(scale * Q K^T + mask) V per (sequence, query
+ * head) with an online softmax over 128-key tiles, and LSE = ln sum_j exp(s_ij)
+ * over visible keys.  q, k, v: dtype; o: o_dtype; lse: FP32.  The result is
+ * bitwise reproducible (no atomics, fixed reduction order).
+ * Alignment: every base pointer 16-byte aligned; every token/head/batch stride
+ * a multiple of 8 elements (16-bit tensors) or 4 (FP32 O).
+ */
+attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, const void* v,
+                       void* o, float* lse, void* workspace, size_t workspace_bytes,
+                       attn_stream_t stream);
+
+/*
+ * Backward (PR #3510 head-parallel backward, PR #3699 helper chain): from Q,
+ * K, V, O, dO and the forward's LSE computes D = rowsum(dO * O) (FP32, kept in
+ * the workspace), then per visible tile P = exp(scale QK^T - LSE),
+ * dP = dO V^T, dS = P (dP - D), dV = P^T dO, dK = scale dS^T Q,
+ * dQ = scale dS K; dK/dV are summed over the query heads of a GQA group
+ * inside the kernel.  dq/dk/dv are fully overwritten (grad_dtype).  The
+ * reduction order is fixed, so the backward is bitwise reproducible.
+ */
+attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, const void* v,
+                       const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                       void* dv, void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * The three stages of attn_bwd, callable one by one with the same arguments
+ * (attn_bwd == preprocess, then dq, then dkdv, on one stream):
+ *   attn_bwd_preprocess: D = rowsum(dO * O) into the workspace; resets the
+ *                        status word (PR #3699 "backward helper chain");
+ *   attn_bwd_dq:         dQ (reads D from the workspace);
+ *   attn_bwd_dkdv:       dK and dV, reduced over each GQA group (reads D).
+ * The dq and dkdv stages require a preprocess on the same workspace, for the
+ * same problem, earlier on the stream.  Arguments a stage does not use may be
+ * NULL.
+ */
+attn_status_t attn_bwd_preprocess(const attn_params_t* p, const void* q, const void* k,
+                                  const void* v, const void* o, const void* dout,
+                                  const float* lse, void* dq, void* dk, void* dv,
+                                  void* workspace, size_t workspace_bytes, attn_stream_t stream);
+attn_status_t attn_bwd_dq(const attn_params_t* p, const void* q, const void* k, const void* v,
+                          const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                          void* dv, void* workspace, size_t workspace_bytes,
+                          attn_stream_t stream);
+attn_status_t attn_bwd_dkdv(const attn_params_t* p, const void* q, const void* k, const void* v,
+                            const void* o, const void* dout, const float* lse, void* dq,
+                            void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                            attn_stream_t stream);
+
+/*
+ * LSE-weighted merge of partial attention results over disjoint key sets
+ * (PR #3527: the context-parallel ring correction exponentiates LSE
+ * differences):  LSE = ln sum_p exp(LSE_p),  O = sum_p exp(LSE_p - LSE) O_p,
+ * with the maximum subtracted first; a part whose LSE is -inf has weight 0 and
+ * a row with no finite part gets O = 0, LSE = -inf.
+ *   o_parts[p]:   device FP32 [part_rows[p]][heads][d_v], contiguous
+ *   lse_parts[p]: device FP32 [heads][part_rows[p]], contiguous
+ *   part part p covers output rows [part_row0[p], part_row0[p] + part_rows[p])
+ *   o_out: [rows][heads][d_v] of o_dtype (BF16, FP16 or FP32), contiguous
+ *   lse_out: [heads][rows] FP32.
+ * The pointer and range arrays are HOST arrays of n_parts entries
+ * (1 <= n_parts <= 64); d_v % 4 == 0.
+ */
+attn_status_t attn_lse_merge(int n_parts, const float* const* o_parts,
+                             const float* const* lse_parts, const int64_t* part_row0,
+                             const int64_t* part_rows, int64_t rows, int heads, int d_v,
+                             void* o_out, attn_dtype_t o_dtype, float* lse_out,
+                             attn_stream_t stream);
+
+/* Synchronises `stream` and returns the status word in `workspace`
+ * (ATTN_OK, ATTN_ERR_BAD_METADATA or ATTN_ERR_TIMEOUT). */
+attn_status_t attn_query_status(const void* workspace, attn_stream_t stream);
+
+/* Message of the last error returned on this thread ("" if none). */
+const char* attn_last_error(void);
+
+/* Number of kernels the last successful attn_fwd / attn_bwd / attn_lse_merge
+ * call on this thread enqueued. */
+int attn_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ATTN_H_ */

@@ -1,0 +1,108 @@
+"""The C-ABI library (CPU-side checks only; nothing here computes on a GPU).
+
+* libattn.so builds for sm_103a and exports every function include/attn.h
+  declares;
+* the host-side validation refuses bad requests with the documented status
+  codes before anything is launched (TransformerEngine PR #3527: unsupported
+  configurations are refused rather than approximated).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from bwd_tcgen05_tmem_gb300 import attn, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return attn.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(attn.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def fake(shape, dtype=torch.bfloat16):
+    # meta tensors give shapes and strides without memory; pointers are never used
+    return torch.empty(shape, dtype=dtype, device="meta")
+
+
+def call_fwd(lib, p, q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, ws=0x6000,
+             ws_bytes=1 << 20):
+    return lib.attn_fwd(ctypes.byref(p), ctypes.c_void_p(q), ctypes.c_void_p(k),
+                        ctypes.c_void_p(v), ctypes.c_void_p(o), ctypes.c_void_p(lse),
+                        ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def base_params(**kw):
+    q = fake((2, 256, 4, 128))
+    k = fake((2, 256, 2, 128))
+    v = fake((2, 256, 2, 128))
+    o = fake((2, 256, 4, 128))
+    return attn.make_params(q, k, v, o=o, **kw)
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (lambda p: setattr(p, "d_qk", 96), 2),            # unsupported head dim
+    (lambda p: setattr(p, "d_qk", 100), 1),           # not a multiple of 8
+    (lambda p: setattr(p, "heads_kv", 3), 1),         # GQA divisibility
+    (lambda p: setattr(p, "window_left", -2), 1),     # window must be >= -1
+    (lambda p: setattr(p, "softmax_scale", 0.0), 1),  # scale must be positive
+    (lambda p: setattr(p, "dtype", 2), 2),            # FP32 inputs refused
+    (lambda p: setattr(p, "o_dtype", 1), 2),          # O dtype mix refused
+    (lambda p: p.stride_q.__setitem__(1, 4 * 128 + 4), 3),  # stride not 16-byte multiple
+])
+def test_validation_refuses(lib, mutate, code):
+    p = base_params()
+    mutate(p)
+    assert call_fwd(lib, p) == code
+    assert lib.attn_last_error()
+
+
+def test_misaligned_pointer_and_workspace(lib):
+    p = base_params()
+    assert call_fwd(lib, p, q=0x1008) == 3
+    assert call_fwd(lib, p, ws=0) == 4
+    assert call_fwd(lib, p, ws_bytes=16) == 4
+    assert call_fwd(lib, p, ws=0x6010) == 3
+
+
+def test_output_overlapping_input_refused(lib):
+    p = base_params()
+    assert call_fwd(lib, p, o=0x1000) == 1
+
+
+def test_workspace_sizes(lib):
+    p = base_params()
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) >= 256
+    need = lib.attn_bwd_workspace_size(ctypes.byref(p))
+    assert need >= 256 + 2 * 4 * 256 * 4  # status word + D for every query row
+
+
+def test_merge_validation(lib):
+    n = 2
+    vp = (ctypes.c_void_p * n)(0x1000, 0x2000)
+    lp = (ctypes.c_void_p * n)(0x3000, 0x4000)
+    r0 = (ctypes.c_int64 * n)(0, 5)
+    nr = (ctypes.c_int64 * n)(10, 10)  # second part exceeds rows
+    rc = lib.attn_lse_merge(n, vp, lp, r0, nr, 12, 2, 64, ctypes.c_void_p(0x9000), 0,
+                            ctypes.c_void_p(0xA000), None)
+    assert rc == 1
+    rc = lib.attn_lse_merge(0, vp, lp, r0, nr, 12, 2, 64, ctypes.c_void_p(0x9000), 0,
+                            ctypes.c_void_p(0xA000), None)
+    assert rc == 1

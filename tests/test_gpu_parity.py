@@ -1,0 +1,179 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle.
+
+Sizes span several 128-row tiles with a ragged tail; cases cover every head
+dim pair, MHA and GQA, BF16 and FP16, dense and packed THD (with empty and
+one-token documents), causal top-left / bottom-right, sliding windows,
+non-causal attention and rows that see no key.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from bwd_tcgen05_tmem_gb300 import attn, synth
+from parity import Reference, check_lse, gate, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from bwd_tcgen05_tmem_gb300 import build
+    build.build()
+    attn.load()
+
+
+def dense_inputs(b, sq, sk, hq, hkv, dqk, dv, dtype):
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
+    q = synth.normal((b, sq, hq, dqk), synth.SEED_Q, dt)
+    k = synth.normal((b, sk, hkv, dqk), synth.SEED_K, dt)
+    v = synth.normal((b, sk, hkv, dv), synth.SEED_V, dt)
+    do = synth.normal((b, sq, hq, dv), synth.SEED_DO, dt)
+    return q, k, v, do
+
+
+def run_and_check(q, k, v, do, *, dtype, causal=True, window=(-1, -1), bottom_right=False,
+                  cu=None, max_len=None, backward=True):
+    scale = 1.0 / math.sqrt(q.shape[-1])
+    dev = "cuda"
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    kw = dict(causal=causal, scale=scale, window=window, bottom_right=bottom_right)
+    if cu is not None:
+        cud = cu.to(dev)
+        kw.update(cu_seqlens_q=cud, cu_seqlens_k=cud, max_seqlen_q=max_len, max_seqlen_k=max_len)
+    o, lse = attn.fwd(qd, kd, vd, **kw)
+    torch.cuda.synchronize()
+    ref = Reference(q, k, v, do if backward else None, causal=causal, scale=scale,
+                    window=window, bottom_right=bottom_right, cu_q=cu, cu_k=cu, dtype=dtype)
+    report = {}
+    gate("o", o, ref.o, ref.floor["o"], report)
+    check_lse(lse, ref.lse)
+    if backward:
+        dq, dk, dv = attn.bwd(qd, kd, vd, o, dod, lse, **kw)
+        torch.cuda.synchronize()
+        for name, got, ex in (("dq", dq, ref.dq), ("dk", dk, ref.dk), ("dv", dv, ref.dv)):
+            gate(name, got, ex, ref.floor[name], report)
+            rel_l2(name, got, ex)
+    return report
+
+
+DENSE = [
+    # b, sq, sk, hq, hkv, dqk, dv, dtype, causal, window, bottom_right
+    (2, 300, 300, 2, 2, 64, 64, "bf16", True, (-1, -1), False),
+    (2, 300, 300, 2, 2, 128, 128, "bf16", True, (-1, -1), False),
+    (2, 300, 300, 2, 2, 192, 128, "bf16", True, (-1, -1), False),
+    (1, 300, 300, 2, 2, 256, 256, "bf16", True, (-1, -1), False),
+    (2, 300, 300, 8, 2, 128, 128, "fp16", True, (-1, -1), False),
+    (1, 300, 300, 6, 2, 192, 128, "fp16", True, (-1, -1), False),
+    (1, 400, 400, 4, 1, 256, 256, "bf16", True, (100, 0), False),
+    (1, 200, 333, 2, 2, 128, 128, "bf16", True, (-1, -1), True),
+    (1, 333, 200, 2, 2, 128, 128, "bf16", True, (-1, -1), True),
+    (1, 300, 300, 2, 2, 128, 128, "bf16", False, (-1, -1), False),
+    (1, 300, 300, 2, 2, 64, 64, "bf16", False, (30, 20), False),
+    (1, 130, 130, 2, 2, 64, 64, "bf16", True, (0, 0), False),
+]
+
+
+@pytest.mark.parametrize("case", DENSE, ids=lambda c: f"b{c[0]}q{c[1]}k{c[2]}h{c[3]}/{c[4]}d{c[5]}-{c[6]}{c[7]}c{int(c[8])}w{c[9][0]}br{int(c[10])}")
+def test_dense(case):
+    b, sq, sk, hq, hkv, dqk, dv, dtype, causal, window, br = case
+    q, k, v, do = dense_inputs(b, sq, sk, hq, hkv, dqk, dv, dtype)
+    run_and_check(q, k, v, do, dtype=dtype, causal=causal, window=window, bottom_right=br)
+
+
+def test_dense_d512_forward():
+    q, k, v, do = dense_inputs(1, 260, 260, 4, 1, 512, 512, "bf16")
+    run_and_check(q, k, v, do, dtype="bf16", backward=False)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("dims", [(128, 128), (192, 128), (64, 64)])
+def test_thd_varlen(dtype, dims):
+    lens = [0, 1, 129, 300, 64, 200, 0]
+    w = synth.Workload("t", 0, 0, 8, 2, dims[0], dims[1], dtype=dtype, thd_total=1)
+    inp = synth.make_inputs(w, lengths=lens)
+    run_and_check(inp["q"], inp["k"], inp["v"], inp["dout"], dtype=dtype,
+                  cu=inp["cu_seqlens"], max_len=inp["max_seqlen"])
+
+
+def test_forward_bitwise_reproducible_and_stream_bound():
+    q, k, v, _ = dense_inputs(1, 700, 700, 4, 4, 192, 128, "bf16")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = attn.fwd(qd, kd, vd)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        outs = [attn.fwd(qd, kd, vd) for _ in range(5)]
+    torch.cuda.synchronize()
+    for o2, l2 in outs:
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_backward_bitwise_reproducible():
+    q, k, v, do = dense_inputs(1, 500, 500, 4, 2, 128, 128, "bf16")
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = attn.fwd(qd, kd, vd)
+    g1 = attn.bwd(qd, kd, vd, o, dod, lse)
+    g2 = attn.bwd(qd, kd, vd, o, dod, lse)
+    torch.cuda.synchronize()
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_causal_row0_is_v0_exactly():
+    q, k, v, _ = dense_inputs(2, 257, 257, 4, 4, 128, 128, "bf16")
+    o, lse = attn.fwd(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(o[:, 0].cpu(), v[:, 0])
+    ref = (q[:, 0].double() * k[:, 0].double()).sum(-1) / math.sqrt(128)
+    assert torch.allclose(lse[:, :, 0].cpu().double(), ref, atol=1e-4, rtol=0)
+
+
+def test_outputs_fully_overwritten():
+    q, k, v, do = dense_inputs(1, 300, 300, 2, 2, 128, 128, "bf16")
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o = torch.full((1, 300, 2, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((1, 2, 300), float("nan"), device="cuda")
+    attn.fwd(qd, kd, vd, out=o, lse=lse)
+    dq = torch.full_like(qd, float("nan"))
+    dk = torch.full_like(kd, float("nan"))
+    dv = torch.full_like(vd, float("nan"))
+    attn.bwd(qd, kd, vd, o, dod, lse, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t).all()
+
+
+def test_keyless_rows_exact_zero():
+    q, k, v, do = dense_inputs(1, 300, 100, 2, 2, 128, 128, "bf16")
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = attn.fwd(qd, kd, vd, bottom_right=True)
+    dq, dk, dv = attn.bwd(qd, kd, vd, o, dod, lse, bottom_right=True)
+    torch.cuda.synchronize()
+    assert torch.all(o[:, :200] == 0)
+    assert torch.all(torch.isneginf(lse[:, :, :200]))
+    assert torch.all(dq[:, :200] == 0)
+
+
+def test_fp32_partial_output_matches():
+    q, k, v, _ = dense_inputs(1, 300, 300, 2, 2, 192, 128, "bf16")
+    o16, l16 = attn.fwd(q.cuda(), k.cuda(), v.cuda())
+    o32, l32 = attn.fwd(q.cuda(), k.cuda(), v.cuda(), o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(l16, l32)
+    assert torch.equal(o32.to(torch.bfloat16), o16)
+
+
+def test_bad_cu_seqlens_reports_status():
+    q = torch.zeros(64, 2, 128, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 10, 5, 64], dtype=torch.int32, device="cuda")  # not monotone
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    o = torch.empty(64, 2, 128, dtype=torch.bfloat16, device="cuda")
+    attn.fwd(q, q, q, cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=64, max_seqlen_k=64,
+             out=o, workspace=ws)
+    with pytest.raises(attn.AttnError) as e:
+        attn.query_status(ws)
+    assert e.value.code == 5
