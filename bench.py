@@ -1,0 +1,431 @@
+"""Benchmark: causal attention forward + backward at 32K tokens on GB300.
+
+One step = the whole attention path on one batch: attn_fwd, then the three
+stages of attn_bwd (D preprocess, dQ, dK/dV) -- exactly the work of
+attn_fwd + attn_bwd -- on device-resident inputs, timed with CUDA events on
+the launching stream (events between the stages give per-kernel times).
+Inputs (Q 384 MiB, K 384 MiB, V/dO 256 MiB) exceed the 129 MB L2, so no flush
+is needed between steps.
+
+Reported: TFLOP/s of the algorithmic work (visible causal pairs only:
+fwd 2*N*(dqk+dv), bwd 2*N*(3*dqk+2*dv)), ms per step, % of the dense BF16
+tensor peak, an end-to-end figure through host buffers, the roofline of the
+dominant kernel, and the FP64 oracle on a bounded sample as the CPU baseline.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Multi-GPU (torchrun): every rank runs its own copy of the workload (weak
+scaling, no collective in the data path); time = max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "b1_h32_s32768_d192_128"
+METRIC = "causal attn fwd+bwd ms & TFLOP/s at 32K seq, % of GB300 BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {"fwd": "fwd.cu", "dq": "bwd_dq.cu", "dkdv": "bwd_dkdv.cu", "pre": "small.cu"}
+
+
+def visible_pairs(w, lengths=None):
+    """Sum over sequences and query heads of visible (query, key) pairs."""
+    lens = lengths if lengths is not None else w.lengths()
+    n = 0
+    for L in lens:
+        if w.window[0] >= 0:
+            W = w.window[0] + 1
+            n += sum(min(i + 1, W) for i in range(L))
+        else:
+            n += L * (L + 1) // 2
+    return n * w.heads_q
+
+
+def flops(w, lengths=None):
+    nv = visible_pairs(w, lengths)
+    fwd = 2 * nv * (w.d_qk + w.d_v)
+    bwd = 2 * nv * (3 * w.d_qk + 2 * w.d_v)
+    # per-kernel attribution of the algorithmic work (sums to fwd + bwd):
+    # dK/dV kernel: S, dP, dV, dK; dQ kernel: dQ (its S/dP recompute is not credited)
+    return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd, "n_visible": nv,
+            "kernel": {"fwd": fwd, "dkdv": 2 * nv * (2 * w.d_qk + 2 * w.d_v),
+                       "dq": 2 * nv * w.d_qk}}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def file_hash(name):
+    p = os.path.join(ROOT, "bwd_tcgen05_tmem_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    if there is none or the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == kernel and not line.startswith("#"):
+                if parts[2] != file_hash(KERNEL_SOURCES[kernel]):
+                    return None
+                return float(parts[1])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.close()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    p = [x.strip() for x in line.split(",")]
+                    if len(p) >= 9:
+                        rows.append(p)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_median": statistics.median([num(r[3]) for r in rows
+                                                     if num(r[3]) is not None] or [0])}
+
+
+def cpu_baseline(w, seconds_target=15.0):
+    """The FP64 oracle, as it stands, on a bounded sample of the workload: the
+    last `rows` query rows of every head against every key (bottom-right
+    causal), forward + backward.  Returns TFLOP/s of the sample's algorithmic
+    work.  The oracle runs one thread per (sequence, head) work item."""
+    import oracle
+    from bwd_tcgen05_tmem_gb300 import synth
+    S = w.seqlen
+    ncpu = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    nthreads = min(ncpu, w.heads_q)
+    q = synth.normal((1, S, w.heads_q, w.d_qk), synth.SEED_Q, w.torch_dtype)[0]
+    k = synth.normal((1, S, w.heads_kv, w.d_qk), synth.SEED_K, w.torch_dtype)[0]
+    v = synth.normal((1, S, w.heads_kv, w.d_v), synth.SEED_V, w.torch_dtype)[0]
+    do = synth.normal((1, S, w.heads_q, w.d_v), synth.SEED_DO, w.torch_dtype)[0]
+    k, v = (t.double().numpy() for t in (k, v))
+
+    def run(rows):
+        qs = q[S - rows:].double().numpy()
+        dos = do[S - rows:].double().numpy()
+        t0 = time.perf_counter()
+        oracle.fwd(qs, k, v, [0, rows], [0, S], scale=w.scale, causal=True, bottom_right=True,
+                   nthreads=nthreads)
+        oracle.bwd(qs, k, v, dos, [0, rows], [0, S], scale=w.scale, causal=True,
+                   bottom_right=True, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        nv = w.heads_q * sum(S - rows + i + 1 for i in range(rows))
+        return dt, 2 * nv * (w.d_qk + w.d_v) + 2 * nv * (3 * w.d_qk + 2 * w.d_v)
+
+    rows = 4
+    dt, f = run(rows)
+    while dt < 1.0 and rows < S:
+        rows = min(S, rows * 4)
+        dt, f = run(rows)
+    if dt < seconds_target and rows < S:
+        rows = min(S, max(rows, int(rows * seconds_target / dt)))
+        dt, f = run(rows)
+    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"FP64 oracle fwd+bwd of the last {rows} query rows of all "
+                      f"{w.heads_q} heads (bottom-right causal against all {S} keys), "
+                      f"{nthreads} threads of {ncpu} host cores"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    samples = []
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(w, seconds_target=5.0)
+        if i >= args.warmup:
+            samples.append(cb)
+    val = statistics.median(s["value"] for s in samples)
+    fl = flops(w)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": fl["total"] / (val * 1e12) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seqlen,
+                   "heads": w.heads_q, "d_qk": w.d_qk, "d_v": w.d_v, "causal": True},
+        "cpu_baseline": {**samples[-1], "value": val},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "note": "the reference arm is the FP64 CPU oracle timed on a bounded sample; "
+                "ms_per_step is extrapolated to the whole workload",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cp", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from bwd_tcgen05_tmem_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from bwd_tcgen05_tmem_gb300 import attn
+
+    inp = synth.make_inputs(w)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "dout"))
+    fl = flops(w)
+    o = torch.empty((*q.shape[:-1], w.d_v), dtype=q.dtype, device=dev)
+    lse = torch.empty((q.shape[0], w.heads_q, q.shape[1]), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fws = torch.empty(attn.workspace_size("fwd", q, k, v), dtype=torch.uint8, device=dev)
+    bws = torch.empty(attn.workspace_size("bwd", q, k, v), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    kw = dict(causal=True, scale=w.scale, window=w.window)
+    stages = ("fwd", "pre", "dq", "dkdv")
+
+    def step(ev=None):
+        n = 0
+        if ev:
+            ev[0].record(stream)
+        attn.fwd(q, k, v, out=o, lse=lse, workspace=fws, **kw)
+        n += attn.last_launch_count()
+        for i, st in enumerate(("preprocess", "dq", "dkdv")):
+            if ev:
+                ev[i + 1].record(stream)
+            attn.bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=bws, stage=st, **kw)
+            n += attn.last_launch_count()
+        if ev:
+            ev[4].record(stream)
+        return n
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    attn.query_status(bws)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for s in range(args.steps):
+            launches += step(events[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    attn.query_status(bws)
+    total_ms = t0.elapsed_time(t1)
+    per_kernel = {st: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in events)
+                  for i, st in enumerate(stages)}
+    ms = total_ms / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = tt.item()
+    clocks = clk.summary()
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for d, h in zip((q, k, v, do), host_in):
+            d.copy_(h, non_blocking=True)
+        attn.fwd(q, k, v, out=o, lse=lse, workspace=fws, **kw)
+        attn.bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=bws, **kw)
+        for h, d in zip(host_out, (o, lse, dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+
+    e2e_steps = max(2, min(args.steps, 5))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = tt.item()
+
+    # ---- one-GPU context-parallel ring emulation (dual chunk swap, 8 ranks)
+    cp_obj = None
+    if not args.no_cp and w.batch == 1 and w.seqlen % 16 == 0:
+        from bwd_tcgen05_tmem_gb300 import cp as cpmod
+        ring = cpmod.CPRing(q, k, v, do, cp=8, scale=w.scale)
+        for _ in range(2):
+            ring.forward()
+            ring.backward()
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c2 = torch.cuda.Event(enable_timing=True)
+        n_cp = 3
+        fwd_ms = bwd_ms = 0.0
+        for _ in range(n_cp):
+            c0.record(stream)
+            ring.forward()
+            c1.record(stream)
+            ring.backward()
+            c2.record(stream)
+            torch.cuda.synchronize()
+            fwd_ms += c0.elapsed_time(c1) / n_cp
+            bwd_ms += c1.elapsed_time(c2) / n_cp
+        cp_obj = {"cp": 8, "chunks": 16, "chunk_tokens": w.seqlen // 16,
+                  "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "ms": fwd_ms + bwd_ms,
+                  "tflops": fl["total"] / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
+                  "launches": ring.launches,
+                  "note": "partials per ring step (FP32) + LSE merge per rank + per-step "
+                          "backward with FP32 accumulation, all ranks on this GPU"}
+        del ring
+
+    peaks, peak_src = load_peaks()
+    peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    dom = max(("fwd", "dq", "dkdv"), key=lambda s: per_kernel[s])
+    ach = fl["kernel"][dom] / (per_kernel[dom] * 1e-3) / 1e12
+    traffic = load_traffic(dom)
+    value = world * fl["total"] / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch * world, "seq_len": w.seqlen,
+                   "heads": w.heads_q, "heads_kv": w.heads_kv, "d_qk": w.d_qk, "d_v": w.d_v,
+                   "causal": True, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "pct_of_peak": 100.0 * (value / world) / peak_tf,
+        "peak_tflops": peak_tf,
+        "peak_source": f"{peak_src} (bf16 sustained)",
+        "tflops_fwd": fl["fwd"] / (per_kernel["fwd"] * 1e-3) / 1e12,
+        "tflops_bwd": fl["bwd"] / ((per_kernel["pre"] + per_kernel["dq"] + per_kernel["dkdv"])
+                                   * 1e-3) / 1e12,
+        "kernel_ms": {k_: round(v_, 4) for k_, v_ in per_kernel.items()},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": ach / peak_tf, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained",
+                     "work_per_launch": fl["kernel"][dom]},
+        "pre_gbs": (w.batch * w.seqlen * w.heads_q * (2 * w.d_v * 2 + 4)) /
+                   (per_kernel["pre"] * 1e-3) / 1e9,
+        "e2e": {"value": world * fl["total"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cp_emulation": cp_obj,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

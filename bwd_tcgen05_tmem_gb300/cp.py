@@ -1,0 +1,164 @@
+"""One-GPU emulation of context-parallel (CP) causal attention with the
+dual-chunk-swap load balance, forward and backward.
+
+The sequence is cut into 2*cp chunks; rank r holds chunks r and 2cp-1-r
+(TransformerEngine PR #3527: ``DUAL_CHUNK_SWAP`` CP layout).  In the p2p ring,
+at step s rank r sees the key/value chunks of rank r' = (r - s) mod cp; the
+per-step kernel window is causal ``(-1, 0)`` at step 0 and full ``(-1, -1)``
+otherwise (PR #3527 review notes on the p2p path), and the partial results are
+combined through their LSE (the ring correction):
+
+* s = 0:   both local query chunks vs both local key chunks, causal over the
+           rank's local concatenation;
+* r' < r:  both query chunks vs key chunk r' only, full;
+* r' > r:  query chunk 2cp-1-r only vs both key chunks, full.
+
+Every rank's data lives on this one GPU, so the "exchange" of step s is the
+address of rank r''s shard; there are no collectives.  All arithmetic runs in
+the library's kernels: ``attn_fwd`` writes FP32 partials, ``attn_lse_merge``
+combines them, and ``attn_bwd`` (FP32 gradients, ``accumulate``) adds each
+step's dQ into the rank's rows and its dK/dV into the source rank's rows.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import attn
+
+
+@dataclasses.dataclass
+class Piece:
+    rank: int
+    src: int
+    q_rows: tuple   # (first, count) rows of the rank's local query shard
+    k_rows: tuple   # (first, count) rows of the source rank's local key shard
+    causal: bool
+
+
+def ring_pieces(cp: int, chunk: int):
+    """The (rank, step) pieces of the dual-chunk-swap p2p ring, per rank."""
+    out = []
+    for r in range(cp):
+        pcs = []
+        for s in range(cp):
+            src = (r - s) % cp
+            if s == 0:
+                pcs.append(Piece(r, src, (0, 2 * chunk), (0, 2 * chunk), True))
+            elif src < r:
+                pcs.append(Piece(r, src, (0, 2 * chunk), (0, chunk), False))
+            else:
+                pcs.append(Piece(r, src, (chunk, chunk), (0, 2 * chunk), False))
+        out.append(pcs)
+    return out
+
+
+def shard(x, cp):
+    """[B, S, H, d] -> list of cp local shards [B, 2c, H, d] (chunks r, 2cp-1-r)."""
+    s = x.shape[1]
+    c = s // (2 * cp)
+    assert c * 2 * cp == s, "sequence must split into 2*cp equal chunks"
+    return [torch.cat([x[:, r * c:(r + 1) * c], x[:, (2 * cp - 1 - r) * c:(2 * cp - r) * c]],
+                      dim=1).contiguous() for r in range(cp)]
+
+
+def unshard(shards, cp):
+    """Inverse of ``shard`` along dim 1."""
+    c = shards[0].shape[1] // 2
+    parts = [None] * (2 * cp)
+    for r, t in enumerate(shards):
+        parts[r] = t[:, :c]
+        parts[2 * cp - 1 - r] = t[:, c:]
+    return torch.cat(parts, dim=1)
+
+
+def unshard_lse(shards, cp):
+    """LSE shards [B, H, 2c] -> [B, H, S]."""
+    c = shards[0].shape[2] // 2
+    parts = [None] * (2 * cp)
+    for r, t in enumerate(shards):
+        parts[r] = t[:, :, :c]
+        parts[2 * cp - 1 - r] = t[:, :, c:]
+    return torch.cat(parts, dim=2)
+
+
+class CPRing:
+    """Holds per-rank shards and the buffers of one emulated CP fwd+bwd.
+
+    q/k/v/dout: dense [1, S, H, d] device tensors (batch 1, as the pages'
+    32K benchmark).  Buffers are allocated once; ``forward``/``backward`` only
+    launch kernels.
+    """
+
+    def __init__(self, q, k, v, dout, cp=8, scale=None):
+        assert q.shape[0] == 1, "the ring emulation runs batch 1"
+        self.cp = cp
+        self.scale = scale
+        self.chunk = q.shape[1] // (2 * cp)
+        self.q, self.k, self.v, self.do = (shard(t, cp) for t in (q, k, v, dout))
+        self.pieces = ring_pieces(cp, self.chunk)
+        dev = q.device
+        hq, dv = q.shape[2], v.shape[3]
+        rows = 2 * self.chunk
+        # FP32 partials per (rank, step), merged outputs, FP32 gradients per rank
+        self.o_part = [[torch.empty((1, pc.q_rows[1], hq, dv), dtype=torch.float32, device=dev)
+                        for pc in pcs] for pcs in self.pieces]
+        self.lse_part = [[torch.empty((1, hq, pc.q_rows[1]), dtype=torch.float32, device=dev)
+                          for pc in pcs] for pcs in self.pieces]
+        self.o = [torch.empty((1, rows, hq, dv), dtype=q.dtype, device=dev) for _ in range(cp)]
+        self.lse = [torch.empty((1, hq, rows), dtype=torch.float32, device=dev)
+                    for _ in range(cp)]
+        self.dq = [torch.zeros((1, rows, *q.shape[2:]), dtype=torch.float32, device=dev)
+                   for _ in range(cp)]
+        self.dk = [torch.zeros((1, rows, *k.shape[2:]), dtype=torch.float32, device=dev)
+                   for _ in range(cp)]
+        self.dv = [torch.zeros((1, rows, *v.shape[2:]), dtype=torch.float32, device=dev)
+                   for _ in range(cp)]
+        self.fwd_ws = torch.empty(256, dtype=torch.uint8, device=dev)
+        need = max(attn.workspace_size("bwd", self.q[0], self.k[0], self.v[0]), 256)
+        self.bwd_ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        self.launches = 0
+
+    def forward(self):
+        """Partials per ring step, then one LSE merge per rank."""
+        n = 0
+        for r, pcs in enumerate(self.pieces):
+            for i, pc in enumerate(pcs):
+                q0, nq = pc.q_rows
+                k0, nk = pc.k_rows
+                attn.fwd(self.q[r][:, q0:q0 + nq], self.k[pc.src][:, k0:k0 + nk],
+                         self.v[pc.src][:, k0:k0 + nk], causal=pc.causal, scale=self.scale,
+                         out=self.o_part[r][i], lse=self.lse_part[r][i],
+                         workspace=self.fwd_ws)
+                n += attn.last_launch_count()
+            attn.lse_merge([t[0] for t in self.o_part[r]], [t[0] for t in self.lse_part[r]],
+                           [pc.q_rows[0] for pc in pcs], [pc.q_rows[1] for pc in pcs],
+                           2 * self.chunk, out=self.o[r][0], lse_out=self.lse[r][0])
+            n += attn.last_launch_count()
+        self.launches = n
+        return self.o, self.lse
+
+    def backward(self):
+        """Per ring step attn_bwd with the merged LSE/O and FP32 gradients.
+
+        Step 0 of every rank covers all of its query rows and all of its own key
+        rows, so the step-0 calls (run first) overwrite every gradient element
+        and the later steps accumulate into them: no zero fill is needed."""
+        n = 0
+        rows = 2 * self.chunk
+        for s in range(self.cp):
+            for r in range(self.cp):
+                pc = self.pieces[r][s]
+                q0, nq = pc.q_rows
+                k0, nk = pc.k_rows
+                lse = self.lse[r][:, :, q0:]  # rows q0.. of the merged LSE, head stride `rows`
+                attn.bwd(self.q[r][:, q0:q0 + nq], self.k[pc.src][:, k0:k0 + nk],
+                         self.v[pc.src][:, k0:k0 + nk], self.o[r][:, q0:q0 + nq],
+                         self.do[r][:, q0:q0 + nq], lse, causal=pc.causal, scale=self.scale,
+                         dq=self.dq[r][:, q0:q0 + nq], dk=self.dk[pc.src][:, k0:k0 + nk],
+                         dv=self.dv[pc.src][:, k0:k0 + nk], grad_dtype=torch.float32,
+                         accumulate=s > 0, lse_strides=(0, rows), workspace=self.bwd_ws)
+                n += attn.last_launch_count()
+        self.launches += n
+        return self.dq, self.dk, self.dv
