@@ -31,14 +31,22 @@ struct DkvCfg {
   static constexpr int kKSlots = DQK / 64;
   static constexpr int kVSlots = kDK ? DV / 64 : 0;
   static constexpr int kResident = (kKSlots + kVSlots) * kSlotBytes;
-  static constexpr int kChunk = BQ * 128;
+  static constexpr int kChunk = BQ * 128;  // one 64-column chunk of a query tile
   static constexpr int kQCh = DQK / 64;
   static constexpr int kDoCh = DV / 64;
-  static constexpr int kPerTile = kQCh + kDoCh;
-  static constexpr int kBudget = 232448 - 1024 - (2 * BQ * 8 + 640);
-  static constexpr int kRingRaw = (kBudget - kResident) / kChunk;
-  static constexpr int kRing = kRingRaw > 24 ? 24 : kRingRaw;
-  static constexpr int kSmem = kResident + kRing * kChunk + 1024;
+  // A streamed operand that an accumulate MMA reads MN-major (Q for dK, dO
+  // for dV) is staged: a whole tile, contiguous, held until that MMA.  The
+  // other operand goes through a chunk ring released after the score MMA.
+  static constexpr bool kQStaged = kDK;
+  static constexpr bool kDStaged = kDV;
+  static constexpr int kStageBytes = (kQStaged ? kQCh : 0) * kChunk + (kDStaged ? kDoCh : 0) * kChunk;
+  static constexpr int kRingTile = (kQStaged ? 0 : kQCh) + (kDStaged ? 0 : kDoCh);  // ring chunks per tile
+  static constexpr int kStatic = 2 * BQ * 4 * (kDK ? 2 : 1) + 512;  // LSE/D staging + barriers
+  static constexpr int kBudget = 232448 - 1024 - kStatic;
+  static constexpr int kStages = (kBudget - kResident - 3 * kStageBytes >= 2 * kRingTile * kChunk) ? 3 : 2;
+  static constexpr int kRingRaw = kRingTile ? (kBudget - kResident - kStages * kStageBytes) / kChunk : 1;
+  static constexpr int kRing = kRingRaw > 12 ? 12 : kRingRaw;
+  static constexpr int kSmem = kResident + kStages * kStageBytes + kRing * kChunk + 1024;
   static constexpr int kHalf = BQ / 2;
   // TMEM columns
   static constexpr int kTS = 0;
@@ -52,16 +60,8 @@ struct DkvCfg {
   static_assert(kTEnd <= 512, "TMEM budget");
   static_assert(BQ == 64 || BQ == 128, "BQ");
   static_assert(MODE >= 1 && MODE <= 3, "MODE");
-  // Slots are assigned in load order.  dK-only loads dO(i) before Q(i) (Q is
-  // held for the dK MMA); the other modes load Q(i) first.  The score MMAs of
-  // tile i+1 are issued before the accumulate MMAs of tile i, so the chunks up
-  // to the end of the scores of tile i+1 must not reuse a slot still held by
-  // tile i.
-  static constexpr bool kDoFirst = kDK && !kDV;
-  static constexpr int kNeed = (kDK && kDV) ? 2 * kPerTile
-                               : kDK        ? kPerTile + kQCh
-                                            : kPerTile;
-  static_assert(kRing >= kNeed, "ring too small for the pipeline");
+  static_assert(kRingTile == 0 || kRing >= 2, "ring");
+  static_assert(DQK <= 256 && DV <= 256, "one MMA covers the accumulator columns");
 };
 
 template <int DQK, int DV, int BQ, int MODE, bool BF16, bool G_F32>
@@ -72,12 +72,16 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::kKSlots * kSlotBytes;
-  uint8_t* sRing = smem + C::kResident;
+  uint8_t* sStage = smem + C::kResident;          // [kStages][Q chunks | dO chunks]
+  uint8_t* sRing = sStage + C::kStages * C::kStageBytes;
+  constexpr int kQOff = 0;                                     // inside a stage
+  constexpr int kDOff = C::kQStaged ? C::kQCh * C::kChunk : 0;
 
-  __shared__ uint64_t full_bar[C::kRing], empty_bar[C::kRing];
+  __shared__ uint64_t sfull[C::kStages], sempty[C::kStages], rfull[C::kRing], rempty[C::kRing];
   __shared__ uint64_t kv_bar, sdp_full, sc_free, pds_full, acc_done, drain_bar;
   __shared__ uint64_t ld_full[2], ld_empty[2];
-  __shared__ float s_lse2[2][BQ], s_d[2][BQ];
+  __shared__ __align__(16) float s_lse2[2][BQ];
+  __shared__ __align__(16) float s_d[2][C::kDK ? BQ : 4];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, skip_sh;
 
@@ -104,9 +108,13 @@ __global__ void __launch_bounds__(384, 1)
   Abort ab{&abort_flag, p.status};
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], 1);
+    }
     for (int i = 0; i < C::kRing; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+      mbar_init(&rfull[i], 1);
+      mbar_init(&rempty[i], 1);
     }
     mbar_init(&kv_bar, 1);
     mbar_init(&sdp_full, 1);
@@ -128,16 +136,9 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  // chunk index of (iteration, which, c): Q chunks first, then dO chunks
-  auto q_idx = [&](int it, int c) {
-    return (uint32_t)(it * C::kPerTile + (C::kDoFirst ? C::kDoCh : 0) + c);
-  };
-  auto do_idx = [&](int it, int c) {
-    return (uint32_t)(it * C::kPerTile + (C::kDoFirst ? 0 : C::kQCh) + c);
-  };
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // per query tile: the ring chunks (score-only operand), then the stage
     if (elect_one_lane() && n_it > 0) {
       int c1, c2, c3;
       map_coords(p.ok, 0, g, sq.k_start + k0, tb, c1, c2, c3);
@@ -149,98 +150,162 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < C::kVSlots; ++c)
           tma_load_4d(sV + c * kSlotBytes, &p.tm_v, &kv_bar, c * 64, c1, c2, c3);
       }
-      uint32_t cnt = 0;
+      uint32_t rcnt = 0;
+      int it = 0;
       bool ok = true;
-      for (int it = 0; it < n_it && ok; ++it) {
+      for (; it < n_it && ok; ++it) {
         const int h = g * grp + it / n_qt;
         const int qrow = sq.q_start + (qt0 + it % n_qt) * BQ;
-        for (int which = 0; which < 2 && ok; ++which) {
-          const bool is_do = (which == 1) != C::kDoFirst;
-          const CUtensorMap* m = is_do ? &p.tm_do : &p.tm_q;
-          int d1, d2, d3;
-          map_coords(is_do ? p.odo : p.oq, 0, h, qrow, tb, d1, d2, d3);
-          const int nch = is_do ? C::kDoCh : C::kQCh;
-          for (int c = 0; c < nch; ++c, ++cnt) {
-            const int slot = cnt % C::kRing;
-            if (!mbar_wait(&empty_bar[slot], ((cnt / C::kRing) & 1u) ^ 1u, ab)) {
+        int qc1, qc2, qc3, dc1, dc2, dc3;
+        map_coords(p.oq, 0, h, qrow, tb, qc1, qc2, qc3);
+        map_coords(p.odo, 0, h, qrow, tb, dc1, dc2, dc3);
+        if constexpr (C::kRingTile > 0) {
+          constexpr int nch = C::kQStaged ? C::kDoCh : C::kQCh;
+          const CUtensorMap* m = C::kQStaged ? &p.tm_do : &p.tm_q;
+#pragma unroll
+          for (int c = 0; c < nch; ++c, ++rcnt) {
+            const uint32_t slot = rcnt % C::kRing;
+            if (!mbar_wait(&rempty[slot], ((rcnt / C::kRing) & 1u) ^ 1u, ab)) {
               ok = false;
               break;
             }
-            mbar_arrive_tx(&full_bar[slot], C::kChunk);
-            tma_load_4d(sRing + slot * C::kChunk, m, &full_bar[slot], c * 64, d1, d2, d3);
+            mbar_arrive_tx(&rfull[slot], C::kChunk);
+            if (C::kQStaged)
+              tma_load_4d(sRing + slot * C::kChunk, m, &rfull[slot], c * 64, dc1, dc2, dc3);
+            else
+              tma_load_4d(sRing + slot * C::kChunk, m, &rfull[slot], c * 64, qc1, qc2, qc3);
           }
+          if (!ok) break;
+        }
+        const int st = it % C::kStages;
+        if (!mbar_wait(&sempty[st], ((it / C::kStages) & 1) ^ 1, ab)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_tx(&sfull[st], C::kStageBytes);
+        uint8_t* dst = sStage + st * C::kStageBytes;
+        if constexpr (C::kQStaged) {
+#pragma unroll
+          for (int c = 0; c < C::kQCh; ++c)
+            tma_load_4d(dst + kQOff + c * C::kChunk, &p.tm_q, &sfull[st], c * 64, qc1, qc2, qc3);
+        }
+        if constexpr (C::kDStaged) {
+#pragma unroll
+          for (int c = 0; c < C::kDoCh; ++c)
+            tma_load_4d(dst + kDOff + c * C::kChunk, &p.tm_do, &sfull[st], c * 64, dc1, dc2, dc3);
         }
       }
       mbar_wait_quiet(&kv_bar, 0, kWaitLimitNs);
-      const uint32_t first = cnt > (uint32_t)C::kRing ? cnt - C::kRing : 0u;
-      for (uint32_t c = first; c < cnt; ++c)
-        mbar_wait_quiet(&full_bar[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
+      const uint32_t first = rcnt > (uint32_t)C::kRing ? rcnt - C::kRing : 0u;
+      for (uint32_t c = first; c < rcnt; ++c)
+        mbar_wait_quiet(&rfull[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
+      const int ns = ok ? n_it : it;  // stages issued
+      for (int v = ns > C::kStages ? ns - C::kStages : 0; v < ns; ++v)
+        mbar_wait_quiet(&sfull[v % C::kStages], (v / C::kStages) & 1, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_lane() && n_it > 0) {
-      const uint32_t idesc_s = make_idesc(128, BQ, BF16, false, false);
-      const uint32_t idesc_a = make_idesc(128, 64, BF16, false, true);
+      constexpr uint32_t idesc_s = make_idesc(128, BQ, BF16, false, false);
+      constexpr uint32_t idesc_v = make_idesc(128, DV, BF16, false, true);
+      constexpr uint32_t idesc_k = make_idesc(128, DQK, BF16, false, true);
+      const uint64_t kdesc = make_sdesc(smem_u32(sK), 16, 1024);
+      const uint64_t vdesc = make_sdesc(smem_u32(sV), 16, 1024);
+      const uint64_t stdesc = make_sdesc(smem_u32(sStage), 16, 1024);           // K-major view
+      const uint64_t stdesc_mn = make_sdesc(smem_u32(sStage), C::kChunk, 1024);  // MN-major view
+      const uint64_t rdesc = make_sdesc(smem_u32(sRing), 16, 1024);
+      uint32_t rcnt = 0;
       bool ok = mbar_wait(&kv_bar, 0, ab);
       tc_fence_after();
-      auto wait_chunk = [&](uint32_t idx) -> uint32_t {
-        const uint32_t slot = idx % C::kRing;
-        if (!mbar_wait(&full_bar[slot], (idx / C::kRing) & 1u, ab)) {
+      // ring chunks are consumed one by one in load order and released as soon
+      // as their score MMAs complete; the stage is held until issue_acc
+      auto ring_chunk = [&]() -> uint64_t {
+        const uint32_t slot = rcnt % C::kRing;
+        if (!mbar_wait(&rfull[slot], (rcnt / C::kRing) & 1u, ab)) {
           ok = false;
-          return 0u;
+          return 0ull;
         }
         tc_fence_after();
-        return smem_u32(sRing + slot * C::kChunk);
+        return rdesc + (uint64_t)((slot * C::kChunk) >> 4);
+      };
+      auto ring_release = [&]() {
+        mma_commit(&rempty[rcnt % C::kRing]);
+        ++rcnt;
+      };
+      // The stage of tile `it` is awaited only right before its first use:
+      // the producer loads a tile's ring chunks before its stage, so waiting
+      // for the stage first would deadlock once the ring is full.
+      auto wait_stage = [&](int it) {
+        if (!mbar_wait(&sfull[it % C::kStages], (it / C::kStages) & 1, ab)) ok = false;
+        tc_fence_after();
       };
       auto issue_scores = [&](int it) {
-        for (int c = 0; c < C::kQCh && ok; ++c) {
-          const uint32_t qb = wait_chunk(q_idx(it, c));
+        const int st = it % C::kStages;
+        const uint32_t st_off = (uint32_t)((st * C::kStageBytes) >> 4);
+        if constexpr (C::kQStaged) {
+          wait_stage(it);
           if (!ok) return;
-          const uint32_t ka = smem_u32(sK + c * kSlotBytes);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + C::kTS, make_sdesc(ka + k * 32, 16, 1024),
-                   make_sdesc(qb + k * 32, 16, 1024), idesc_s, (c | k) ? 1u : 0u);
-          if (!C::kDK) mma_commit(&empty_bar[q_idx(it, c) % C::kRing]);
         }
-        if (C::kDK) {
-          for (int c = 0; c < C::kDoCh && ok; ++c) {
-            const uint32_t db = wait_chunk(do_idx(it, c));
-            if (!ok) return;
-            const uint32_t va = smem_u32(sV + c * kSlotBytes);
+        // S^T = K Q^T
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(tmem + C::kTdP, make_sdesc(va + k * 32, 16, 1024),
-                     make_sdesc(db + k * 32, 16, 1024), idesc_s, (c | k) ? 1u : 0u);
-            if (!C::kDV) mma_commit(&empty_bar[do_idx(it, c) % C::kRing]);
+        for (int c = 0; c < C::kQCh; ++c) {
+          const uint64_t ka = kdesc + (uint64_t)(c * (kSlotBytes >> 4));
+          uint64_t qb;
+          if constexpr (C::kQStaged) {
+            qb = stdesc + st_off + (uint64_t)((kQOff + c * C::kChunk) >> 4);
+          } else {
+            qb = ring_chunk();
+            if (!ok) return;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ss(tmem + C::kTS, ka + 2 * k, qb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+          if constexpr (!C::kQStaged) ring_release();
+        }
+        // dP^T = V dO^T
+        if constexpr (C::kDK) {
+          if constexpr (C::kDStaged && !C::kQStaged) {
+            wait_stage(it);
+            if (!ok) return;
+          }
+#pragma unroll
+          for (int c = 0; c < C::kDoCh; ++c) {
+            const uint64_t va = vdesc + (uint64_t)(c * (kSlotBytes >> 4));
+            uint64_t db;
+            if constexpr (C::kDStaged) {
+              db = stdesc + st_off + (uint64_t)((kDOff + c * C::kChunk) >> 4);
+            } else {
+              db = ring_chunk();
+              if (!ok) return;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mma_ss(tmem + C::kTdP, va + 2 * k, db + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+            if constexpr (!C::kDStaged) ring_release();
           }
         }
-        if (ok) mma_commit(&sdp_full);
+        mma_commit(&sdp_full);
       };
       auto issue_acc = [&](int it) {
-        if (C::kDV) {
-          for (int c = 0; c < C::kDoCh && ok; ++c) {
-            const uint32_t db = wait_chunk(do_idx(it, c));  // already complete when dK
-            if (!ok) return;
+        const int st = it % C::kStages;
+        wait_stage(it);  // completes at once if the score MMAs already waited
+        if (!ok) return;
+        const uint32_t st_off = (uint32_t)((st * C::kStageBytes) >> 4);
+        const uint32_t first = it > 0 ? 1u : 0u;
+        if constexpr (C::kDV) {  // dV += P^T dO   (dO stage MN-major, N = DV)
+          const uint64_t db = stdesc_mn + st_off + (uint64_t)(kDOff >> 4);
+          mma_ts(tmem + C::kTdV, tmem + C::kTP, db, idesc_v, first);
 #pragma unroll
-            for (int k = 0; k < BQ / 16; ++k)
-              mma_ts(tmem + C::kTdV + c * 64, tmem + C::kTP + k * 8,
-                     make_sdesc(db + k * 2048, 16, 1024), idesc_a, (it > 0 || k > 0) ? 1u : 0u);
-            mma_commit(&empty_bar[do_idx(it, c) % C::kRing]);
-          }
+          for (int k = 1; k < BQ / 16; ++k)
+            mma_ts(tmem + C::kTdV, tmem + C::kTP + k * 8, db + k * 128, idesc_v, 1u);
         }
-        if (C::kDK) {
-          for (int c = 0; c < C::kQCh && ok; ++c) {
-            const uint32_t qb = wait_chunk(q_idx(it, c));
-            if (!ok) return;
+        if constexpr (C::kDK) {  // dK += dS^T Q   (Q stage MN-major, N = DQK)
+          const uint64_t qb = stdesc_mn + st_off + (uint64_t)(kQOff >> 4);
+          mma_ts(tmem + C::kTdK, tmem + C::kTdS, qb, idesc_k, first);
 #pragma unroll
-            for (int k = 0; k < BQ / 16; ++k)
-              mma_ts(tmem + C::kTdK + c * 64, tmem + C::kTdS + k * 8,
-                     make_sdesc(qb + k * 2048, 16, 1024), idesc_a, (it > 0 || k > 0) ? 1u : 0u);
-            mma_commit(&empty_bar[q_idx(it, c) % C::kRing]);
-          }
+          for (int k = 1; k < BQ / 16; ++k)
+            mma_ts(tmem + C::kTdK, tmem + C::kTdS + k * 8, qb + k * 128, idesc_k, 1u);
         }
-        if (ok) mma_commit(&acc_done);
+        mma_commit(&sempty[st]);
+        mma_commit(&acc_done);
       };
       if (ok) issue_scores(0);
       for (int it = 0; it < n_it && ok; ++it) {
@@ -326,19 +391,32 @@ __global__ void __launch_bounds__(384, 1)
                              ((long long)c0 >= krow_last - sq.off - sq.R) &&
                              ((long long)(c0 + C::kHalf - 1) <= (long long)k0 - sq.off + sq.L);
       const long long lo = vis_lo - c0, hi = vis_hi - c0;
+      // this warpgroup's LSE / D columns, read as 16-byte shared loads
+      const float4* l4 = reinterpret_cast<const float4*>(&s_lse2[st][col0]);
+      const float4* d4 = reinterpret_cast<const float4*>(&s_d[st][col0]);
       uint32_t pp[C::kHalf / 2], pd[C::kHalf / 2];
 #pragma unroll
-      for (int t = 0; t < C::kHalf; t += 2) {
-        float e0 = ex2(fmaf(s[t], sl2, -s_lse2[st][col0 + t]));
-        float e1 = ex2(fmaf(s[t + 1], sl2, -s_lse2[st][col0 + t + 1]));
-        if (!full_tile) {
-          if (t < lo || t > hi) e0 = 0.0f;
-          if (t + 1 < lo || t + 1 > hi) e1 = 0.0f;
+      for (int t4 = 0; t4 < C::kHalf / 4; ++t4) {
+        const float4 la = l4[t4];
+        const float lz[4] = {la.x, la.y, la.z, la.w};
+        float dz[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (C::kDK) {
+          const float4 da = d4[t4];
+          dz[0] = da.x; dz[1] = da.y; dz[2] = da.z; dz[3] = da.w;
         }
-        if constexpr (C::kDV) pp[t / 2] = Pack<BF16>::two(e0, e1);
-        if constexpr (C::kDK)
-          pd[t / 2] = Pack<BF16>::two(e0 * (dp[t] - s_d[st][col0 + t]),
-                                      e1 * (dp[t + 1] - s_d[st][col0 + t + 1]));
+#pragma unroll
+        for (int u = 0; u < 4; u += 2) {
+          const int t = 4 * t4 + u;
+          float e0 = ex2(fmaf(s[t], sl2, -lz[u]));
+          float e1 = ex2(fmaf(s[t + 1], sl2, -lz[u + 1]));
+          if (!full_tile) {
+            if (t < lo || t > hi) e0 = 0.0f;
+            if (t + 1 < lo || t + 1 > hi) e1 = 0.0f;
+          }
+          if constexpr (C::kDV) pp[t / 2] = Pack<BF16>::two(e0, e1);
+          if constexpr (C::kDK)
+            pd[t / 2] = Pack<BF16>::two(e0 * (dp[t] - dz[u]), e1 * (dp[t + 1] - dz[u + 1]));
+        }
       }
       mbar_arrive(&ld_empty[st]);
       if (it > 0 && !mbar_wait_warp(&acc_done, (it - 1) & 1u, ab)) {

@@ -25,26 +25,26 @@ template <int DQK, int DV, int BKV>
 struct DqCfg {
   static constexpr int kQSlots = DQK / 64;
   static constexpr int kDoSlots = DV / 64;
-  static constexpr int kChunk = BKV * 128;
-  static constexpr int kResident = (kQSlots + kDoSlots) * kSlotBytes;
-  static constexpr int kBudget = 232448 - 1024 - 1024;
-  static constexpr int kRingRaw = (kBudget - kResident) / kChunk;
-  static constexpr int kRing = kRingRaw > 24 ? 24 : kRingRaw;
+  static constexpr int kChunk = BKV * 128;  // one 64-column chunk of a key/value tile
   static constexpr int kKCh = DQK / 64;
   static constexpr int kVCh = DV / 64;
+  static constexpr int kResident = (kQSlots + kDoSlots) * kSlotBytes;
+  static constexpr int kBudget = kMaxSlots * kSlotBytes;  // dynamic bytes beyond the pad
+  // K tiles live in whole stages (the dQ MMA reads K MN-major across its
+  // chunks); V chunks go through a ring (the dP MMA reads them one by one).
+  static constexpr int kKStage = kKCh * kChunk;
+  static constexpr int kKStages = (kBudget - kResident - 3 * kKStage >= kVCh * kChunk) ? 3 : 2;
+  static constexpr int kVRingRaw = (kBudget - kResident - kKStages * kKStage) / kChunk;
+  static constexpr int kVRing = kVRingRaw > 12 ? 12 : kVRingRaw;
+  static constexpr int kSmem = kResident + kKStages * kKStage + kVRing * kChunk + 1024;
   static constexpr int kTdP = BKV;
   static constexpr int kTdS = 2 * BKV;
   static constexpr int kTdQ = ((5 * BKV / 2) + 31) / 32 * 32;
-  static constexpr int kSmem = kResident + kRing * kChunk + 1024;
   static constexpr int kHalf = BKV / 2;  // columns per softmax warpgroup
   static_assert(kTdQ + DQK <= 512, "TMEM budget");
-  // Slots are assigned in load order (V(j) then K(j)); K(j) stays held until
-  // dQ(j) is issued, after the score MMAs of tile j+1.  Those need the chunks
-  // up to the end of tile j+1, which reuse slots of tile j's K only if
-  // kRing < (chunks per tile) + kKCh.
-  static constexpr int kPerTile = kKCh + kVCh;
-  static_assert(kRing >= kPerTile + kKCh, "ring too small for the pipeline");
+  static_assert(kVRing >= kVCh, "V ring must hold one tile");
   static_assert(BKV == 64 || BKV == 128, "BKV");
+  static_assert(DQK <= 256, "one MMA covers the dQ columns");
 };
 
 template <int DQK, int DV, int BKV, bool BF16, bool G_F32>
@@ -54,9 +54,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sQ = smem;
   uint8_t* sDo = smem + C::kQSlots * kSlotBytes;
-  uint8_t* sRing = smem + C::kResident;
+  uint8_t* sK = smem + C::kResident;
+  uint8_t* sV = sK + C::kKStages * C::kKStage;
 
-  __shared__ uint64_t full_bar[C::kRing], empty_bar[C::kRing];
+  __shared__ uint64_t kfull[C::kKStages], kempty[C::kKStages], vfull[C::kVRing], vempty[C::kVRing];
   __shared__ uint64_t q_bar, sdp_full, sc_free, ds_full, dq_done, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, skip_sh;
@@ -82,9 +83,13 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
   Abort ab{&abort_flag, p.status};
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int i = 0; i < C::kRing; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+    for (int i = 0; i < C::kKStages; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
+    }
+    for (int i = 0; i < C::kVRing; ++i) {
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vempty[i], 1);
     }
     mbar_init(&q_bar, 1);
     mbar_init(&sdp_full, 1);
@@ -104,6 +109,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // per key tile: V chunks (ring), then the K stage
     if (elect_one_lane() && n_kv > 0) {
       int c1, c2, c3;
       map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
@@ -113,84 +119,96 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
       map_coords(p.odo, 0, h, sq.q_start + q0, tb, c1, c2, c3);
       for (int c = 0; c < C::kDoSlots; ++c)
         tma_load_4d(sDo + c * kSlotBytes, &p.tm_do, &q_bar, c * 64, c1, c2, c3);
-      uint32_t cnt = 0;
+      uint32_t vcnt = 0;
+      int jt = 0;
       bool ok = true;
-      for (int jt = 0; jt < n_kv && ok; ++jt) {
+      for (; jt < n_kv && ok; ++jt) {
         const int krow = sq.k_start + (kt0 + jt) * BKV;
-        for (int which = 0; which < 2 && ok; ++which) {  // V(j) first, then K(j)
-          const bool is_k = which == 1;
-          const CUtensorMap* m = is_k ? &p.tm_k : &p.tm_v;
-          int d1, d2, d3;
-          map_coords(is_k ? p.ok : p.ov, 0, g, krow, tb, d1, d2, d3);
-          const int nch = is_k ? C::kKCh : C::kVCh;
-          for (int c = 0; c < nch; ++c, ++cnt) {
-            const int slot = cnt % C::kRing;
-            if (!mbar_wait(&empty_bar[slot], ((cnt / C::kRing) & 1u) ^ 1u, ab)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_tx(&full_bar[slot], C::kChunk);
-            tma_load_4d(sRing + slot * C::kChunk, m, &full_bar[slot], c * 64, d1, d2, d3);
+        int d1, d2, d3;
+        map_coords(p.ov, 0, g, krow, tb, d1, d2, d3);
+#pragma unroll
+        for (int c = 0; c < C::kVCh; ++c, ++vcnt) {
+          const uint32_t slot = vcnt % C::kVRing;
+          if (!mbar_wait(&vempty[slot], ((vcnt / C::kVRing) & 1u) ^ 1u, ab)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_tx(&vfull[slot], C::kChunk);
+          tma_load_4d(sV + slot * C::kChunk, &p.tm_v, &vfull[slot], c * 64, d1, d2, d3);
         }
+        if (!ok) break;
+        const int st = jt % C::kKStages;
+        if (!mbar_wait(&kempty[st], ((jt / C::kKStages) & 1) ^ 1, ab)) {
+          ok = false;
+          break;
+        }
+        map_coords(p.ok, 0, g, krow, tb, d1, d2, d3);
+        mbar_arrive_tx(&kfull[st], C::kKStage);
+#pragma unroll
+        for (int c = 0; c < C::kKCh; ++c)
+          tma_load_4d(sK + st * C::kKStage + c * C::kChunk, &p.tm_k, &kfull[st], c * 64, d1, d2,
+                      d3);
       }
       mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
-      const uint32_t first = cnt > (uint32_t)C::kRing ? cnt - C::kRing : 0u;
-      for (uint32_t c = first; c < cnt; ++c)
-        mbar_wait_quiet(&full_bar[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
+      const uint32_t first = vcnt > (uint32_t)C::kVRing ? vcnt - C::kVRing : 0u;
+      for (uint32_t c = first; c < vcnt; ++c)
+        mbar_wait_quiet(&vfull[c % C::kVRing], (c / C::kVRing) & 1u, kWaitLimitNs);
+      const int nk = ok ? n_kv : jt;  // K stages issued
+      for (int v = nk > C::kKStages ? nk - C::kKStages : 0; v < nk; ++v)
+        mbar_wait_quiet(&kfull[v % C::kKStages], (v / C::kKStages) & 1, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_lane() && n_kv > 0) {
-      const uint32_t idesc_s = make_idesc(128, BKV, BF16, false, false);
-      const uint32_t idesc_q = make_idesc(128, 64, BF16, false, true);
-      bool ok = true;
-      auto wait_chunk = [&](uint32_t idx) -> uint32_t {
-        const uint32_t slot = idx % C::kRing;
-        if (!mbar_wait(&full_bar[slot], (idx / C::kRing) & 1u, ab)) {
-          ok = false;
-          return 0u;
-        }
-        tc_fence_after();
-        return smem_u32(sRing + slot * C::kChunk);
-      };
-      // chunk index of tile jt: V chunks first, then K chunks
-      auto v_idx = [&](int jt, int c) { return (uint32_t)(jt * C::kPerTile + c); };
-      auto k_idx = [&](int jt, int c) { return (uint32_t)(jt * C::kPerTile + C::kVCh + c); };
-      ok = mbar_wait(&q_bar, 0, ab);
+      constexpr uint32_t idesc_s = make_idesc(128, BKV, BF16, false, false);
+      constexpr uint32_t idesc_q = make_idesc(128, DQK, BF16, false, true);
+      const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
+      const uint64_t ddesc = make_sdesc(smem_u32(sDo), 16, 1024);
+      const uint64_t kdesc = make_sdesc(smem_u32(sK), 16, 1024);
+      const uint64_t kdesc_mn = make_sdesc(smem_u32(sK), C::kChunk, 1024);
+      const uint64_t vdesc = make_sdesc(smem_u32(sV), 16, 1024);
+      uint32_t vcnt = 0;
+      bool ok = mbar_wait(&q_bar, 0, ab);
       tc_fence_after();
       auto issue_scores = [&](int jt) {
-        for (int c = 0; c < C::kVCh && ok; ++c) {
-          const uint32_t vb = wait_chunk(v_idx(jt, c));
-          if (!ok) return;
-          const uint32_t da = smem_u32(sDo + c * kSlotBytes);
+#pragma unroll
+        for (int c = 0; c < C::kVCh; ++c, ++vcnt) {  // dP = dO V^T
+          const uint32_t slot = vcnt % C::kVRing;
+          if (!mbar_wait(&vfull[slot], (vcnt / C::kVRing) & 1u, ab)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+          const uint64_t da = ddesc + (uint64_t)(c * (kSlotBytes >> 4));
+          const uint64_t vb = vdesc + (uint64_t)(slot * (C::kChunk >> 4));
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + C::kTdP, make_sdesc(da + k * 32, 16, 1024),
-                   make_sdesc(vb + k * 32, 16, 1024), idesc_s, (c | k) ? 1u : 0u);
-          mma_commit(&empty_bar[v_idx(jt, c) % C::kRing]);
+            mma_ss(tmem + C::kTdP, da + 2 * k, vb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+          mma_commit(&vempty[slot]);
         }
-        for (int c = 0; c < C::kKCh && ok; ++c) {
-          const uint32_t kb = wait_chunk(k_idx(jt, c));
-          if (!ok) return;
-          const uint32_t qa = smem_u32(sQ + c * kSlotBytes);
+        const int st = jt % C::kKStages;  // S = Q K^T
+        if (!mbar_wait(&kfull[st], (jt / C::kKStages) & 1, ab)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem, make_sdesc(qa + k * 32, 16, 1024), make_sdesc(kb + k * 32, 16, 1024),
-                   idesc_s, (c | k) ? 1u : 0u);
-        }
-        if (ok) mma_commit(&sdp_full);
-      };
-      auto issue_dq = [&](int jt) {
         for (int c = 0; c < C::kKCh; ++c) {
-          const uint32_t slot = k_idx(jt, c) % C::kRing;  // held since the S MMA of tile jt
-          const uint32_t kb = smem_u32(sRing + slot * C::kChunk);
+          const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
+          const uint64_t kb = kdesc + (uint64_t)((st * C::kKStage + c * C::kChunk) >> 4);
 #pragma unroll
-          for (int k = 0; k < BKV / 16; ++k)
-            mma_ts(tmem + C::kTdQ + c * 64, tmem + C::kTdS + k * 8,
-                   make_sdesc(kb + k * 2048, 16, 1024), idesc_q, (jt > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&empty_bar[slot]);
+          for (int k = 0; k < 4; ++k) mma_ss(tmem, qa + 2 * k, kb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
         }
+        mma_commit(&sdp_full);
+      };
+      auto issue_dq = [&](int jt) {  // dQ += dS K  (K stage read MN-major, N = DQK)
+        const int st = jt % C::kKStages;
+        const uint64_t kb = kdesc_mn + (uint64_t)((st * C::kKStage) >> 4);
+        mma_ts(tmem + C::kTdQ, tmem + C::kTdS, kb, idesc_q, jt > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 1; k < BKV / 16; ++k)
+          mma_ts(tmem + C::kTdQ, tmem + C::kTdS + k * 8, kb + k * 128, idesc_q, 1u);
+        mma_commit(&kempty[st]);
         mma_commit(&dq_done);
       };
       if (ok) issue_scores(0);

@@ -23,13 +23,18 @@ namespace attn {
 template <int DQK, int DV_CTA, bool BF16, bool O_F32>
 struct FwdCfg {
   static constexpr int kQSlots = DQK / 64;
-  static constexpr int kRing = kMaxSlots - kQSlots;
-  static constexpr int kVChunks = DV_CTA / 64;
-  static constexpr int kKChunks = DQK / 64;
-  static constexpr int kSmem = (kQSlots + kRing) * kSlotBytes + 1024;
+  static constexpr int kKCh = DQK / 64;    // K tile = kKCh 64-column chunks (K-major)
+  static constexpr int kVCh = DV_CTA / 64;  // V tile = kVCh chunks, kept contiguous
+  // V tiles live in whole stages so that one MMA covers all DV_CTA columns
+  // (the B operand is MN-major and spans the chunks through LBO); K chunks go
+  // through their own ring since the S MMA consumes them one chunk at a time.
+  static constexpr int kVStages = (kQSlots + 2 * kVCh + 2 <= kMaxSlots) ? 2 : 1;
+  static constexpr int kKRingRaw = kMaxSlots - kQSlots - kVStages * kVCh;
+  static constexpr int kKRing = kKRingRaw > 16 ? 16 : kKRingRaw;
+  static constexpr int kSmem = (kQSlots + kVStages * kVCh + kKRing) * kSlotBytes + 1024;
   static constexpr int kTmemO = 256;
   static_assert(DQK % 64 == 0 && DV_CTA % 64 == 0 && DV_CTA <= 256, "head dim");
-  static_assert(kRing >= 2, "ring");
+  static_assert(kKRing >= 2, "ring");
 };
 
 template <int DQK, int DV_CTA, bool BF16, bool O_F32>
@@ -38,9 +43,10 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sQ = smem;
-  uint8_t* sRing = smem + C::kQSlots * kSlotBytes;
+  uint8_t* sV = smem + C::kQSlots * kSlotBytes;
+  uint8_t* sK = sV + C::kVStages * C::kVCh * kSlotBytes;
 
-  __shared__ uint64_t full_bar[C::kRing], empty_bar[C::kRing];
+  __shared__ uint64_t kfull[C::kKRing], kempty[C::kKRing], vfull[C::kVStages], vempty[C::kVStages];
   __shared__ uint64_t q_bar, s_full[2], p_full[2], o_done, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, skip_sh;
@@ -68,9 +74,13 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   Abort ab{&abort_flag, p.status};
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int i = 0; i < C::kRing; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+    for (int i = 0; i < C::kKRing; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vempty[i], 1);
     }
     mbar_init(&q_bar, 1);
     for (int i = 0; i < 2; ++i) {
@@ -91,6 +101,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // load order = MMA order: K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1)
     if (elect_one_lane() && n_kv > 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
@@ -100,90 +111,101 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       mbar_arrive_tx(&q_bar, C::kQSlots * kSlotBytes);
       for (int c = 0; c < C::kQSlots; ++c)
         tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
-      uint32_t cnt = 0;
+      uint32_t kcnt = 0;
+      int vcnt = 0;
       bool ok = true;
-      // consumption order: K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1)
-      auto load_chunks = [&](bool is_v, int jt) {
-        const int krow = sq.k_start + (kt0 + jt) * kBlockN;
+      auto load_k = [&](int jt) {
         int d1, d2, d3;
-        if (is_v)
-          map_coords(p.ov, 0, g, krow, tb, d1, d2, d3);
-        else
-          map_coords(p.ok, 0, g, krow, tb, d1, d2, d3);
-        const int nch = is_v ? C::kVChunks : C::kKChunks;
-        const int col0 = is_v ? split * DV_CTA : 0;
-        for (int c = 0; c < nch && ok; ++c, ++cnt) {
-          const int slot = cnt % C::kRing;
-          const uint32_t ph = (cnt / C::kRing) & 1u;
-          if (!mbar_wait(&empty_bar[slot], ph ^ 1u, ab)) {
+        map_coords(p.ok, 0, g, sq.k_start + (kt0 + jt) * kBlockN, tb, d1, d2, d3);
+#pragma unroll
+        for (int c = 0; c < C::kKCh; ++c, ++kcnt) {
+          const uint32_t slot = kcnt % C::kKRing;
+          if (!mbar_wait(&kempty[slot], ((kcnt / C::kKRing) & 1u) ^ 1u, ab)) {
             ok = false;
-            break;
+            return;
           }
-          mbar_arrive_tx(&full_bar[slot], kSlotBytes);
-          tma_load_4d(sRing + slot * kSlotBytes, is_v ? &p.tm_v : &p.tm_k, &full_bar[slot],
-                      col0 + c * 64, d1, d2, d3);
+          mbar_arrive_tx(&kfull[slot], kSlotBytes);
+          tma_load_4d(sK + slot * kSlotBytes, &p.tm_k, &kfull[slot], c * 64, d1, d2, d3);
         }
       };
-      load_chunks(false, 0);
+      auto load_v = [&](int jt) {
+        int d1, d2, d3;
+        map_coords(p.ov, 0, g, sq.k_start + (kt0 + jt) * kBlockN, tb, d1, d2, d3);
+        const int st = vcnt % C::kVStages;
+        if (!mbar_wait(&vempty[st], ((vcnt / C::kVStages) & 1) ^ 1, ab)) {
+          ok = false;
+          return;
+        }
+        mbar_arrive_tx(&vfull[st], C::kVCh * kSlotBytes);
+#pragma unroll
+        for (int c = 0; c < C::kVCh; ++c)
+          tma_load_4d(sV + (st * C::kVCh + c) * kSlotBytes, &p.tm_v, &vfull[st],
+                      split * DV_CTA + c * 64, d1, d2, d3);
+        ++vcnt;
+      };
+      load_k(0);
       for (int jt = 0; jt < n_kv && ok; ++jt) {
-        if (jt + 1 < n_kv) load_chunks(false, jt + 1);
-        load_chunks(true, jt);
+        if (jt + 1 < n_kv) load_k(jt + 1);
+        if (ok) load_v(jt);
       }
       // let every copy still in flight land before the CTA can exit
       mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
-      const uint32_t first = cnt > (uint32_t)C::kRing ? cnt - C::kRing : 0u;
-      for (uint32_t c = first; c < cnt; ++c)
-        mbar_wait_quiet(&full_bar[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
+      const uint32_t first = kcnt > (uint32_t)C::kKRing ? kcnt - C::kKRing : 0u;
+      for (uint32_t c = first; c < kcnt; ++c)
+        mbar_wait_quiet(&kfull[c % C::kKRing], (c / C::kKRing) & 1u, kWaitLimitNs);
+      for (int v = vcnt > C::kVStages ? vcnt - C::kVStages : 0; v < vcnt; ++v)
+        mbar_wait_quiet(&vfull[v % C::kVStages], (v / C::kVStages) & 1, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Descriptors are built once; per MMA only small constant offsets are
+    // added (the start-address field counts 16-byte units).
     if (elect_one_lane() && n_kv > 0) {
-      const uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
-      const uint32_t idesc_o = make_idesc(128, 64, BF16, false, true);
-      uint32_t cnt = 0;
+      constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
+      constexpr uint32_t idesc_o = make_idesc(128, DV_CTA, BF16, false, true);
+      const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
+      const uint64_t kdesc = make_sdesc(smem_u32(sK), 16, 1024);
+      const uint64_t vdesc = make_sdesc(smem_u32(sV), kSlotBytes, 1024);
+      uint32_t kcnt = 0;
       bool ok = mbar_wait(&q_bar, 0, ab);
       tc_fence_after();
       auto issue_s = [&](int jt) {
         const uint32_t d = tmem + (uint32_t)((jt & 1) * 128);
-        for (int c = 0; c < C::kKChunks && ok; ++c, ++cnt) {
-          const int slot = cnt % C::kRing;
-          if (!mbar_wait(&full_bar[slot], (cnt / C::kRing) & 1u, ab)) {
+#pragma unroll
+        for (int c = 0; c < C::kKCh; ++c, ++kcnt) {
+          const uint32_t slot = kcnt % C::kKRing;
+          if (!mbar_wait(&kfull[slot], (kcnt / C::kKRing) & 1u, ab)) {
             ok = false;
-            break;
+            return;
           }
           tc_fence_after();
-          const uint32_t qa = smem_u32(sQ + c * kSlotBytes);
-          const uint32_t kb = smem_u32(sRing + slot * kSlotBytes);
+          const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
+          const uint64_t kb = kdesc + (uint64_t)(slot * (kSlotBytes >> 4));
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(d, make_sdesc(qa + k * 32, 16, 1024), make_sdesc(kb + k * 32, 16, 1024),
-                   idesc_s, (c | k) ? 1u : 0u);
-          mma_commit(&empty_bar[slot]);
+            mma_ss(d, qa + 2 * k, kb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+          mma_commit(&kempty[slot]);
         }
-        if (ok) mma_commit(&s_full[jt & 1]);
+        mma_commit(&s_full[jt & 1]);
       };
       auto issue_pv = [&](int jt) {
         if (!mbar_wait(&p_full[jt & 1], (jt >> 1) & 1u, ab)) {
           ok = false;
           return;
         }
+        const int st = jt % C::kVStages;
+        if (!mbar_wait(&vfull[st], (jt / C::kVStages) & 1, ab)) {
+          ok = false;
+          return;
+        }
         tc_fence_after();
         const uint32_t pa = tmem + (uint32_t)((jt & 1) * 128);
-        for (int c = 0; c < C::kVChunks && ok; ++c, ++cnt) {
-          const int slot = cnt % C::kRing;
-          if (!mbar_wait(&full_bar[slot], (cnt / C::kRing) & 1u, ab)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t vb = smem_u32(sRing + slot * kSlotBytes);
+        const uint64_t vb = vdesc + (uint64_t)(st * C::kVCh * (kSlotBytes >> 4));
+        mma_ts(tmem + C::kTmemO, pa, vb, idesc_o, jt > 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + C::kTmemO + c * 64, pa + k * 8, make_sdesc(vb + k * 2048, 16, 1024),
-                   idesc_o, (jt > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&empty_bar[slot]);
-        }
-        if (ok) mma_commit(&o_done);
+        for (int k = 1; k < 8; ++k) mma_ts(tmem + C::kTmemO, pa + k * 8, vb + k * 128, idesc_o, 1u);
+        mma_commit(&vempty[st]);
+        mma_commit(&o_done);
       };
       if (ok) issue_s(0);
       for (int jt = 0; jt < n_kv && ok; ++jt) {
@@ -237,16 +259,22 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
         for (int t = 0; t < 128; ++t)
           if (t < lo || t > hi) s[t] = -INFINITY;
       }
-      float mx = -INFINITY;
+      // row maximum as 8 independent chains (one warp per sub-partition has
+      // no other warp to hide a 128-long dependency chain)
+      float mxv[8];
 #pragma unroll
-      for (int t = 0; t < 128; ++t) mx = fmaxf(mx, s[t]);
+      for (int u = 0; u < 8; ++u) mxv[u] = s[u];
+#pragma unroll
+      for (int t = 8; t < 128; ++t) mxv[t & 7] = fmaxf(mxv[t & 7], s[t]);
+      const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
+                             fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
       const float m_tile = mx * sl2;
       const bool grow = m_tile > m_run + 8.0f;
       const float m_new = grow ? m_tile : m_run;
       const float alpha = grow ? ex2(m_run - m_new) : 1.0f;
       m_run = m_new;
       const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
-      float rs = 0.0f;
+      float rsv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -254,11 +282,13 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
         for (int t = 0; t < 16; ++t) {
           const float e0 = ex2(fmaf(s[c * 32 + 2 * t], sl2, neg_m));
           const float e1 = ex2(fmaf(s[c * 32 + 2 * t + 1], sl2, neg_m));
-          rs += e0 + e1;
+          rsv[(2 * t) & 7] += e0;
+          rsv[(2 * t + 1) & 7] += e1;
           pk[t] = Pack<BF16>::two(e0, e1);
         }
         tmem_st16(sb + c * 16, pk);
       }
+      const float rs = ((rsv[0] + rsv[1]) + (rsv[2] + rsv[3])) + ((rsv[4] + rsv[5]) + (rsv[6] + rsv[7]));
       l_run = l_run * alpha + rs;
       // rescale O rows whose maximum grew (after PV(jt-1) has finished)
       if (__any_sync(0xffffffffu, grow && jt > 0)) {

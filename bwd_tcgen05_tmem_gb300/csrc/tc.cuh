@@ -233,7 +233,7 @@ __device__ __forceinline__ uint32_t elect_one_lane() {
 }
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
