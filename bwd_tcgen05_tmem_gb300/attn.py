@@ -28,7 +28,8 @@ _STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
            3: "ATTN_ERR_ALIGNMENT", 4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_BAD_METADATA",
            6: "ATTN_ERR_TIMEOUT", 7: "ATTN_ERR_CUDA"}
 EXPORTED = ["attn_fwd_workspace_size", "attn_bwd_workspace_size", "attn_fwd", "attn_bwd",
-            "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkdv", "attn_lse_merge",
+            "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkdv", "attn_bwd_noalloc",
+            "attn_lse_merge",
             "attn_query_status", "attn_last_error", "attn_last_launch_count"]
 
 
@@ -85,6 +86,8 @@ def load():
             fn = getattr(lib, name)
             fn.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             fn.restype = ctypes.c_int
+        lib.attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.attn_bwd_noalloc.restype = ctypes.c_int
         lib.attn_lse_merge.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                        i64p, i64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                        vp, ctypes.c_int, vp, vp]
@@ -235,6 +238,35 @@ def bwd(q, k, v, o, dout, lse, *, causal=True, scale=None, window=(-1, -1),
     _check(fn(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
                         _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                         workspace.numel(), _stream(stream)))
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, o, dout, lse, *, causal=True, scale=None, window=(-1, -1),
+                bottom_right=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None,
+                max_seqlen_k=None, dq=None, dk=None, dv=None, grad_dtype=None,
+                lse_strides=(0, 0), accumulate=False, stream=None):
+    """attn_bwd_noalloc: the backward without a caller workspace.
+
+    For callers that must not allocate device memory while they run (the
+    library's own 8 MiB static scratch area is used instead; concurrent calls
+    on one device race).  The output tensors are still the caller's.
+    Returns (dq, dk, dv)."""
+    lib = load()
+    gdt = grad_dtype if grad_dtype is not None else q.dtype
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=gdt, device=q.device)
+    if dk is None:
+        dk = torch.empty(k.shape, dtype=gdt, device=q.device)
+    if dv is None:
+        dv = torch.empty(v.shape, dtype=gdt, device=q.device)
+    p = make_params(q, k, v, causal=causal, scale=scale, window=window,
+                    bottom_right=bottom_right, cu_seqlens_q=cu_seqlens_q,
+                    cu_seqlens_k=cu_seqlens_k, max_seqlen_q=max_seqlen_q,
+                    max_seqlen_k=max_seqlen_k, o=o, dout=dout, dq=dq, dk=dk, dv=dv,
+                    o_dtype=o.dtype, grad_dtype=gdt, lse_strides=lse_strides,
+                    accumulate=accumulate)
+    _check(lib.attn_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
+                                _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
     return dq, dk, dv
 
 

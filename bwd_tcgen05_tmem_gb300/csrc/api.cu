@@ -1,5 +1,8 @@
 // api.cu -- the C ABI declared in include/attn.h: host-side validation,
-// tensor-map construction and kernel dispatch.  No allocation, no state.
+// tensor-map construction and kernel dispatch.  No call allocates memory; the
+// only state is a thread-local error string, cached device attributes and
+// (for attn_bwd_noalloc) a static scratch area and its per-device address.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -436,6 +439,57 @@ attn_status_t attn_bwd_dkdv(const attn_params_t* p, const void* q, const void* k
                             void* dk, void* dv, void* ws, size_t ws_bytes,
                             attn_stream_t stream) {
   return bwd_impl(p, q, k, v, o, dout, lse, dq, dk, dv, ws, ws_bytes, stream, kStageDkv);
+}
+
+}  // extern "C"
+
+// ----------------------------------------------------------------- attn_bwd_noalloc
+// Scratch for callers that cannot allocate: reserved in this library's image,
+// so every GPU that loads the library holds it until the process exits.  In
+// host code the symbol is only a host-side stand-in; kernels get its device
+// address, looked up once per device with that device current.
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+attn_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device index %d", dev);
+  void* ptr = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_addr[dev].store(ptr, std::memory_order_release);
+  }
+  *out = ptr;
+  return ATTN_OK;
+}
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_bwd_noalloc(const attn_params_t* p, const void* q, const void* k,
+                               const void* v, const void* o, const void* dout, const float* lse,
+                               void* dq, void* dk, void* dv, attn_stream_t stream) {
+  g_err[0] = 0;
+  g_launches = 0;
+  if (!p) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
+  const size_t need = attn_bwd_workspace_size(p);
+  if (need > kNoAllocScratchBytes)
+    return fail(ATTN_ERR_WORKSPACE,
+                "problem needs %zu bytes of scratch; attn_bwd_noalloc has a fixed %zu-byte "
+                "area (use attn_bwd with a caller workspace)",
+                need, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  attn_status_t s = noalloc_scratch(&ws);
+  if (s) return s;
+  return bwd_impl(p, q, k, v, o, dout, lse, dq, dk, dv, ws, kNoAllocScratchBytes, stream,
+                  kStageAll);
 }
 
 attn_status_t attn_lse_merge(int n_parts, const float* const* o_parts,

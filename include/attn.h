@@ -145,6 +145,37 @@ attn_status_t attn_bwd_dkdv(const attn_params_t* p, const void* q, const void* k
                             attn_stream_t stream);
 
 /*
+ * attn_bwd for callers that cannot allocate device memory (this entry point
+ * has no counterpart on the attention pages; it is a deployment aid).
+ *
+ * Some callers are not allowed to call cudaMalloc while they run: cudaMalloc
+ * may synchronise the whole device and takes an unbounded time, so serving
+ * loops with latency budgets, plugin hosts that plan every byte of device
+ * memory up front, and code running inside another runtime's callbacks
+ * forbid it -- and such callers often have no allocator of their own from
+ * which to hand attn_bwd a workspace.  attn_bwd_noalloc takes the same
+ * arguments as attn_bwd minus the workspace and uses instead a scratch area
+ * that the library reserves statically: 8 MiB of device memory per GPU that
+ * loads the library, held until the process exits.  That covers problems
+ * whose attn_bwd_workspace_size() is at most 8 MiB (about two million
+ * query rows x query heads); larger ones return ATTN_ERR_WORKSPACE and
+ * nothing is launched.  It calls no allocating routine.
+ *
+ * The first call on each device looks up the scratch area's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture.  Every call on a device shares the one scratch area and
+ * the status word in it, so calls whose work overlaps on the GPU (different
+ * streams, or host threads) race with each other: serialise them.  The
+ * status word is cleared at the start of each call; as the caller holds no
+ * pointer to it, device-detected problems (inconsistent cu_seqlens, a wait
+ * past its limit) are not reported to it -- use attn_bwd where that matters.
+ * Results are identical to attn_bwd's.
+ */
+attn_status_t attn_bwd_noalloc(const attn_params_t* p, const void* q, const void* k,
+                               const void* v, const void* o, const void* dout, const float* lse,
+                               void* dq, void* dk, void* dv, attn_stream_t stream);
+
+/*
  * LSE-weighted merge of partial attention results over disjoint key sets
  * (PR #3527: the context-parallel ring correction exponentiates LSE
  * differences):  LSE = ln sum_p exp(LSE_p),  O = sum_p exp(LSE_p - LSE) O_p,
