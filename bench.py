@@ -196,6 +196,22 @@ def cpu_baseline(w, seconds_target=15.0):
                       f"{nthreads} threads of {ncpu} host cores"}
 
 
+def max_over_ranks(value, device=None):
+    """The slowest rank's value (the job's time); a no-op on one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank, ms, world):
+    """Whole-job throughput: every rank processed `flops_per_rank` in at most `ms`."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -307,10 +323,7 @@ def main():
     per_kernel = {st: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in events)
                   for i, st in enumerate(stages)}
     ms = total_ms / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = tt.item()
+    ms = max_over_ranks(ms, dev)
     clocks = clk.summary()
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
@@ -341,10 +354,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = tt.item()
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     # ---- one-GPU context-parallel ring emulation (dual chunk swap, 8 ranks)
     cp_obj = None
@@ -382,7 +392,7 @@ def main():
     dom = max(("fwd", "dq", "dkdv"), key=lambda s: per_kernel[s])
     ach = fl["kernel"][dom] / (per_kernel[dom] * 1e-3) / 1e12
     traffic = load_traffic(dom)
-    value = world * fl["total"] / (ms * 1e-3) / 1e12
+    value = job_tflops(fl["total"], ms, world)
     line = {
         "metric": METRIC,
         "value": value,
@@ -413,7 +423,7 @@ def main():
                      "work_per_launch": fl["kernel"][dom]},
         "pre_gbs": (w.batch * w.seqlen * w.heads_q * (2 * w.d_v * 2 + 4)) /
                    (per_kernel["pre"] * 1e-3) / 1e9,
-        "e2e": {"value": world * fl["total"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(fl["total"], e2e_ms, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
