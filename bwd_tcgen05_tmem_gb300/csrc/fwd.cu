@@ -7,8 +7,9 @@
 //
 // One CTA owns 128 query rows of one (sequence, query head) and, for head dim
 // 512, one half of the value columns.  Warp roles (256 threads):
-//   warp 0      TMA producer: Q once, then K/V 64-column chunks through a ring
-//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warp 0      TMA producer: Q once, then K chunks (ring) and V tiles (stages)
+//   warp 1      TMEM allocator and S-MMA issuer (one thread)
+//   warp 2      PV-MMA issuer (one thread)
 //   warps 4..7  softmax: one TMEM lane (= query row) per thread; rescales O
 //               in TMEM when the running maximum grows, writes P (16-bit)
 //               into TMEM, and runs the epilogue.
@@ -47,7 +48,8 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   uint8_t* sK = sV + C::kVStages * C::kVCh * kSlotBytes;
 
   __shared__ uint64_t kfull[C::kKRing], kempty[C::kKRing], vfull[C::kVStages], vempty[C::kVStages];
-  __shared__ uint64_t q_bar, s_full[2], p_full[2], o_done, drain_bar;
+  // o_done[b]: PV of the key tiles that used S buffer b (one phase per use)
+  __shared__ uint64_t q_bar, s_full[2], p_full[2], o_done[2], drain_bar, drain_bar2;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, skip_sh;
 
@@ -87,8 +89,10 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
     }
-    mbar_init(&o_done, 1);
+    mbar_init(&o_done[0], 1);
+    mbar_init(&o_done[1], 1);
     mbar_init(&drain_bar, 1);
+    mbar_init(&drain_bar2, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -156,18 +160,21 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       for (int v = vcnt > C::kVStages ? vcnt - C::kVStages : 0; v < vcnt; ++v)
         mbar_wait_quiet(&vfull[v % C::kVStages], (v / C::kVStages) & 1, kWaitLimitNs);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Descriptors are built once; per MMA only small constant offsets are
-    // added (the start-address field counts 16-byte units).
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 1 issues S = Q K^T, warp 2 issues O += P V: each blocks on its own
+    // barriers while the other keeps the tensor pipe fed.  Descriptors are
+    // built once; per MMA only small constant offsets are added (the
+    // start-address field counts 16-byte units).
     if (elect_one_lane() && n_kv > 0) {
+      const bool s_role = warp == 1;
       constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
       constexpr uint32_t idesc_o = make_idesc(128, DV_CTA, BF16, false, true);
       const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
       const uint64_t kdesc = make_sdesc(smem_u32(sK), 16, 1024);
       const uint64_t vdesc = make_sdesc(smem_u32(sV), kSlotBytes, 1024);
       uint32_t kcnt = 0;
-      bool ok = mbar_wait(&q_bar, 0, ab);
+      bool ok = s_role ? mbar_wait(&q_bar, 0, ab) : true;
       tc_fence_after();
       auto issue_s = [&](int jt) {
         const uint32_t d = tmem + (uint32_t)((jt & 1) * 128);
@@ -205,19 +212,21 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
         for (int k = 1; k < 8; ++k) mma_ts(tmem + C::kTmemO, pa + k * 8, vb + k * 128, idesc_o, 1u);
         mma_commit(&vempty[st]);
-        mma_commit(&o_done);
+        mma_commit(&o_done[jt & 1]);
       };
-      if (ok) issue_s(0);
-      for (int jt = 0; jt < n_kv && ok; ++jt) {
-        if (jt + 1 < n_kv) {
-          // S buffer (jt+1)&1 last held P(jt-1): wait until PV(jt-1) has read it
-          if (jt >= 1 && !mbar_wait(&o_done, (jt - 1) & 1u, ab)) break;
-          issue_s(jt + 1);
+      if (s_role) {
+        for (int jt = 0; jt < n_kv && ok; ++jt) {
+          // S buffer jt&1 last held P(jt-2): wait until PV(jt-2) has read it
+          if (jt >= 2 && !mbar_wait(&o_done[jt & 1], ((jt - 2) >> 1) & 1u, ab)) break;
+          issue_s(jt);
         }
-        if (ok) issue_pv(jt);
+        mma_commit(&drain_bar);
+        mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+      } else {
+        for (int jt = 0; jt < n_kv && ok; ++jt) issue_pv(jt);
+        mma_commit(&drain_bar2);
+        mbar_wait_quiet(&drain_bar2, 0, kWaitLimitNs);
       }
-      mma_commit(&drain_bar);
-      mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       l_run = l_run * alpha + rs;
       // rescale O rows whose maximum grew (after PV(jt-1) has finished)
       if (__any_sync(0xffffffffu, grow && jt > 0)) {
-        if (!mbar_wait_warp(&o_done, (jt - 1) & 1u, ab)) {
+        if (!mbar_wait_warp(&o_done[(jt - 1) & 1], ((jt - 1) >> 1) & 1u, ab)) {
           ok = false;
           break;
         }
@@ -317,10 +326,9 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       mbar_arrive(&p_full[jt & 1]);
     }
     // ------------------------------------------------------------ epilogue
-    // PV(n-2) may still be in flight here (the rescale wait is conditional), so
-    // complete the phases in order: a parity wait cannot tell phase n-1 from n-3.
-    if (ok && n_kv > 1) ok = mbar_wait_warp(&o_done, (n_kv - 2) & 1u, ab);
-    if (ok && n_kv > 0) ok = mbar_wait_warp(&o_done, (n_kv - 1) & 1u, ab);
+    // PV(n-2) and PV(n-1) used different S buffers, hence different barriers
+    if (ok && n_kv > 1) ok = mbar_wait_warp(&o_done[(n_kv - 2) & 1], ((n_kv - 2) >> 1) & 1u, ab);
+    if (ok && n_kv > 0) ok = mbar_wait_warp(&o_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1u, ab);
     if (ok) {
       tc_fence_after();
       const bool valid = i < sq.lq;
