@@ -202,6 +202,57 @@ attn_status_t launch_check_if_thd(const attn_params_t* p, int* status, cudaStrea
   return ATTN_OK;
 }
 
+// Backward workspace: [status][D: rows x heads_q fp32] and, for head dims
+// above 256, [per-sequence block prefix][64 KiB score blocks].
+struct BwdLayout {
+  size_t d_off, plan_off, blk_off, total;
+  long long cap;  // score blocks
+};
+
+bool wide(const attn_params_t* p) { return p->d_qk > 256 || p->d_v > 256; }
+
+// Score blocks of the wide backward over all query heads: exact for dense
+// inputs; for packed (THD) inputs a bound that takes every document's keys
+// as max_seqlen_k long.
+long long wide_block_count(const attn_params_t* p) {
+  const long long hq = p->heads_q > 0 ? p->heads_q : 0;
+  if (p->batch <= 0 || hq == 0) return 0;
+  if (thd(p)) {
+    const long long nq = (p->total_q > 0 ? p->total_q : 0) / 128 + p->batch;
+    const long long nk = (p->seqlen_k > 0 ? (long long)p->seqlen_k + 127 : 0) / 128;
+    return hq * nq * nk;
+  }
+  if (p->seqlen_q <= 0 || p->seqlen_k <= 0) return 0;
+  attn::Seq s;
+  s.q_start = s.k_start = 0;
+  s.lq = p->seqlen_q;
+  s.lk = p->seqlen_k;
+  s.off = p->bottom_right ? (long long)(s.lk - s.lq) : 0ll;
+  s.L = p->window_left < 0 ? attn::kInfBound : (long long)p->window_left;
+  s.R = p->causal ? 0ll : (p->window_right < 0 ? attn::kInfBound : (long long)p->window_right);
+  long long t = 0;
+  int kb0;
+  for (int qt = 0; qt < (s.lq + 127) / 128; ++qt) t += attn::wide_blocks_of_qtile(s, qt, kb0);
+  return (long long)p->batch * hq * t;
+}
+
+BwdLayout bwd_layout(const attn_params_t* p) {
+  BwdLayout l;
+  memset(&l, 0, sizeof(l));
+  const int64_t rq = rows_q(p);
+  const size_t d_bytes = (size_t)(rq > 0 ? rq : 0) * (size_t)(p->heads_q > 0 ? p->heads_q : 0) * 4;
+  l.d_off = kStatusBytes;
+  l.total = l.d_off + ((d_bytes + 255) / 256) * 256;
+  if (wide(p)) {
+    l.plan_off = l.total;
+    const size_t plan_bytes = (size_t)(p->batch > 0 ? p->batch + 1 : 1) * 8;
+    l.blk_off = ((l.plan_off + plan_bytes + 1023) / 1024) * 1024;
+    l.cap = wide_block_count(p);
+    l.total = l.blk_off + (size_t)l.cap * attn::kWideBlock;
+  }
+  return l;
+}
+
 }  // namespace
 
 extern "C" {
@@ -213,9 +264,7 @@ size_t attn_fwd_workspace_size(const attn_params_t* p) {
 
 size_t attn_bwd_workspace_size(const attn_params_t* p) {
   if (!p) return kStatusBytes;
-  const int64_t rq = thd(p) ? (int64_t)p->total_q : (int64_t)p->batch * p->seqlen_q;
-  const size_t d_bytes = (size_t)(rq > 0 ? rq : 0) * (size_t)(p->heads_q > 0 ? p->heads_q : 0) * 4;
-  return kStatusBytes + ((d_bytes + 255) / 256) * 256;
+  return bwd_layout(p).total;
 }
 
 attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, const void* v,
@@ -344,7 +393,8 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
     }
   }
   int* status = (int*)ws;
-  float* dbuf = (float*)((char*)ws + kStatusBytes);
+  const BwdLayout lay = bwd_layout(p);
+  float* dbuf = (float*)((char*)ws + lay.d_off);
   cudaError_t e;
   if (pre) {
     e = cudaMemsetAsync(status, 0, sizeof(int), st);
@@ -377,6 +427,11 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
   lse_strides(p, a.lse_sb, a.lse_sh);
   a.d = dbuf;
   default_d_strides(p, a.d_sb, a.d_sh);
+  if (wide(p)) {
+    a.wide_plan = (long long*)((char*)ws + lay.plan_off);
+    a.wide_blocks = (uint8_t*)ws + lay.blk_off;
+    a.wide_cap = lay.cap;
+  }
   a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout;
   a.dq = dq; a.dk = dk; a.dvp = dv;
   memcpy(a.sq, p->stride_q, sizeof(a.sq));

@@ -23,6 +23,76 @@ struct BwdArgs {
   int64_t sq[3], sk[3], sv[3], so[3], sdo[3], sdq[3], sdk[3], sdv[3];
   CUtensorMap tm_q128, tm_q64, tm_do128, tm_do64, tm_k128, tm_k64, tm_v128, tm_v64;
   MapOrder oq, odo, ok, ov;
+  // head dims above 256: per-sequence block prefix and the score tiles
+  long long* wide_plan;
+  uint8_t* wide_blocks;
+  long long wide_cap;
+};
+
+// ---------------------------------------------------------------- wide path
+// Head dims above 256 materialise P and dS: one 64 KiB block per (sequence,
+// query head, 128-row query tile, visible 128-key block), holding four
+// 128 x 64 16-bit tiles in their 128-byte-swizzled shared-memory image:
+// P keys 0-63, P keys 64-127, dS keys 0-63, dS keys 64-127.
+constexpr int kWideTile = 128 * 64 * 2;
+constexpr int kWideBlock = 4 * kWideTile;
+
+// Visible 128-key blocks of query tile qt: returns their count, first in kb0.
+__host__ __device__ inline int wide_blocks_of_qtile(const Seq& s, int qt, int& kb0) {
+  const long long i0 = (long long)qt * 128;
+  kb0 = 0;
+  if (i0 > (long long)s.lq - 1) return 0;
+  const long long i1 = i0 + 127 < (long long)s.lq - 1 ? i0 + 127 : (long long)s.lq - 1;
+  long long j0, j1;
+  key_range(s, i0, i1, j0, j1);
+  if (j1 < j0) return 0;
+  kb0 = (int)(j0 / 128);
+  return (int)(j1 / 128) - kb0 + 1;
+}
+
+struct WidePlanParams {
+  Geometry geo;
+  long long* plan;  // [batch + 1] exclusive prefix of per-sequence block counts
+  long long cap;    // blocks the workspace holds
+  int batch, hq;
+  int* status;
+};
+
+struct WideScoresParams {
+  CUtensorMap tm_q, tm_k, tm_v;  // q: 128-row boxes, k/v: 64-row boxes
+  MapOrder oq, ok, ov;
+  Geometry geo;
+  const float* lse;
+  int64_t lse_sb, lse_sh;
+  const float* d;
+  int64_t d_sb, d_sh;
+  const void* dout;
+  int64_t sdo_b, sdo_t, sdo_h;
+  const long long* plan;
+  uint8_t* blocks;
+  long long cap;
+  int batch, hq, hkv, n_qtiles;
+  float scale_log2;
+  int* status;
+};
+
+// dQ (kind 0: per query tile) and dV / dK (kind 1: per key tile) GEMMs over
+// the materialised tiles.
+struct WideAccParams {
+  CUtensorMap tm_b0, tm_b1;  // B operand (64-row boxes): dQ: K, -;  dK/dV: dO, Q
+  MapOrder ob0, ob1;
+  Geometry geo;
+  const long long* plan;
+  const uint8_t* blocks;
+  long long cap;
+  void* out0;  // dQ, or dV
+  int64_t so0_b, so0_t, so0_h;
+  void* out1;  // dK
+  int64_t so1_b, so1_t, so1_h;
+  int accum;
+  int batch, hq, hkv, n_tiles;
+  float scale;
+  int* status;
 };
 
 // q-stationary kernel: dQ = scale * sum_j dS_ij k_j
@@ -58,6 +128,8 @@ struct DkvParams {
   float scale, scale_log2;
   int* status;
 };
+
+cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* n_launches);
 
 // stages: bit 0 D preprocess, bit 1 dQ, bit 2 dK/dV
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_launches);

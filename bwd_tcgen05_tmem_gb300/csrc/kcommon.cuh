@@ -55,7 +55,7 @@ __device__ __forceinline__ Seq load_seq(const Geometry& g, int b) {
 }
 
 // Keys visible from any query in [i0, i1] (inclusive) -> [j0, j1]; empty if j1 < j0.
-__device__ __forceinline__ void key_range(const Seq& s, long long i0, long long i1, long long& j0,
+__host__ __device__ inline void key_range(const Seq& s, long long i0, long long i1, long long& j0,
                                           long long& j1) {
   j0 = i0 + s.off - s.L;
   j1 = i1 + s.off + s.R;
@@ -64,7 +64,7 @@ __device__ __forceinline__ void key_range(const Seq& s, long long i0, long long 
 }
 
 // Queries that see any key in [j0, j1] -> [i0, i1]; empty if i1 < i0.
-__device__ __forceinline__ void query_range(const Seq& s, long long j0, long long j1,
+__host__ __device__ inline void query_range(const Seq& s, long long j0, long long j1,
                                             long long& i0, long long& i1) {
   i0 = j0 - s.off - s.R;
   i1 = j1 - s.off + s.L;

@@ -27,6 +27,7 @@ enum : int {
   DEV_TIMEOUT = 1,      // an mbarrier wait exceeded its time limit
   DEV_BAD_SEQLENS = 2,  // cu_seqlens failed validation
   DEV_TMEM = 3,         // TMEM allocation returned an unusable address
+  DEV_WORKSPACE = 4,    // the score tiles of the wide backward exceed the workspace
 };
 
 // Wall-clock limit of one wait (ns).  A healthy wait lasts microseconds.
@@ -129,6 +130,17 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
       "r"(c3)
+      : "memory");
+}
+
+// Plain (non-tensor) bulk copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"((uint64_t)__cvta_generic_to_global(gsrc)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 

@@ -106,3 +106,37 @@ def test_merge_validation(lib):
     rc = lib.attn_lse_merge(0, vp, lp, r0, nr, 12, 2, 64, ctypes.c_void_p(0x9000), 0,
                             ctypes.c_void_p(0xA000), None)
     assert rc == 1
+
+
+def _visible_blocks(sq, sk, causal, wl, wr, bottom_right):
+    """Brute force: 128x128 (query tile, key block) pairs holding a visible key."""
+    off = sk - sq if bottom_right else 0
+    n = 0
+    for qt in range((sq + 127) // 128):
+        blocks = set()
+        for i in range(qt * 128, min(qt * 128 + 128, sq)):
+            lo = 0 if wl < 0 else max(0, i + off - wl)
+            hi = sk - 1
+            if causal:
+                hi = min(hi, i + off)
+            elif wr >= 0:
+                hi = min(hi, i + off + wr)
+            for j in range(lo, hi + 1, 1):
+                blocks.add(j // 128)
+        n += len(blocks)
+    return n
+
+
+@pytest.mark.parametrize("sq,sk,causal,wl,wr,br", [
+    (300, 300, True, -1, -1, False), (200, 333, True, -1, -1, True),
+    (333, 200, True, -1, -1, True), (300, 300, False, 100, 30, False),
+    (700, 700, True, 129, 0, False), (260, 260, False, -1, -1, False)])
+def test_wide_backward_workspace_counts_visible_blocks(lib, sq, sk, causal, wl, wr, br):
+    """Head dim 512: one 64 KiB block of P/dS per visible (query tile, key block)."""
+    b, hq, hkv = 2, 4, 2
+    q, k = fake((b, sq, hq, 512)), fake((b, sk, hkv, 512))
+    p = attn.make_params(q, k, k, o=q, causal=causal, window=(wl, wr), bottom_right=br)
+    base = 256 + -(-(b * sq * hq * 4) // 256) * 256
+    blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
+    blocks = b * hq * _visible_blocks(sq, sk, causal, wl, wr, br)
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == blk_off + blocks * 65536

@@ -74,6 +74,10 @@ DENSE = [
     (1, 300, 300, 2, 2, 128, 128, "bf16", False, (-1, -1), False),
     (1, 300, 300, 2, 2, 64, 64, "bf16", False, (30, 20), False),
     (1, 130, 130, 2, 2, 64, 64, "bf16", True, (0, 0), False),
+    # head dim 512: the materialising backward
+    (1, 260, 260, 4, 1, 512, 512, "bf16", True, (-1, -1), False),
+    (2, 200, 333, 2, 2, 512, 512, "fp16", True, (-1, -1), True),
+    (1, 300, 300, 2, 1, 512, 512, "bf16", False, (100, 30), False),
 ]
 
 
@@ -84,13 +88,8 @@ def test_dense(case):
     run_and_check(q, k, v, do, dtype=dtype, causal=causal, window=window, bottom_right=br)
 
 
-def test_dense_d512_forward():
-    q, k, v, do = dense_inputs(1, 260, 260, 4, 1, 512, 512, "bf16")
-    run_and_check(q, k, v, do, dtype="bf16", backward=False)
-
-
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
-@pytest.mark.parametrize("dims", [(128, 128), (192, 128), (64, 64)])
+@pytest.mark.parametrize("dims", [(128, 128), (192, 128), (64, 64), (512, 512)])
 def test_thd_varlen(dtype, dims):
     lens = [0, 1, 129, 300, 64, 200, 0]
     w = synth.Workload("t", 0, 0, 8, 2, dims[0], dims[1], dtype=dtype, thd_total=1)
@@ -112,8 +111,9 @@ def test_forward_bitwise_reproducible_and_stream_bound():
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_backward_bitwise_reproducible():
-    q, k, v, do = dense_inputs(1, 500, 500, 4, 2, 128, 128, "bf16")
+@pytest.mark.parametrize("d", [128, 512])
+def test_backward_bitwise_reproducible(d):
+    q, k, v, do = dense_inputs(1, 500, 500, 4, 2, d, d, "bf16")
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     o, lse = attn.fwd(qd, kd, vd)
     g1 = attn.bwd(qd, kd, vd, o, dod, lse)
@@ -180,7 +180,7 @@ def test_bad_cu_seqlens_reports_status():
 
 
 @pytest.mark.parametrize("cp,s,dims", [(8, 640, (192, 128)), (2, 520, (128, 128)),
-                                       (4, 1024, (64, 64))])
+                                       (4, 1024, (64, 64)), (2, 520, (512, 512))])
 def test_cp_ring_emulation_matches_full_attention(cp, s, dims):
     """Dual-chunk-swap ring: FP32 partials + LSE merge + per-step backward."""
     from bwd_tcgen05_tmem_gb300 import cp as cpmod
@@ -219,8 +219,9 @@ def test_cp_ring_equals_direct_path():
         assert err.item() < 1e-2
 
 
-def test_backward_stages_equal_full_call():
-    q, k, v, do = dense_inputs(1, 300, 300, 4, 2, 192, 128, "bf16")
+@pytest.mark.parametrize("dims", [(192, 128), (512, 512)])
+def test_backward_stages_equal_full_call(dims):
+    q, k, v, do = dense_inputs(1, 300, 300, 4, 2, dims[0], dims[1], "bf16")
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     o, lse = attn.fwd(qd, kd, vd)
     g1 = attn.bwd(qd, kd, vd, o, dod, lse)
@@ -233,8 +234,9 @@ def test_backward_stages_equal_full_call():
         assert torch.equal(a, b)
 
 
-def test_fp32_gradient_accumulate():
-    q, k, v, do = dense_inputs(1, 300, 300, 2, 2, 128, 128, "bf16")
+@pytest.mark.parametrize("d", [128, 512])
+def test_fp32_gradient_accumulate(d):
+    q, k, v, do = dense_inputs(1, 300, 300, 2, 2, d, d, "bf16")
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     o, lse = attn.fwd(qd, kd, vd)
     g = attn.bwd(qd, kd, vd, o, dod, lse, grad_dtype=torch.float32)
