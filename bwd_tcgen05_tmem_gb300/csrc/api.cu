@@ -614,6 +614,8 @@ attn_status_t attn_query_status(const void* ws, attn_stream_t stream) {
   if (v == attn::DEV_BAD_SEQLENS)
     return fail(ATTN_ERR_BAD_METADATA, "device check: cu_seqlens inconsistent");
   if (v == attn::DEV_TIMEOUT) return fail(ATTN_ERR_TIMEOUT, "device wait exceeded its limit");
+  if (v == attn::DEV_WORKSPACE)
+    return fail(ATTN_ERR_WORKSPACE, "device check: score tiles exceed the workspace");
   return fail(ATTN_ERR_CUDA, "device status %d", v);
 }
 

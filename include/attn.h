@@ -91,7 +91,12 @@ typedef struct {
 } attn_params_t;
 
 /* Bytes of workspace attn_fwd / attn_bwd need for `p` (always >= 256: the
- * status word lives at offset 0).  The workspace must be 256-byte aligned. */
+ * status word lives at offset 0).  The workspace must be 256-byte aligned.
+ * For head dims above 256 the backward also keeps P and dS of every visible
+ * 128-query x 128-key tile (64 KiB each, all query heads) in the workspace:
+ * the count is exact for dense inputs, and for THD it is a bound that takes
+ * every document's keys as max_seqlen_k long (about 8.7 GB for batch 1,
+ * 16 query heads, 16384 causal tokens). */
 size_t attn_fwd_workspace_size(const attn_params_t* p);
 size_t attn_bwd_workspace_size(const attn_params_t* p);
 
@@ -115,6 +120,10 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
  * dQ = scale dS K; dK/dV are summed over the query heads of a GQA group
  * inside the kernel.  dq/dk/dv are fully overwritten (grad_dtype).  The
  * reduction order is fixed, so the backward is bitwise reproducible.
+ * Head dim 512 (PR #3527: the d512 backward): P and dS are written once to
+ * the workspace (16-bit, as the fused kernels round them too) and the five
+ * contractions run in three kernels; a workspace whose block table does not
+ * fit sets ATTN_ERR_WORKSPACE in the status word.
  */
 attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, const void* v,
                        const void* o, const void* dout, const float* lse, void* dq, void* dk,
@@ -128,8 +137,10 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
  *   attn_bwd_dq:         dQ (reads D from the workspace);
  *   attn_bwd_dkdv:       dK and dV, reduced over each GQA group (reads D).
  * The dq and dkdv stages require a preprocess on the same workspace, for the
- * same problem, earlier on the stream.  Arguments a stage does not use may be
- * NULL.
+ * same problem, earlier on the stream.  For head dim 512 the dq stage also
+ * writes P and dS into the workspace, and the dkdv stage reads them: it then
+ * requires the dq stage earlier on the stream as well.  Arguments a stage
+ * does not use may be NULL.
  */
 attn_status_t attn_bwd_preprocess(const attn_params_t* p, const void* q, const void* k,
                                   const void* v, const void* o, const void* dout,
@@ -196,7 +207,8 @@ attn_status_t attn_lse_merge(int n_parts, const float* const* o_parts,
                              attn_stream_t stream);
 
 /* Synchronises `stream` and returns the status word in `workspace`
- * (ATTN_OK, ATTN_ERR_BAD_METADATA or ATTN_ERR_TIMEOUT). */
+ * (ATTN_OK, ATTN_ERR_BAD_METADATA, ATTN_ERR_TIMEOUT or, for the head-dim-512
+ * backward, ATTN_ERR_WORKSPACE). */
 attn_status_t attn_query_status(const void* workspace, attn_stream_t stream);
 
 /* Message of the last error returned on this thread ("" if none). */
