@@ -56,10 +56,14 @@ def flops(w, lengths=None):
     fwd = 2 * nv * (w.d_qk + w.d_v)
     bwd = 2 * nv * (3 * w.d_qk + 2 * w.d_v)
     # per-kernel attribution of the algorithmic work (sums to fwd + bwd):
-    # dK/dV kernel: S, dP, dV, dK; dQ kernel: dQ (its S/dP recompute is not credited)
-    return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd, "n_visible": nv,
-            "kernel": {"fwd": fwd, "dkdv": 2 * nv * (2 * w.d_qk + 2 * w.d_v),
-                       "dq": 2 * nv * w.d_qk}}
+    # head dims <= 256: dK/dV kernel S, dP, dV, dK; dQ kernel dQ (its S/dP
+    # recompute is not credited).  Above 256 the dq stage runs the scores
+    # kernel (S, dP) and the dQ GEMM, the dkdv stage the dV and dK GEMMs.
+    if w.d_qk > 256:
+        kern = {"fwd": fwd, "dq": 2 * nv * (2 * w.d_qk + w.d_v), "dkdv": 2 * nv * (w.d_qk + w.d_v)}
+    else:
+        kern = {"fwd": fwd, "dkdv": 2 * nv * (2 * w.d_qk + 2 * w.d_v), "dq": 2 * nv * w.d_qk}
+    return {"fwd": fwd, "bwd": bwd, "total": fwd + bwd, "n_visible": nv, "kernel": kern}
 
 
 def load_peaks():
@@ -274,14 +278,21 @@ def main():
 
     inp = synth.make_inputs(w)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "dout"))
-    fl = flops(w)
-    o = torch.empty((*q.shape[:-1], w.d_v), dtype=q.dtype, device=dev)
-    lse = torch.empty((q.shape[0], w.heads_q, q.shape[1]), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fws = torch.empty(attn.workspace_size("fwd", q, k, v), dtype=torch.uint8, device=dev)
-    bws = torch.empty(attn.workspace_size("bwd", q, k, v), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
     kw = dict(causal=True, scale=w.scale, window=w.window)
+    if w.is_thd:  # packed documents: [tokens, heads, d], LSE [heads, tokens]
+        cu = inp["cu_seqlens"].to(dev)
+        kw.update(cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=inp["max_seqlen"],
+                  max_seqlen_k=inp["max_seqlen"])
+        fl = flops(w, (inp["cu_seqlens"][1:] - inp["cu_seqlens"][:-1]).tolist())
+        lse = torch.empty((w.heads_q, q.shape[0]), dtype=torch.float32, device=dev)
+    else:
+        fl = flops(w)
+        lse = torch.empty((q.shape[0], w.heads_q, q.shape[1]), dtype=torch.float32, device=dev)
+    o = torch.empty((*q.shape[:-1], w.d_v), dtype=q.dtype, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fws = torch.empty(attn.workspace_size("fwd", q, k, v, **kw), dtype=torch.uint8, device=dev)
+    bws = torch.empty(attn.workspace_size("bwd", q, k, v, **kw), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
     stages = ("fwd", "pre", "dq", "dkdv")
 
     def step(ev=None):
@@ -358,7 +369,7 @@ def main():
 
     # ---- one-GPU context-parallel ring emulation (dual chunk swap, 8 ranks)
     cp_obj = None
-    if not args.no_cp and w.batch == 1 and w.seqlen % 16 == 0:
+    if not args.no_cp and not w.is_thd and w.batch == 1 and w.seqlen % 16 == 0:
         from bwd_tcgen05_tmem_gb300 import cp as cpmod
         ring = cpmod.CPRing(q, k, v, do, cp=8, scale=w.scale)
         for _ in range(2):
@@ -421,7 +432,7 @@ def main():
                      "unit": "TFLOP/s", "frac": ach / peak_tf, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops_sustained",
                      "work_per_launch": fl["kernel"][dom]},
-        "pre_gbs": (w.batch * w.seqlen * w.heads_q * (2 * w.d_v * 2 + 4)) /
+        "pre_gbs": (q.shape[0] * (1 if w.is_thd else q.shape[1]) * w.heads_q * (2 * w.d_v * 2 + 4)) /
                    (per_kernel["pre"] * 1e-3) / 1e9,
         "e2e": {"value": job_tflops(fl["total"], e2e_ms, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -87,8 +87,11 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = blockIdx.x;
-  const int ktile = blockIdx.y;
+  // (key tile, kv head) in the grid order of tile_major(); under a causal mask
+  // the lowest key tiles are the heaviest and start first
+  const bool tmaj = tile_major(p.n_ktiles);
+  const int g = tmaj ? blockIdx.y : blockIdx.x;
+  const int ktile = tmaj ? blockIdx.x : blockIdx.y;
   const int b = blockIdx.z;
   const int tb = p.geo.cu_q ? 0 : b;  // TMA batch coordinate (packed THD tensors have one)
   const int grp = p.hq / p.hkv;
@@ -516,7 +519,8 @@ static cudaError_t launch_dkv_t(const DkvParams& p, cudaStream_t st) {
   auto k = attn_bwd_dkdv_kernel<DQK, DV, BQ, MODE, BF16, G_F32>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.hkv, (unsigned)p.n_ktiles, (unsigned)p.batch);
+  dim3 grid = tile_major(p.n_ktiles) ? dim3((unsigned)p.n_ktiles, (unsigned)p.hkv, (unsigned)p.batch)
+                                      : dim3((unsigned)p.hkv, (unsigned)p.n_ktiles, (unsigned)p.batch);
   k<<<grid, 384, C::kSmem, st>>>(p);
   return cudaGetLastError();
 }

@@ -63,8 +63,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
   __shared__ int abort_flag, skip_sh;
 
   const int warp = threadIdx.x >> 5;
-  const int h = blockIdx.x;
-  const int tile = p.n_qtiles - 1 - blockIdx.y;
+  // (query tile, head) in the grid order of tile_major(); heaviest tiles first
+  const bool tmaj = tile_major(p.n_qtiles);
+  const int h = tmaj ? blockIdx.y : blockIdx.x;
+  const int tile = p.n_qtiles - 1 - (tmaj ? blockIdx.x : blockIdx.y);
   const int b = blockIdx.z;
   const int tb = p.geo.cu_q ? 0 : b;  // TMA batch coordinate (packed THD tensors have one)
   const int g = h / (p.hq / p.hkv);
@@ -370,7 +372,8 @@ static cudaError_t launch_dq_t(const DqParams& p, cudaStream_t st) {
   auto k = attn_bwd_dq_kernel<DQK, DV, BKV, BF16, G_F32>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.hq, (unsigned)p.n_qtiles, (unsigned)p.batch);
+  dim3 grid = tile_major(p.n_qtiles) ? dim3((unsigned)p.n_qtiles, (unsigned)p.hq, (unsigned)p.batch)
+                                      : dim3((unsigned)p.hq, (unsigned)p.n_qtiles, (unsigned)p.batch);
   k<<<grid, 384, C::kSmem, st>>>(p);
   return cudaGetLastError();
 }

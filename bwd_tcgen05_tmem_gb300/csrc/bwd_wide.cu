@@ -122,8 +122,9 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.x;
-  const int qt = p.n_qtiles - 1 - (int)blockIdx.y;
+  const bool tmaj = tile_major(p.n_qtiles);  // grid order, heaviest tiles first
+  const int h = tmaj ? blockIdx.y : blockIdx.x;
+  const int qt = p.n_qtiles - 1 - (int)(tmaj ? blockIdx.x : blockIdx.y);
   const int b = blockIdx.z;
   const int tb = p.geo.cu_q ? 0 : b;
   const int g = h / (p.hq / p.hkv);
@@ -384,10 +385,13 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int grp = p.hq / p.hkv;
-  // KIND 0: x = query head, y = query tile (heaviest first);
-  // KIND 1: x = kv head, y = key tile, z = 2 * sequence + (0: dV, 1: dK)
-  const int hx = blockIdx.x;
-  const int tile = KIND == 0 ? p.n_tiles - 1 - (int)blockIdx.y : (int)blockIdx.y;
+  // (tile, head) in the grid order of tile_major(), heaviest tiles first:
+  // KIND 0 query tile and query head, KIND 1 key tile and kv head with
+  // z = 2 * sequence + (0: dV, 1: dK)
+  const bool tmaj = tile_major(p.n_tiles);
+  const int hx = tmaj ? blockIdx.y : blockIdx.x;
+  const int tx = tmaj ? blockIdx.x : blockIdx.y;
+  const int tile = KIND == 0 ? p.n_tiles - 1 - tx : tx;
   const int b = KIND == 0 ? (int)blockIdx.z : (int)(blockIdx.z >> 1);
   const int which = KIND == 0 ? 0 : (int)(blockIdx.z & 1);
   const int tb = p.geo.cu_q ? 0 : b;
@@ -631,7 +635,9 @@ cudaError_t launch_scores_t(const WideScoresParams& p, cudaStream_t st) {
   auto k = attn_bwd_wide_scores_kernel<512, 512, BF16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  k<<<dim3((unsigned)p.hq, (unsigned)p.n_qtiles, (unsigned)p.batch), 384, C::kSmem, st>>>(p);
+  const dim3 grid = tile_major(p.n_qtiles) ? dim3((unsigned)p.n_qtiles, (unsigned)p.hq, (unsigned)p.batch)
+                                            : dim3((unsigned)p.hq, (unsigned)p.n_qtiles, (unsigned)p.batch);
+  k<<<grid, 384, C::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -641,8 +647,10 @@ cudaError_t launch_acc_t(const WideAccParams& p, cudaStream_t st) {
   auto k = attn_bwd_wide_acc_kernel<512, KIND, BF16, G_F32>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  const dim3 grid = KIND == 0 ? dim3((unsigned)p.hq, (unsigned)p.n_tiles, (unsigned)p.batch)
-                              : dim3((unsigned)p.hkv, (unsigned)p.n_tiles, (unsigned)(2 * p.batch));
+  const unsigned nh = (unsigned)(KIND == 0 ? p.hq : p.hkv);
+  const unsigned nz = (unsigned)(KIND == 0 ? p.batch : 2 * p.batch);
+  const dim3 grid = tile_major(p.n_tiles) ? dim3((unsigned)p.n_tiles, nh, nz)
+                                          : dim3(nh, (unsigned)p.n_tiles, nz);
   k<<<grid, 384, C::kSmem, st>>>(p);
   return cudaGetLastError();
 }

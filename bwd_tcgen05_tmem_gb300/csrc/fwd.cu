@@ -54,9 +54,12 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   __shared__ int abort_flag, skip_sh;
 
   const int warp = threadIdx.x >> 5;
-  const int split = blockIdx.x % p.n_split;
-  const int h = blockIdx.x / p.n_split;
-  const int tile = p.n_qtiles - 1 - blockIdx.y;
+  // (query tile, head x column split) in the grid order of tile_major()
+  const bool tmaj = tile_major(p.n_qtiles);
+  const int hs = tmaj ? blockIdx.y : blockIdx.x;
+  const int split = hs % p.n_split;
+  const int h = hs / p.n_split;
+  const int tile = p.n_qtiles - 1 - (tmaj ? blockIdx.x : blockIdx.y);
   const int b = blockIdx.z;
   const int tb = p.geo.cu_q ? 0 : b;  // TMA batch coordinate (packed THD tensors have one)
   const int g = h / (p.hq / p.hkv);
@@ -415,7 +418,9 @@ cudaError_t launch_fwd(const FwdParams& p, int dqk, int dv, bool bf16, bool o_f3
                        cudaStream_t st) {
   const int nsplit = dv > 256 ? dv / 256 : 1;
   if (p.n_split != nsplit) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)(p.hq * nsplit), (unsigned)p.n_qtiles, (unsigned)p.batch);
+  dim3 grid = tile_major(p.n_qtiles)
+                  ? dim3((unsigned)p.n_qtiles, (unsigned)(p.hq * nsplit), (unsigned)p.batch)
+                  : dim3((unsigned)(p.hq * nsplit), (unsigned)p.n_qtiles, (unsigned)p.batch);
   if (dqk == 64 && dv == 64) return launch_fwd_d<64, 64>(p, grid, bf16, o_f32, st);
   if (dqk == 128 && dv == 128) return launch_fwd_d<128, 128>(p, grid, bf16, o_f32, st);
   if (dqk == 192 && dv == 128) return launch_fwd_d<192, 128>(p, grid, bf16, o_f32, st);

@@ -22,6 +22,12 @@ constexpr int kSlotBytes = 128 * 64 * 2;
 constexpr int kMaxSlots = 14;  // 14 x 16 KiB + alignment pad fits in 227 KiB
 constexpr long long kInfBound = (1ll << 40);
 
+// Grid order.  With many tiles per head, x walks the tiles of one head so the
+// CTAs resident at one time stream the same head's operands from L2; with
+// few, x walks the heads so the heaviest tiles of every head start first.
+constexpr int kTileMajorMin = 64;
+__host__ __device__ inline bool tile_major(int n_tiles) { return n_tiles >= kTileMajorMin; }
+
 struct Geometry {
   const int32_t* cu_q;  // null: dense
   const int32_t* cu_k;

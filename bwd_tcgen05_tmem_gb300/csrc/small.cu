@@ -11,62 +11,102 @@
 namespace attn {
 
 // ----------------------------------------------------------------- D = rowsum(dO * O)
-// One warp per (token, head) row; each lane reads 16-byte vectors of O and dO.
-template <bool BF16>
+// Rows are (token, head) pairs.  LPR lanes share a row (each reads 16-byte
+// vectors of O and dO, NCH of them), so a warp covers 32/LPR rows per pass
+// with every lane busy, and kU passes are unrolled to keep 2*kU*NCH loads in
+// flight per lane: the kernel is a pure HBM stream.
+template <bool BF16, int LPR, int NCH>
 __global__ void __launch_bounds__(256) attn_pre_kernel(const PreParams p) {
+  constexpr int kRowsPerPass = 32 / LPR;
+  constexpr int kU = 4;
   if (p.status && *(volatile int*)p.status) return;
   const int lane = threadIdx.x & 31;
-  const int64_t rows = (int64_t)(p.cu_q ? p.total_q : p.batch * p.seqlen_q) * p.hq;
+  const int sub = lane / LPR, l = lane % LPR;
+  const int64_t rows = (int64_t)(p.cu_q ? p.total_q : (int64_t)p.batch * p.seqlen_q) * p.hq;
   const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t r = warp_id; r < rows; r += nwarps) {
-    const int h = (int)(r % p.hq);
-    const int64_t t = r / p.hq;  // token (dense: b*S + i)
-    int b;
-    int64_t tok;
-    if (p.cu_q) {
-      // binary search for the sequence that owns token t
-      int lo = 0, hi = p.batch;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.cu_q[mid] <= t) lo = mid; else hi = mid;
+  for (int64_t base = warp_id * (kRowsPerPass * kU); base < rows;
+       base += nwarps * (kRowsPerPass * kU)) {
+    uint4 ov[kU][NCH], dv[kU][NCH];
+    int64_t didx[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t r = base + u * kRowsPerPass + sub;
+      didx[u] = -1;
+      if (r < rows) {
+        // rows < 2^32 (checked at launch): 32-bit division
+        const uint32_t r32 = (uint32_t)r;
+        const int h = (int)(r32 % (uint32_t)p.hq);
+        const uint32_t t = r32 / (uint32_t)p.hq;  // token (dense: b*S + i)
+        int b;
+        int64_t tok;
+        if (p.cu_q) {  // the sequence that owns token t
+          int lo = 0, hi = p.batch;
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if ((uint32_t)p.cu_q[mid] <= t) lo = mid; else hi = mid;
+          }
+          b = lo;
+          tok = t;
+        } else {
+          b = (int)(t / (uint32_t)p.seqlen_q);
+          tok = t - (uint32_t)b * (uint32_t)p.seqlen_q;
+        }
+        const int64_t bb = p.cu_q ? 0 : b;
+        const uint4* orow = reinterpret_cast<const uint4*>(
+            (const uint16_t*)p.o + bb * p.so_b + tok * p.so_t + (int64_t)h * p.so_h);
+        const uint4* drow = reinterpret_cast<const uint4*>(
+            (const uint16_t*)p.dout + bb * p.sdo_b + tok * p.sdo_t + (int64_t)h * p.sdo_h);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          ov[u][c] = orow[c * LPR + l];
+          dv[u][c] = drow[c * LPR + l];
+        }
+        didx[u] = (int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok;
+      } else {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) ov[u][c] = dv[u][c] = make_uint4(0u, 0u, 0u, 0u);
       }
-      b = lo;
-      tok = t;
-    } else {
-      b = (int)(t / p.seqlen_q);
-      tok = t % p.seqlen_q;
-    }
-    const uint16_t* orow = (const uint16_t*)p.o + (int64_t)b * p.so_b * (p.cu_q ? 0 : 1) +
-                           tok * p.so_t + (int64_t)h * p.so_h;
-    const uint16_t* drow = (const uint16_t*)p.dout + (int64_t)b * p.sdo_b * (p.cu_q ? 0 : 1) +
-                           tok * p.sdo_t + (int64_t)h * p.sdo_h;
-    float acc = 0.0f;
-    for (int c = lane * 8; c < p.dv; c += 256) {
-      const uint4 ov = *reinterpret_cast<const uint4*>(orow + c);
-      const uint4 dv = *reinterpret_cast<const uint4*>(drow + c);
-      const uint16_t* oe = reinterpret_cast<const uint16_t*>(&ov);
-      const uint16_t* de = reinterpret_cast<const uint16_t*>(&dv);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc = fmaf(Pack<BF16>::to_f(oe[e]), Pack<BF16>::to_f(de[e]), acc);
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok] = acc;
+    for (int u = 0; u < kU; ++u) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const uint16_t* oe = reinterpret_cast<const uint16_t*>(&ov[u][c]);
+        const uint16_t* de = reinterpret_cast<const uint16_t*>(&dv[u][c]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(Pack<BF16>::to_f(oe[e]), Pack<BF16>::to_f(de[e]), acc);
+      }
+#pragma unroll
+      for (int s = LPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+      if (l == 0 && didx[u] >= 0) p.d[didx[u]] = acc;
+    }
   }
 }
 
+template <bool BF16>
+static cudaError_t launch_pre_t(const PreParams& p, unsigned blocks, cudaStream_t st) {
+  switch (p.dv) {
+    case 64: attn_pre_kernel<BF16, 8, 1><<<blocks, 256, 0, st>>>(p); break;
+    case 128: attn_pre_kernel<BF16, 16, 1><<<blocks, 256, 0, st>>>(p); break;
+    case 256: attn_pre_kernel<BF16, 32, 1><<<blocks, 256, 0, st>>>(p); break;
+    case 512: attn_pre_kernel<BF16, 32, 2><<<blocks, 256, 0, st>>>(p); break;
+    default: return cudaErrorNotSupported;
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pre(const PreParams& p, bool bf16, int num_sms, cudaStream_t st) {
-  const int64_t rows = (int64_t)(p.cu_q ? p.total_q : p.batch * p.seqlen_q) * p.hq;
-  int64_t blocks = (rows + 7) / 8;
-  const int64_t cap = (int64_t)num_sms * 8;
+  const int64_t rows = (int64_t)(p.cu_q ? p.total_q : (int64_t)p.batch * p.seqlen_q) * p.hq;
+  if (rows >= (int64_t(1) << 32)) return cudaErrorNotSupported;
+  const int lpr = p.dv >= 256 ? 32 : p.dv / 8;
+  const int64_t per_block = 8 * (32 / lpr) * 4;  // 8 warps x rows per pass x unroll
+  int64_t blocks = (rows + per_block - 1) / per_block;
+  const int64_t cap = (int64_t)num_sms * 8;  // 8 resident blocks per SM
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (bf16)
-    attn_pre_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(p);
-  else
-    attn_pre_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return bf16 ? launch_pre_t<true>(p, (unsigned)blocks, st) : launch_pre_t<false>(p, (unsigned)blocks, st);
 }
 
 // ----------------------------------------------------------------- LSE merge
