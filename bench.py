@@ -397,6 +397,28 @@ def main():
                   "note": "partials per ring step (FP32) + LSE merge per rank + per-step "
                           "backward with FP32 accumulation, all ranks on this GPU"}
         del ring
+        # all-gather variant: one call per local query chunk on the trimmed keys
+        ag = cpmod.CPAllGather(q, k, v, do, cp=8, scale=w.scale, window=(w.window[0], 0))
+        for _ in range(2):
+            ag.forward()
+            ag.backward()
+        torch.cuda.synchronize()
+        fwd_ms = bwd_ms = 0.0
+        for _ in range(n_cp):
+            c0.record(stream)
+            ag.forward()
+            c1.record(stream)
+            ag.backward()
+            c2.record(stream)
+            torch.cuda.synchronize()
+            fwd_ms += c0.elapsed_time(c1) / n_cp
+            bwd_ms += c1.elapsed_time(c2) / n_cp
+        cp_obj["allgather"] = {
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "ms": fwd_ms + bwd_ms,
+            "tflops": fl["total"] / ((fwd_ms + bwd_ms) * 1e-3) / 1e12, "launches": ag.launches,
+            "note": "KV gathered and trimmed per query chunk, bottom-right causal, no LSE "
+                    "merge; dK/dV partials summed in FP32 (the reduce-scatter), one GPU"}
+        del ag
 
     peaks, peak_src = load_peaks()
     peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))

@@ -186,8 +186,9 @@ def _lse_shape(q, thd):
 
 def fwd(q, k, v, *, causal=True, scale=None, window=(-1, -1), bottom_right=False,
         cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
-        out=None, lse=None, o_dtype=None, workspace=None, stream=None):
-    """Fused attention forward. Returns (o, lse)."""
+        out=None, lse=None, o_dtype=None, lse_strides=(0, 0), workspace=None, stream=None):
+    """Fused attention forward. Returns (o, lse).  lse_strides: element strides
+    {batch, head} of `lse` ((0, 0) = its default layout)."""
     lib = load()
     thd = cu_seqlens_q is not None
     odt = o_dtype if o_dtype is not None else (out.dtype if out is not None else q.dtype)
@@ -199,7 +200,7 @@ def fwd(q, k, v, *, causal=True, scale=None, window=(-1, -1), bottom_right=False
     p = make_params(q, k, v, causal=causal, scale=scale, window=window,
                     bottom_right=bottom_right, cu_seqlens_q=cu_seqlens_q,
                     cu_seqlens_k=cu_seqlens_k, max_seqlen_q=max_seqlen_q,
-                    max_seqlen_k=max_seqlen_k, o=out, o_dtype=odt)
+                    max_seqlen_k=max_seqlen_k, o=out, o_dtype=odt, lse_strides=lse_strides)
     need = lib.attn_fwd_workspace_size(ctypes.byref(p))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

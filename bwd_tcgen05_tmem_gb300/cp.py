@@ -162,3 +162,97 @@ class CPRing:
                 n += attn.last_launch_count()
         self.launches += n
         return self.dq, self.dk, self.dv
+
+
+def allgather_pieces(cp: int, chunk: int, window_left: int = -1):
+    """The per-rank calls of the all-gather CP variant: (rank, local query
+    rows (first, count), global key range (first, end)).
+
+    After the all-gather every rank holds all of K/V; for its query chunk c
+    (global rows [c*chunk, (c+1)*chunk)) it keeps only the keys the chunk can
+    see, [max(0, c*chunk - L), (c+1)*chunk) with L = window_left (unbounded if
+    < 0), and runs one call with BOTTOM-RIGHT causal alignment, which places the
+    diagonal at the end of that trimmed range (TransformerEngine PR #3527 review
+    notes on all_gather: KV gathered and trimmed, a per-step window causal
+    relative to the trimmed range, no LSE correction).  The window's left bound
+    counts from the diagonal, so it is the same in the trimmed frame."""
+    out = []
+    for r in range(cp):
+        pcs = []
+        for local, c in enumerate((r, 2 * cp - 1 - r)):
+            k_end = (c + 1) * chunk
+            k_first = 0 if window_left < 0 else max(0, c * chunk - window_left)
+            pcs.append((r, (local * chunk, chunk), (k_first, k_end)))
+        out.append(pcs)
+    return out
+
+
+class CPAllGather:
+    """One-GPU emulation of the all-gather CP variant with the dual-chunk-swap
+    layout: rank r holds query chunks r and 2cp-1-r, gathers the whole K/V
+    (here: the full tensors are already on this GPU) and calls attn_fwd /
+    attn_bwd once per local chunk on the trimmed keys.  dQ of a chunk is
+    complete after its call; the dK/dV of the trimmed range are partial sums
+    that a real system reduce-scatters to the owners; here every call adds
+    them (FP32, ``accumulate``) into full-sequence dK/dV buffers.
+
+    q/k/v/dout: dense [1, S, H, d] device tensors.  ``window`` = (left, right)
+    with right 0 or -1 (causal); left -1 = unbounded."""
+
+    def __init__(self, q, k, v, dout, cp=8, scale=None, window=(-1, 0)):
+        assert q.shape[0] == 1, "the emulation runs batch 1"
+        self.cp = cp
+        self.scale = scale
+        self.window = (window[0], 0)
+        self.chunk = q.shape[1] // (2 * cp)
+        self.k_full, self.v_full = k, v
+        self.q, self.do = shard(q, cp), shard(dout, cp)
+        self.pieces = allgather_pieces(cp, self.chunk, window[0])
+        dev = q.device
+        hq, dv = q.shape[2], v.shape[3]
+        rows = 2 * self.chunk
+        self.o = [torch.empty((1, rows, hq, dv), dtype=q.dtype, device=dev) for _ in range(cp)]
+        self.lse = [torch.empty((1, hq, rows), dtype=torch.float32, device=dev) for _ in range(cp)]
+        self.dq = [torch.empty((1, rows, *q.shape[2:]), dtype=torch.float32, device=dev)
+                   for _ in range(cp)]
+        self.dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        self.dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+        self.fwd_ws = torch.empty(256, dtype=torch.uint8, device=dev)
+        need = max(attn.workspace_size("bwd", self.q[0][:, :self.chunk], k[:, k0:k1],
+                                       v[:, k0:k1], causal=True, bottom_right=True,
+                                       window=self.window)
+                   for pcs in self.pieces for _, _, (k0, k1) in pcs)
+        self.bwd_ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self.launches = 0
+
+    def forward(self):
+        n = 0
+        for r, pcs in enumerate(self.pieces):
+            for _, (q0, nq), (k0, k1) in pcs:
+                attn.fwd(self.q[r][:, q0:q0 + nq], self.k_full[:, k0:k1], self.v_full[:, k0:k1],
+                         causal=True, bottom_right=True, window=self.window, scale=self.scale,
+                         out=self.o[r][:, q0:q0 + nq], lse=self.lse[r][:, :, q0:q0 + nq],
+                         lse_strides=(0, 2 * self.chunk), workspace=self.fwd_ws)
+                n += attn.last_launch_count()
+        self.launches = n
+        return self.o, self.lse
+
+    def backward(self):
+        """dQ per chunk; dK/dV summed over every chunk's trimmed range.  The
+        library's accumulate flag covers all three gradients, so the FP32
+        buffers start from zero."""
+        for t in (*self.dq, self.dk, self.dv):
+            t.zero_()
+        n = 0
+        rows = 2 * self.chunk
+        for r, pcs in enumerate(self.pieces):
+            for _, (q0, nq), (k0, k1) in pcs:
+                attn.bwd(self.q[r][:, q0:q0 + nq], self.k_full[:, k0:k1], self.v_full[:, k0:k1],
+                         self.o[r][:, q0:q0 + nq], self.do[r][:, q0:q0 + nq],
+                         self.lse[r][:, :, q0:], causal=True, bottom_right=True,
+                         window=self.window, scale=self.scale, dq=self.dq[r][:, q0:q0 + nq],
+                         dk=self.dk[:, k0:k1], dv=self.dv[:, k0:k1], grad_dtype=torch.float32,
+                         accumulate=True, lse_strides=(0, rows), workspace=self.bwd_ws)
+                n += attn.last_launch_count()
+        self.launches += n
+        return self.dq, self.dk, self.dv

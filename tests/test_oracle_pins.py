@@ -336,6 +336,41 @@ def test_lse_merge_of_chunk_pairs_equals_full():
         np.testing.assert_allclose(lse, full_l[:, qr], atol=1e-12)
 
 
+@pytest.mark.parametrize("wl", [-1, 5])
+def test_allgather_trimmed_calls_equal_full(wl):
+    """All-gather CP decomposition: per query chunk, the trimmed key range with
+    bottom-right causal alignment (and the same window) reproduces the full
+    causal attention exactly; the per-chunk dK/dV partials sum to the full
+    dK/dV (TransformerEngine PR #3527 review notes on all_gather)."""
+    from bwd_tcgen05_tmem_gb300 import cp as cpmod
+    s, ncp, hq, hkv = 48, 3, 2, 1
+    q, k, v, do = rand(s, hq, 8), rand(s, hkv, 8), rand(s, hkv, 6), rand(s, hq, 6)
+    kw = dict(scale=0.4, causal=True, window=(wl, -1))
+    full_o, full_l = oracle.fwd(q, k, v, [0, s], [0, s], **kw)
+    fdq, fdk, fdv = oracle.bwd(q, k, v, do, [0, s], [0, s], **kw)
+    c = s // (2 * ncp)
+    dk, dv = np.zeros_like(fdk), np.zeros_like(fdv)
+    seen = np.zeros(s, dtype=bool)
+    for pcs in cpmod.allgather_pieces(ncp, c, wl):
+        for r, (q0, nq), (k0, k1) in pcs:
+            # local row q0 of rank r is global chunk r (q0 = 0) or 2cp-1-r (q0 = c)
+            g0 = (r if q0 == 0 else 2 * ncp - 1 - r) * c
+            qr = slice(g0, g0 + nq)
+            kr = slice(k0, k1)
+            kwp = dict(kw, bottom_right=True)
+            o, lse = oracle.fwd(q[qr], k[kr], v[kr], [0, nq], [0, k1 - k0], **kwp)
+            pdq, pdk, pdv = oracle.bwd(q[qr], k[kr], v[kr], do[qr], [0, nq], [0, k1 - k0], **kwp)
+            np.testing.assert_allclose(o, full_o[qr], atol=1e-12)
+            np.testing.assert_allclose(lse, full_l[:, qr], atol=1e-12)
+            np.testing.assert_allclose(pdq, fdq[qr], atol=1e-12)
+            dk[kr] += pdk
+            dv[kr] += pdv
+            seen[qr] = True
+    assert seen.all()  # the chunks cover every query row exactly
+    np.testing.assert_allclose(dk, fdk, atol=1e-12)
+    np.testing.assert_allclose(dv, fdv, atol=1e-12)
+
+
 def test_lse_merge_neg_inf_parts():
     o_parts = rand(3, 4, 2, 5)
     l_parts = rand(3, 2, 4)
