@@ -83,12 +83,30 @@ def unshard_lse(shards, cp):
     return torch.cat(parts, dim=2)
 
 
+class _Streams:
+    """One CUDA stream per emulated rank, forked from and joined back into the
+    caller's current stream, so the ranks' launches overlap on the GPU."""
+
+    def __init__(self, n, device):
+        self.s = [torch.cuda.Stream(device=device) for _ in range(n)]
+
+    def fork(self):
+        cur = torch.cuda.current_stream()
+        for st in self.s:
+            st.wait_stream(cur)
+
+    def join(self):
+        cur = torch.cuda.current_stream()
+        for st in self.s:
+            cur.wait_stream(st)
+
+
 class CPRing:
     """Holds per-rank shards and the buffers of one emulated CP fwd+bwd.
 
     q/k/v/dout: dense [1, S, H, d] device tensors (batch 1, as the pages'
     32K benchmark).  Buffers are allocated once; ``forward``/``backward`` only
-    launch kernels.
+    launch kernels, each rank on its own stream (each with its own workspace).
     """
 
     def __init__(self, q, k, v, dout, cp=8, scale=None):
@@ -115,27 +133,31 @@ class CPRing:
                    for _ in range(cp)]
         self.dv = [torch.zeros((1, rows, *v.shape[2:]), dtype=torch.float32, device=dev)
                    for _ in range(cp)]
-        self.fwd_ws = torch.empty(256, dtype=torch.uint8, device=dev)
+        self.fwd_ws = [torch.empty(256, dtype=torch.uint8, device=dev) for _ in range(cp)]
         need = max(attn.workspace_size("bwd", self.q[0], self.k[0], self.v[0]), 256)
-        self.bwd_ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        self.bwd_ws = [torch.empty(need, dtype=torch.uint8, device=dev) for _ in range(cp)]
+        self.streams = _Streams(cp, dev)
         self.launches = 0
 
     def forward(self):
-        """Partials per ring step, then one LSE merge per rank."""
+        """Partials per ring step, then one LSE merge per rank (rank r on stream r)."""
         n = 0
+        self.streams.fork()
         for r, pcs in enumerate(self.pieces):
+            st = self.streams.s[r]
             for i, pc in enumerate(pcs):
                 q0, nq = pc.q_rows
                 k0, nk = pc.k_rows
                 attn.fwd(self.q[r][:, q0:q0 + nq], self.k[pc.src][:, k0:k0 + nk],
                          self.v[pc.src][:, k0:k0 + nk], causal=pc.causal, scale=self.scale,
                          out=self.o_part[r][i], lse=self.lse_part[r][i],
-                         workspace=self.fwd_ws)
+                         workspace=self.fwd_ws[r], stream=st)
                 n += attn.last_launch_count()
             attn.lse_merge([t[0] for t in self.o_part[r]], [t[0] for t in self.lse_part[r]],
                            [pc.q_rows[0] for pc in pcs], [pc.q_rows[1] for pc in pcs],
-                           2 * self.chunk, out=self.o[r][0], lse_out=self.lse[r][0])
+                           2 * self.chunk, out=self.o[r][0], lse_out=self.lse[r][0], stream=st)
             n += attn.last_launch_count()
+        self.streams.join()
         self.launches = n
         return self.o, self.lse
 
@@ -144,11 +166,21 @@ class CPRing:
 
         Step 0 of every rank covers all of its query rows and all of its own key
         rows, so the step-0 calls (run first) overwrite every gradient element
-        and the later steps accumulate into them: no zero fill is needed."""
+        and the later steps accumulate into them: no zero fill is needed.
+
+        Rank r runs on stream r.  Its step s adds into the dK/dV shard of rank
+        (r - s) mod cp, which rank r - 1 added into at step s - 1, so each call
+        waits for that one call (an event) and nothing else."""
         n = 0
         rows = 2 * self.chunk
-        for s in range(self.cp):
-            for r in range(self.cp):
+        cp = self.cp
+        done = [[None] * cp for _ in range(cp)]
+        self.streams.fork()
+        for s in range(cp):
+            for r in range(cp):
+                st = self.streams.s[r]
+                if s > 0:
+                    st.wait_event(done[s - 1][(r - 1) % cp])
                 pc = self.pieces[r][s]
                 q0, nq = pc.q_rows
                 k0, nk = pc.k_rows
@@ -158,8 +190,12 @@ class CPRing:
                          self.do[r][:, q0:q0 + nq], lse, causal=pc.causal, scale=self.scale,
                          dq=self.dq[r][:, q0:q0 + nq], dk=self.dk[pc.src][:, k0:k0 + nk],
                          dv=self.dv[pc.src][:, k0:k0 + nk], grad_dtype=torch.float32,
-                         accumulate=s > 0, lse_strides=(0, rows), workspace=self.bwd_ws)
+                         accumulate=s > 0, lse_strides=(0, rows), workspace=self.bwd_ws[r],
+                         stream=st)
                 n += attn.last_launch_count()
+                done[s][r] = torch.cuda.Event()
+                done[s][r].record(st)
+        self.streams.join()
         self.launches += n
         return self.dq, self.dk, self.dv
 
@@ -226,6 +262,8 @@ class CPAllGather:
         self.launches = 0
 
     def forward(self):
+        """One call per local query chunk, in order on the current stream (the
+        calls are large enough to fill the GPU one at a time)."""
         n = 0
         for r, pcs in enumerate(self.pieces):
             for _, (q0, nq), (k0, k1) in pcs:
@@ -240,7 +278,8 @@ class CPAllGather:
     def backward(self):
         """dQ per chunk; dK/dV summed over every chunk's trimmed range.  The
         library's accumulate flag covers all three gradients, so the FP32
-        buffers start from zero."""
+        buffers start from zero.  Every call adds into the shared dK/dV, so
+        the calls run in order on the current stream."""
         for t in (*self.dq, self.dk, self.dv):
             t.zero_()
         n = 0
