@@ -419,6 +419,39 @@ def main():
             "note": "KV gathered and trimmed per query chunk, bottom-right causal, no LSE "
                     "merge; dK/dV partials summed in FP32 (the reduce-scatter), one GPU"}
         del ag
+        # all-to-all variant: relayout to head shards, full-sequence attention per rank
+        a2a = cpmod.CPA2A(q, k, v, do, cp=8, scale=w.scale, window=(w.window[0], 0))
+        for _ in range(2):
+            a2a.forward()
+            a2a.backward()
+        torch.cuda.synchronize()
+        fwd_ms = bwd_ms = 0.0
+        for _ in range(n_cp):
+            c0.record(stream)
+            a2a.forward()
+            c1.record(stream)
+            a2a.backward()
+            c2.record(stream)
+            torch.cuda.synchronize()
+            fwd_ms += c0.elapsed_time(c1) / n_cp
+            bwd_ms += c1.elapsed_time(c2) / n_cp
+        # the relayout kernel alone: Q to head shards (read + write bytes)
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(5):
+            attn.cp_relayout(a2a.q_seq, a2a.q_h, to_heads=True, cp=8)
+        r1.record(stream)
+        torch.cuda.synchronize()
+        rl_ms = r0.elapsed_time(r1) / 5
+        cp_obj["a2a"] = {
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "ms": fwd_ms + bwd_ms,
+            "tflops": fl["total"] / ((fwd_ms + bwd_ms) * 1e-3) / 1e12, "launches": a2a.launches,
+            "relayout_q_ms": rl_ms,
+            "relayout_q_gbs": 2 * q.numel() * q.element_size() / (rl_ms * 1e-3) / 1e9,
+            "note": "sequence shards -> head shards (attn_cp_relayout), attention over the "
+                    "whole sequence for H/cp heads per rank, outputs and gradients back"}
+        del a2a
 
     peaks, peak_src = load_peaks()
     peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))

@@ -29,7 +29,7 @@ _STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
            6: "ATTN_ERR_TIMEOUT", 7: "ATTN_ERR_CUDA"}
 EXPORTED = ["attn_fwd_workspace_size", "attn_bwd_workspace_size", "attn_fwd", "attn_bwd",
             "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkdv", "attn_bwd_noalloc",
-            "attn_lse_merge",
+            "attn_lse_merge", "attn_cp_relayout",
             "attn_query_status", "attn_last_error", "attn_last_launch_count"]
 
 
@@ -92,6 +92,10 @@ def load():
                                        i64p, i64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                        vp, ctypes.c_int, vp, vp]
         lib.attn_lse_merge.restype = ctypes.c_int
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.attn_cp_relayout.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, vp, i64p, vp, i64p, vp]
+        lib.attn_cp_relayout.restype = ctypes.c_int
         lib.attn_query_status.argtypes = [vp, vp]
         lib.attn_query_status.restype = ctypes.c_int
         lib.attn_last_error.argtypes = []
@@ -301,3 +305,28 @@ def lse_merge(o_parts, lse_parts, row0, nrows, rows, *, out=None, lse_out=None,
 def query_status(workspace, stream=None):
     """Synchronise the stream and raise if the device status word is set."""
     _check(load().attn_query_status(_ptr(workspace), _stream(stream)))
+
+
+def cp_relayout(src, dst, *, to_heads, cp, stream=None):
+    """All-to-all CP relayout between sequence shards and head shards.
+
+    Token-major tensors (Q, K, V, O, dO, gradients): sequence side
+    [cp, 2*chunk, heads, d], head side [cp, seqlen, heads/cp, d].
+    LSE-like FP32 tensors (head-major): sequence side [cp, heads, 2*chunk],
+    head side [cp, heads/cp, seqlen].  to_heads: src is the sequence side."""
+    seq, head = (src, dst) if to_heads else (dst, src)
+    if seq.dim() == 4:  # [cp, tokens, heads, d]
+        seqlen, heads, d = head.shape[1], seq.shape[2], seq.shape[3]
+        ss = (seq.stride(0), seq.stride(1), seq.stride(2))
+        hs = (head.stride(0), head.stride(1), head.stride(2))
+        assert seq.stride(3) == 1 and head.stride(3) == 1, "d must be contiguous"
+    else:  # [cp, heads, tokens]
+        seqlen, heads, d = head.shape[2], seq.shape[1], 1
+        ss = (seq.stride(0), seq.stride(2), seq.stride(1))
+        hs = (head.stride(0), head.stride(2), head.stride(1))
+    assert src.dtype == dst.dtype
+    arr = ctypes.c_int64 * 3
+    s_src, s_dst = (arr(*ss), arr(*hs)) if to_heads else (arr(*hs), arr(*ss))
+    _check(load().attn_cp_relayout(int(bool(to_heads)), cp, seqlen, heads, d, src.element_size(),
+                                   _ptr(src), s_src, _ptr(dst), s_dst, _stream(stream)))
+    return dst

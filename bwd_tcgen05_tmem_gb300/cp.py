@@ -295,3 +295,76 @@ class CPAllGather:
                 n += attn.last_launch_count()
         self.launches += n
         return self.dq, self.dk, self.dv
+
+
+class CPA2A:
+    """One-GPU emulation of the all-to-all (head-parallel) CP variant
+    (TransformerEngine PR #3527 review notes on a2a: after the all-to-all each
+    rank holds the full sequence for a subset of heads, so there is no ring
+    and no LSE correction, and a window applies unchanged).
+
+    The ranks' inputs are the dual-chunk-swap sequence shards, stacked
+    [cp, 2*chunk, H, d].  ``attn_cp_relayout`` moves them to head shards
+    [cp, S, H/cp, d] (the all-to-all of cp ranks held on one GPU), every rank
+    runs attn_fwd / attn_bwd over the whole sequence for its heads, and O, LSE
+    and the gradients move back to the sequence shards.  Query and key/value
+    head counts must both divide by cp."""
+
+    def __init__(self, q, k, v, dout, cp=8, scale=None, window=(-1, 0)):
+        assert q.shape[0] == 1, "the emulation runs batch 1"
+        s, hq, dqk = q.shape[1:]
+        hkv, dv = k.shape[2], v.shape[3]
+        assert hq % cp == 0 and hkv % cp == 0, "head counts must divide by cp"
+        self.cp, self.scale, self.window = cp, scale, (window[0], 0)
+        self.chunk = s // (2 * cp)
+        stack = lambda x: torch.stack([t[0] for t in shard(x, cp)])  # noqa: E731
+        self.q_seq, self.k_seq, self.v_seq, self.do_seq = (stack(t) for t in (q, k, v, dout))
+        dev, dt = q.device, q.dtype
+        e = lambda *shape, dtype=dt: torch.empty(shape, dtype=dtype, device=dev)  # noqa: E731
+        self.q_h, self.k_h, self.v_h = e(cp, s, hq // cp, dqk), e(cp, s, hkv // cp, dqk), \
+            e(cp, s, hkv // cp, dv)
+        self.do_h, self.o_h = e(cp, s, hq // cp, dv), e(cp, s, hq // cp, dv)
+        self.lse_h = e(cp, hq // cp, s, dtype=torch.float32)
+        self.dq_h, self.dk_h, self.dv_h = (torch.empty_like(t) for t in (self.q_h, self.k_h, self.v_h))
+        self.o_seq = e(cp, 2 * self.chunk, hq, dv)
+        self.lse_seq = e(cp, hq, 2 * self.chunk, dtype=torch.float32)
+        self.dq_seq, self.dk_seq, self.dv_seq = (torch.empty_like(t) for t in
+                                                 (self.q_seq, self.k_seq, self.v_seq))
+        self.fwd_ws = torch.empty(256, dtype=torch.uint8, device=dev)
+        need = attn.workspace_size("bwd", self.q_h[:1], self.k_h[:1], self.v_h[:1],
+                                   causal=True, window=self.window)
+        self.bwd_ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self.launches = 0
+
+    def _kw(self):
+        return dict(causal=True, window=self.window, scale=self.scale)
+
+    def forward(self):
+        n = 0
+        for src, dst in ((self.q_seq, self.q_h), (self.k_seq, self.k_h), (self.v_seq, self.v_h)):
+            attn.cp_relayout(src, dst, to_heads=True, cp=self.cp)
+            n += 1
+        for r in range(self.cp):
+            sl = slice(r, r + 1)
+            attn.fwd(self.q_h[sl], self.k_h[sl], self.v_h[sl], out=self.o_h[sl],
+                     lse=self.lse_h[sl], workspace=self.fwd_ws, **self._kw())
+            n += attn.last_launch_count()
+        attn.cp_relayout(self.o_h, self.o_seq, to_heads=False, cp=self.cp)
+        attn.cp_relayout(self.lse_h, self.lse_seq, to_heads=False, cp=self.cp)
+        self.launches = n + 2
+        return self.o_seq, self.lse_seq
+
+    def backward(self):
+        attn.cp_relayout(self.do_seq, self.do_h, to_heads=True, cp=self.cp)
+        n = 1
+        for r in range(self.cp):
+            sl = slice(r, r + 1)
+            attn.bwd(self.q_h[sl], self.k_h[sl], self.v_h[sl], self.o_h[sl], self.do_h[sl],
+                     self.lse_h[sl], dq=self.dq_h[sl], dk=self.dk_h[sl], dv=self.dv_h[sl],
+                     workspace=self.bwd_ws, **self._kw())
+            n += attn.last_launch_count()
+        for src, dst in ((self.dq_h, self.dq_seq), (self.dk_h, self.dk_seq), (self.dv_h, self.dv_seq)):
+            attn.cp_relayout(src, dst, to_heads=False, cp=self.cp)
+            n += 1
+        self.launches += n
+        return self.dq_seq, self.dk_seq, self.dv_seq

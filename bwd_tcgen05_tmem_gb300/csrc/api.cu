@@ -604,6 +604,48 @@ attn_status_t attn_lse_merge(int n_parts, const float* const* o_parts,
   return ATTN_OK;
 }
 
+attn_status_t attn_cp_relayout(int to_heads, int cp, int64_t seqlen, int heads, int d,
+                               int elem_bytes, const void* src, const int64_t src_strides[3],
+                               void* dst, const int64_t dst_strides[3], attn_stream_t stream) {
+  g_err[0] = 0;
+  g_launches = 0;
+  if (cp < 1 || heads < 1 || d < 1 || seqlen < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "cp, heads, d and seqlen must be positive");
+  if (seqlen % (2 * (int64_t)cp)) return fail(ATTN_ERR_INVALID_ARG, "seqlen must split into 2*cp chunks");
+  if (heads % cp) return fail(ATTN_ERR_INVALID_ARG, "heads must divide by cp");
+  if (elem_bytes != 2 && elem_bytes != 4) return fail(ATTN_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
+  if (!src || !dst || !src_strides || !dst_strides) return fail(ATTN_ERR_INVALID_ARG, "NULL argument");
+  if ((uintptr_t)src % elem_bytes || (uintptr_t)dst % elem_bytes)
+    return fail(ATTN_ERR_ALIGNMENT, "pointers must be aligned to elem_bytes");
+  for (int i = 0; i < 3; ++i)
+    if (src_strides[i] < 0 || dst_strides[i] < 0) return fail(ATTN_ERR_INVALID_ARG, "negative stride");
+  // extents of both sides (elements), for the overlap check
+  const int64_t chunk = seqlen / (2 * cp);
+  const int64_t* ss = to_heads ? src_strides : dst_strides;  // sequence side
+  const int64_t* hs = to_heads ? dst_strides : src_strides;  // head side
+  const int64_t seq_last = (cp - 1) * ss[0] + (2 * chunk - 1) * ss[1] + (int64_t)(heads - 1) * ss[2] + d;
+  const int64_t head_last = (cp - 1) * hs[0] + (seqlen - 1) * hs[1] + (int64_t)(heads / cp - 1) * hs[2] + d;
+  const Span s_src{(uintptr_t)src, (uintptr_t)src + (uintptr_t)((to_heads ? seq_last : head_last) * elem_bytes)};
+  const Span s_dst{(uintptr_t)dst, (uintptr_t)dst + (uintptr_t)((to_heads ? head_last : seq_last) * elem_bytes)};
+  if (overlap(s_src, s_dst)) return fail(ATTN_ERR_INVALID_ARG, "src and dst overlap");
+  attn::RelayoutParams rp;
+  memset(&rp, 0, sizeof(rp));
+  rp.src = (const uint8_t*)src;
+  rp.dst = (uint8_t*)dst;
+  memcpy(rp.seq_s, ss, sizeof(rp.seq_s));
+  memcpy(rp.head_s, hs, sizeof(rp.head_s));
+  rp.seqlen = seqlen;
+  rp.cp = cp;
+  rp.heads = heads;
+  rp.d = d;
+  rp.elem_bytes = elem_bytes;
+  rp.to_heads = to_heads ? 1 : 0;
+  cudaError_t e = attn::launch_relayout(rp, num_sms(), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "relayout kernel launch");
+  g_launches = 1;
+  return ATTN_OK;
+}
+
 attn_status_t attn_query_status(const void* ws, attn_stream_t stream) {
   if (!ws) return fail(ATTN_ERR_INVALID_ARG, "workspace is NULL");
   int v = 0;

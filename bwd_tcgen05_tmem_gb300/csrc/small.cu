@@ -4,7 +4,11 @@
 //   * attn_merge_kernel: LSE-weighted merge of partial results
 //                        (PR #3527: the context-parallel ring correction);
 //   * attn_check_kernel: device validation of cu_seqlens (PR #3699: every
-//                        execution checks the packed-layout metadata on device).
+//                        execution checks the packed-layout metadata on device);
+//   * attn_relayout_kernel: the local data movement of the all-to-all
+//                        context-parallel path (PR #3527: after the all-to-all
+//                        each rank holds the full sequence for a subset of
+//                        heads), sequence shards <-> head shards, bit-preserving.
 #include "kcommon.cuh"
 #include "small_params.h"
 
@@ -207,6 +211,66 @@ __global__ void __launch_bounds__(256) attn_check_kernel(const CheckParams p) {
 
 cudaError_t launch_check(const CheckParams& p, cudaStream_t st) {
   attn_check_kernel<<<1, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn
+
+namespace attn {
+
+// ----------------------------------------------------------------- CP relayout
+// One (token, head) row of d elements per warp pass; VEC = 16-byte vectors
+// (d * elem_bytes a multiple of 16 and 16-byte-aligned rows) or single
+// elements of elem_bytes.  Pure copy: every bit is preserved.
+template <bool VEC>
+__global__ void __launch_bounds__(256) attn_relayout_kernel(const RelayoutParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t chunk = p.seqlen / (2 * p.cp);
+  const int hpr = p.heads / p.cp;  // heads per rank on the head side
+  const int64_t rows = p.seqlen * p.heads;
+  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int row_bytes = p.d * p.elem_bytes;
+  for (int64_t r = warp_id; r < rows; r += nwarps) {
+    const int64_t t = r / p.heads;  // global token
+    const int h = (int)(r - t * p.heads);
+    const int64_t ch = t / chunk, u = t - ch * chunk;
+    // sequence side: owner rank and local token of global token t
+    const int64_t srank = ch < p.cp ? ch : 2 * p.cp - 1 - ch;
+    const int64_t stok = ch < p.cp ? u : chunk + u;
+    const int64_t seq_off = srank * p.seq_s[0] + stok * p.seq_s[1] + (int64_t)h * p.seq_s[2];
+    const int64_t head_off = (int64_t)(h / hpr) * p.head_s[0] + t * p.head_s[1] +
+                             (int64_t)(h % hpr) * p.head_s[2];
+    const uint8_t* src = p.src + (p.to_heads ? seq_off : head_off) * p.elem_bytes;
+    uint8_t* dst = p.dst + (p.to_heads ? head_off : seq_off) * p.elem_bytes;
+    if (VEC) {
+      for (int c = lane * 16; c < row_bytes; c += 32 * 16)
+        *reinterpret_cast<uint4*>(dst + c) = *reinterpret_cast<const uint4*>(src + c);
+    } else {
+      for (int c = lane * p.elem_bytes; c < row_bytes; c += 32 * p.elem_bytes) {
+        if (p.elem_bytes == 4)
+          *reinterpret_cast<uint32_t*>(dst + c) = *reinterpret_cast<const uint32_t*>(src + c);
+        else
+          *reinterpret_cast<uint16_t*>(dst + c) = *reinterpret_cast<const uint16_t*>(src + c);
+      }
+    }
+  }
+}
+
+cudaError_t launch_relayout(const RelayoutParams& p, int num_sms, cudaStream_t st) {
+  const int64_t rows = p.seqlen * p.heads;
+  int64_t blocks = (rows + 7) / 8;
+  const int64_t cap = (int64_t)num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  bool vec = (p.d * p.elem_bytes) % 16 == 0 && ((uintptr_t)p.src % 16) == 0 &&
+             ((uintptr_t)p.dst % 16) == 0;
+  for (int i = 0; i < 3; ++i)
+    vec = vec && (p.seq_s[i] * p.elem_bytes) % 16 == 0 && (p.head_s[i] * p.elem_bytes) % 16 == 0;
+  if (vec)
+    attn_relayout_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(p);
+  else
+    attn_relayout_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -37,7 +37,23 @@ struct CheckParams {
   int* status;
 };
 
+// Context-parallel all-to-all relayout: sequence shards <-> head shards.
+// Sequence side: rank r holds chunks r and 2cp-1-r (chunk = seqlen / 2cp) as
+// its local tokens [0, 2*chunk); head side: rank r holds heads
+// [r*heads/cp, (r+1)*heads/cp) of every token in sequence order.  Strides are
+// in elements {rank, token, head}; the d elements of one (token, head) are
+// contiguous.
+struct RelayoutParams {
+  const uint8_t* src;
+  uint8_t* dst;
+  int64_t seq_s[3], head_s[3];  // strides of the sequence-side / head-side tensors
+  int64_t seqlen;
+  int cp, heads, d, elem_bytes;
+  int to_heads;  // 1: sequence side -> head side, 0: head side -> sequence side
+};
+
 cudaError_t launch_pre(const PreParams& p, bool bf16, int num_sms, cudaStream_t st);
+cudaError_t launch_relayout(const RelayoutParams& p, int num_sms, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t st);
 cudaError_t launch_check(const CheckParams& p, cudaStream_t st);
 

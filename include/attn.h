@@ -206,6 +206,27 @@ attn_status_t attn_lse_merge(int n_parts, const float* const* o_parts,
                              void* o_out, attn_dtype_t o_dtype, float* lse_out,
                              attn_stream_t stream);
 
+/*
+ * Local data movement of the all-to-all context-parallel path (PR #3527: after
+ * the all-to-all each rank holds the full sequence for a subset of heads), for
+ * the cp ranks of a dual-chunk-swap layout held in device memory:
+ *   sequence side: rank r holds global chunks r and 2cp-1-r (chunk =
+ *     seqlen / (2 cp)) as its local tokens [0, chunk) and [chunk, 2 chunk),
+ *     all `heads` heads;
+ *   head side:     rank r holds heads [r*heads/cp, (r+1)*heads/cp) of every
+ *     token, in sequence order.
+ * to_heads = 1 copies sequence side -> head side (src is the sequence side),
+ * 0 the reverse.  Each side is described by element strides {rank, token,
+ * head}; the d elements of one (token, head) are contiguous and elem_bytes
+ * wide (2 for BF16/FP16 tensors, 4 for FP32 such as LSE, which is d = 1 with
+ * head-major strides).  A bit-preserving copy; src and dst must not overlap.
+ * Requirements: cp >= 1, seqlen a positive multiple of 2 cp, heads % cp == 0,
+ * elem_bytes 2 or 4, pointers aligned to elem_bytes.
+ */
+attn_status_t attn_cp_relayout(int to_heads, int cp, int64_t seqlen, int heads, int d,
+                               int elem_bytes, const void* src, const int64_t src_strides[3],
+                               void* dst, const int64_t dst_strides[3], attn_stream_t stream);
+
 /* Synchronises `stream` and returns the status word in `workspace`
  * (ATTN_OK, ATTN_ERR_BAD_METADATA, ATTN_ERR_TIMEOUT or, for the head-dim-512
  * backward, ATTN_ERR_WORKSPACE). */

@@ -140,3 +140,20 @@ def test_wide_backward_workspace_counts_visible_blocks(lib, sq, sk, causal, wl, 
     blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
     blocks = b * hq * _visible_blocks(sq, sk, causal, wl, wr, br)
     assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == blk_off + blocks * 65536
+
+
+def test_cp_relayout_validation(lib):
+    arr = ctypes.c_int64 * 3
+    # contiguous [cp, 2*chunk, heads, d] sequence side and [cp, S, heads/cp, d] head side;
+    # every call below is refused before anything is launched (the pointers are fake)
+    seq_s, head_s = arr(256 * 8 * 64, 8 * 64, 64), arr(1024 * 2 * 64, 2 * 64, 64)
+
+    def call(to_heads=1, cp=4, seqlen=1024, heads=8, d=64, eb=2, src=0x100000, dst=0x40000000):
+        return lib.attn_cp_relayout(to_heads, cp, seqlen, heads, d, eb, ctypes.c_void_p(src),
+                                    seq_s, ctypes.c_void_p(dst), head_s, None)
+    assert call(seqlen=1001) == 1          # not 2*cp chunks
+    assert call(heads=6) == 1              # heads % cp
+    assert call(eb=3) == 1                 # element size
+    assert call(cp=0) == 1
+    assert call(src=0x100001) == 3         # misaligned
+    assert call(dst=0x100000 + 64) == 1    # overlapping src/dst

@@ -224,6 +224,54 @@ def test_cp_allgather_emulation_matches_full_attention(cp, s, dims, wl):
         rel_l2(name, got, ex)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_cp_relayout_bit_exact(dtype):
+    """Sequence shards <-> head shards: a bit-preserving permutation, checked
+    against the same permutation written with torch indexing."""
+    from bwd_tcgen05_tmem_gb300 import cp as cpmod
+    cp, s, h, d = 4, 256, 8, 24
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(1, s, h, d, generator=g).to(dtype).cuda()
+    seq = torch.stack([t[0] for t in cpmod.shard(x, cp)])
+    heads = torch.empty(cp, s, h // cp, d, dtype=dtype, device="cuda")
+    attn.cp_relayout(seq, heads, to_heads=True, cp=cp)
+    ref = x[0].reshape(s, cp, h // cp, d).permute(1, 0, 2, 3)
+    back = torch.empty_like(seq)
+    attn.cp_relayout(heads, back, to_heads=False, cp=cp)
+    # head-major FP32 rows of one element (the LSE layout)
+    lse = torch.randn(1, h, s, generator=g).cuda()
+    lse_seq = torch.stack([cpmod.shard(lse.transpose(1, 2), cp)[r][0].transpose(0, 1)
+                           for r in range(cp)]).contiguous()
+    lse_h = torch.empty(cp, h // cp, s, device="cuda")
+    attn.cp_relayout(lse_seq, lse_h, to_heads=True, cp=cp)
+    torch.cuda.synchronize()
+    assert torch.equal(heads.view(torch.uint8), ref.contiguous().view(torch.uint8))
+    assert torch.equal(back.view(torch.uint8), seq.view(torch.uint8))
+    assert torch.equal(lse_h, lse[0].reshape(cp, h // cp, s))
+
+
+@pytest.mark.parametrize("cp,s,dims,hkv,wl", [(4, 1024, (192, 128), 4, -1), (2, 520, (128, 128), 2, 100),
+                                              (2, 512, (512, 512), 2, -1)])
+def test_cp_a2a_emulation_matches_full_attention(cp, s, dims, hkv, wl):
+    """All-to-all CP: relayout to head shards, full-sequence attention per rank."""
+    from bwd_tcgen05_tmem_gb300 import cp as cpmod
+    q, k, v, do = dense_inputs(1, s, s, 8, hkv, dims[0], dims[1], "bf16")
+    a2a = cpmod.CPA2A(q.cuda(), k.cuda(), v.cuda(), do.cuda(), cp=cp, window=(wl, 0))
+    o_sh, lse_sh = a2a.forward()
+    g_sh = a2a.backward()
+    torch.cuda.synchronize()
+    un = lambda t: cpmod.unshard([x[None] for x in t], cp).cpu()  # noqa: E731
+    o = un(o_sh)
+    lse = cpmod.unshard_lse([x[None] for x in lse_sh], cp).cpu()
+    ref = Reference(q, k, v, do, causal=True, scale=1.0 / math.sqrt(dims[0]), window=(wl, 0),
+                    dtype="bf16")
+    gate("o", o, ref.o, ref.floor["o"])
+    check_lse(lse, ref.lse)
+    for name, got, ex in zip(("dq", "dk", "dv"), g_sh, (ref.dq, ref.dk, ref.dv)):
+        gate(name, un(got), ex, ref.floor[name])
+        rel_l2(name, un(got), ex)
+
+
 def test_cp_ring_equals_direct_path():
     """The ring emulation and the direct kernels agree closely (plumbing check)."""
     from bwd_tcgen05_tmem_gb300 import cp as cpmod

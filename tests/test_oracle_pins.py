@@ -447,3 +447,24 @@ def test_two_x_criterion_and_mutation(dtype):
     assert any(rejected), rejected
     if dtype == "fp16":
         assert all(rejected), rejected  # fp16's finer mantissa exposes it everywhere
+
+
+def test_a2a_head_shards_equal_full():
+    """All-to-all CP: rank r attends over the whole sequence with query heads
+    [r*hq/cp, ...) and kv heads [r*hkv/cp, ...); with GQA the local group map
+    h_local -> h_local // (hq/hkv) is the global one restricted to the rank."""
+    s, hq, hkv, ncp = 20, 8, 4, 2
+    q, k, v, do = rand(s, hq, 6), rand(s, hkv, 6), rand(s, hkv, 5), rand(s, hq, 5)
+    kw = dict(scale=0.5, causal=True, window=(7, -1))
+    fo, fl = oracle.fwd(q, k, v, [0, s], [0, s], **kw)
+    fdq, fdk, fdv = oracle.bwd(q, k, v, do, [0, s], [0, s], **kw)
+    a, b = hq // ncp, hkv // ncp
+    for r in range(ncp):
+        hs, gs = slice(r * a, (r + 1) * a), slice(r * b, (r + 1) * b)
+        o, lse = oracle.fwd(q[:, hs], k[:, gs], v[:, gs], [0, s], [0, s], **kw)
+        dq, dk, dv = oracle.bwd(q[:, hs], k[:, gs], v[:, gs], do[:, hs], [0, s], [0, s], **kw)
+        np.testing.assert_array_equal(o, fo[:, hs])
+        np.testing.assert_array_equal(lse, fl[hs])
+        np.testing.assert_allclose(dq, fdq[:, hs], atol=1e-14)
+        np.testing.assert_allclose(dk, fdk[:, gs], atol=1e-14)
+        np.testing.assert_allclose(dv, fdv[:, gs], atol=1e-14)
