@@ -57,6 +57,7 @@ class Params(ctypes.Structure):
         ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
         ("softmax_scale", ctypes.c_float),
         ("accumulate", ctypes.c_int),
+        ("seqused_q", ctypes.c_void_p), ("seqused_k", ctypes.c_void_p),
     ]
 
 
@@ -148,7 +149,7 @@ def _stream(stream):
 def make_params(q, k, v, *, causal=True, scale=None, window=(-1, -1), bottom_right=False,
                 cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
                 o=None, dout=None, dq=None, dk=None, dv=None, o_dtype=None, grad_dtype=None,
-                lse_strides=(0, 0), accumulate=False):
+                lse_strides=(0, 0), accumulate=False, seqused_q=None, seqused_k=None):
     thd = cu_seqlens_q is not None
     p = Params()
     p.dtype = _code(q.dtype)
@@ -179,6 +180,9 @@ def make_params(q, k, v, *, causal=True, scale=None, window=(-1, -1), bottom_rig
     p.window_left, p.window_right = int(window[0]), int(window[1])
     p.softmax_scale = float(scale if scale is not None else 1.0 / math.sqrt(dqk))
     p.accumulate = int(bool(accumulate))
+    if seqused_q is not None:  # padded THD: device int32 [batch] visible lengths
+        p.seqused_q = seqused_q.data_ptr()
+        p.seqused_k = (seqused_k if seqused_k is not None else seqused_q).data_ptr()
     return p
 
 
@@ -190,7 +194,8 @@ def _lse_shape(q, thd):
 
 def fwd(q, k, v, *, causal=True, scale=None, window=(-1, -1), bottom_right=False,
         cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
-        out=None, lse=None, o_dtype=None, lse_strides=(0, 0), workspace=None, stream=None):
+        seqused_q=None, seqused_k=None, out=None, lse=None, o_dtype=None, lse_strides=(0, 0),
+        workspace=None, stream=None):
     """Fused attention forward. Returns (o, lse).  lse_strides: element strides
     {batch, head} of `lse` ((0, 0) = its default layout)."""
     lib = load()
@@ -204,7 +209,8 @@ def fwd(q, k, v, *, causal=True, scale=None, window=(-1, -1), bottom_right=False
     p = make_params(q, k, v, causal=causal, scale=scale, window=window,
                     bottom_right=bottom_right, cu_seqlens_q=cu_seqlens_q,
                     cu_seqlens_k=cu_seqlens_k, max_seqlen_q=max_seqlen_q,
-                    max_seqlen_k=max_seqlen_k, o=out, o_dtype=odt, lse_strides=lse_strides)
+                    max_seqlen_k=max_seqlen_k, o=out, o_dtype=odt, lse_strides=lse_strides,
+                    seqused_q=seqused_q, seqused_k=seqused_k)
     need = lib.attn_fwd_workspace_size(ctypes.byref(p))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -215,8 +221,9 @@ def fwd(q, k, v, *, causal=True, scale=None, window=(-1, -1), bottom_right=False
 
 def bwd(q, k, v, o, dout, lse, *, causal=True, scale=None, window=(-1, -1),
         bottom_right=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None,
-        max_seqlen_k=None, dq=None, dk=None, dv=None, grad_dtype=None, lse_strides=(0, 0),
-        accumulate=False, workspace=None, stream=None, stage="all"):
+        max_seqlen_k=None, seqused_q=None, seqused_k=None, dq=None, dk=None, dv=None,
+        grad_dtype=None, lse_strides=(0, 0), accumulate=False, workspace=None, stream=None,
+        stage="all"):
     """Fused attention backward. Returns (dq, dk, dv).
 
     ``stage``: "all" (attn_bwd), or one of "preprocess", "dq", "dkdv" to run a
@@ -234,7 +241,7 @@ def bwd(q, k, v, o, dout, lse, *, causal=True, scale=None, window=(-1, -1),
                     cu_seqlens_k=cu_seqlens_k, max_seqlen_q=max_seqlen_q,
                     max_seqlen_k=max_seqlen_k, o=o, dout=dout, dq=dq, dk=dk, dv=dv,
                     o_dtype=o.dtype, grad_dtype=gdt, lse_strides=lse_strides,
-                    accumulate=accumulate)
+                    accumulate=accumulate, seqused_q=seqused_q, seqused_k=seqused_k)
     need = lib.attn_bwd_workspace_size(ctypes.byref(p))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

@@ -127,6 +127,13 @@ attn_status_t check_params(const attn_params_t* p) {
     if ((uintptr_t)p->cu_seqlens_q % 4 || (uintptr_t)p->cu_seqlens_k % 4)
       return fail(ATTN_ERR_ALIGNMENT, "cu_seqlens must be 4-byte aligned");
   }
+  if (p->seqused_q || p->seqused_k) {
+    if (!thd(p)) return fail(ATTN_ERR_INVALID_ARG, "seqused needs the packed (THD) layout");
+    if (!p->seqused_q || !p->seqused_k)
+      return fail(ATTN_ERR_INVALID_ARG, "seqused_q and seqused_k must both be set or NULL");
+    if ((uintptr_t)p->seqused_q % 4 || (uintptr_t)p->seqused_k % 4)
+      return fail(ATTN_ERR_ALIGNMENT, "seqused must be 4-byte aligned");
+  }
   if (p->window_left < -1 || p->window_right < -1)
     return fail(ATTN_ERR_INVALID_ARG, "window bounds must be >= -1");
   if (!(p->softmax_scale > 0.0f) || !std::isfinite(p->softmax_scale))
@@ -163,6 +170,8 @@ attn::Geometry geometry(const attn_params_t* p) {
   attn::Geometry g;
   g.cu_q = p->cu_seqlens_q;
   g.cu_k = p->cu_seqlens_k;
+  g.used_q = p->seqused_q;
+  g.used_k = p->seqused_k;
   g.seqlen_q = p->seqlen_q;
   g.seqlen_k = p->seqlen_k;
   g.causal = p->causal ? 1 : 0;
@@ -190,6 +199,8 @@ attn_status_t launch_check_if_thd(const attn_params_t* p, int* status, cudaStrea
   attn::CheckParams c;
   c.cu_q = p->cu_seqlens_q;
   c.cu_k = p->cu_seqlens_k;
+  c.used_q = p->seqused_q;
+  c.used_k = p->seqused_k;
   c.batch = p->batch;
   c.max_q = p->seqlen_q;
   c.max_k = p->seqlen_k;

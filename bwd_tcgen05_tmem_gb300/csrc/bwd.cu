@@ -27,6 +27,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_lau
     pp.dout = a.dout;
     pp.d = a.d;
     pp.cu_q = a.thd ? a.geo.cu_q : nullptr;
+    pp.used_q = a.thd ? a.geo.used_q : nullptr;
     pp.so_b = a.so[0]; pp.so_t = a.so[1]; pp.so_h = a.so[2];
     pp.sdo_b = a.sdo[0]; pp.sdo_t = a.sdo[1]; pp.sdo_h = a.sdo[2];
     pp.d_sb = a.d_sb;

@@ -31,6 +31,8 @@ __host__ __device__ inline bool tile_major(int n_tiles) { return n_tiles >= kTil
 struct Geometry {
   const int32_t* cu_q;  // null: dense
   const int32_t* cu_k;
+  const int32_t* used_q;  // padded THD: visible length of each sequence (else null)
+  const int32_t* used_k;
   int seqlen_q, seqlen_k;  // dense lengths (ignored for varlen)
   int causal, bottom_right, wl, wr;
 };
@@ -45,9 +47,9 @@ __device__ __forceinline__ Seq load_seq(const Geometry& g, int b) {
   Seq s;
   if (g.cu_q) {
     s.q_start = g.cu_q[b];
-    s.lq = g.cu_q[b + 1] - s.q_start;
+    s.lq = g.used_q ? g.used_q[b] : g.cu_q[b + 1] - s.q_start;
     s.k_start = g.cu_k[b];
-    s.lk = g.cu_k[b + 1] - s.k_start;
+    s.lk = g.used_k ? g.used_k[b] : g.cu_k[b + 1] - s.k_start;
   } else {
     s.q_start = 0;
     s.k_start = 0;

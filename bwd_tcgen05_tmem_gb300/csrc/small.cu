@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256) attn_pre_kernel(const PreParams p) {
     for (int u = 0; u < kU; ++u) {
       const int64_t r = base + u * kRowsPerPass + sub;
       didx[u] = -1;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) ov[u][c] = dv[u][c] = make_uint4(0u, 0u, 0u, 0u);
       if (r < rows) {
         // rows < 2^32 (checked at launch): 32-bit division
         const uint32_t r32 = (uint32_t)r;
@@ -52,6 +54,7 @@ __global__ void __launch_bounds__(256) attn_pre_kernel(const PreParams p) {
           }
           b = lo;
           tok = t;
+          if (p.used_q && (int64_t)t - p.cu_q[b] >= p.used_q[b]) continue;  // a gap row: no D
         } else {
           b = (int)(t / (uint32_t)p.seqlen_q);
           tok = t - (uint32_t)b * (uint32_t)p.seqlen_q;
@@ -67,9 +70,6 @@ __global__ void __launch_bounds__(256) attn_pre_kernel(const PreParams p) {
           dv[u][c] = drow[c * LPR + l];
         }
         didx[u] = (int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok;
-      } else {
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) ov[u][c] = dv[u][c] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
 #pragma unroll
@@ -199,6 +199,9 @@ __global__ void __launch_bounds__(256) attn_check_kernel(const CheckParams p) {
     const int lq = p.cu_q[b + 1] - p.cu_q[b];
     const int lk = p.cu_k[b + 1] - p.cu_k[b];
     if (lq < 0 || lq > p.max_q || lk < 0 || lk > p.max_k) local = 1;
+    // padded layout: the visible length fits in the sequence's padded extent
+    if (p.used_q && (p.used_q[b] < 0 || p.used_q[b] > lq)) local = 1;
+    if (p.used_k && (p.used_k[b] < 0 || p.used_k[b] > lk)) local = 1;
   }
   if (threadIdx.x == 0) {
     if (p.cu_q[0] != 0 || p.cu_k[0] != 0) local = 1;

@@ -11,6 +11,7 @@ struct PreParams {
   const void* dout;
   float* d;             // D in the LSE layout
   const int32_t* cu_q;  // null: dense
+  const int32_t* used_q;  // padded THD: rows past used_q[b] are a gap (skipped)
   int64_t so_b, so_t, so_h, sdo_b, sdo_t, sdo_h;
   int64_t d_sb, d_sh;   // D index = b*d_sb + h*d_sh + token
   int batch, seqlen_q, total_q, hq, dv;
@@ -33,6 +34,8 @@ struct MergeParams {
 struct CheckParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
+  const int32_t* used_q;  // optional visible lengths (padded THD)
+  const int32_t* used_k;
   int batch, max_q, max_k, total_q, total_k;
   int* status;
 };

@@ -88,6 +88,12 @@ typedef struct {
   int accumulate;          /* attn_bwd with grad_dtype FP32 only: 1 adds the gradients
                               into dq/dk/dv instead of overwriting them (used to sum
                               the partial gradients of a context-parallel ring) */
+  const int32_t* seqused_q; /* THD only, device [batch] or NULL: padded layout (PR #3149:
+                               physical padded offsets plus visible lengths).  Sequence b
+                               then uses rows [cu_seqlens_q[b], cu_seqlens_q[b] +
+                               seqused_q[b]); the rows up to cu_seqlens_q[b+1] are a gap
+                               that no kernel reads or writes. */
+  const int32_t* seqused_k; /* the same for keys/values; set both or neither */
 } attn_params_t;
 
 /* Bytes of workspace attn_fwd / attn_bwd need for `p` (always >= 256: the

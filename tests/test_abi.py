@@ -157,3 +157,18 @@ def test_cp_relayout_validation(lib):
     assert call(cp=0) == 1
     assert call(src=0x100001) == 3         # misaligned
     assert call(dst=0x100000 + 64) == 1    # overlapping src/dst
+
+
+def test_seqused_validation(lib):
+    p = base_params()
+    p.seqused_q = 0x7000  # dense tensors: seqused needs THD
+    p.seqused_k = 0x7000
+    assert call_fwd(lib, p) == 1
+    q = fake((64, 4, 128))
+    cu = torch.zeros(3, dtype=torch.int32)  # host tensor: only its address is read
+    p = attn.make_params(q, fake((64, 2, 128)), fake((64, 2, 128)), o=q, cu_seqlens_q=cu,
+                         max_seqlen_q=64, max_seqlen_k=64)
+    p.seqused_q = 0x7000  # only one of the pair
+    assert call_fwd(lib, p) == 1
+    p.seqused_k = 0x7002  # misaligned
+    assert call_fwd(lib, p) == 3

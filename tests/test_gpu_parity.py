@@ -98,6 +98,50 @@ def test_thd_varlen(dtype, dims):
                   cu=inp["cu_seqlens"], max_len=inp["max_seqlen"])
 
 
+@pytest.mark.parametrize("dims", [(128, 128), (192, 128), (512, 512)])
+def test_thd_padded_seqused(dims):
+    """Padded THD (TransformerEngine PR #3149: physical padded offsets plus
+    visible lengths): gap rows are neither read nor written, and the visible
+    rows equal the oracle run on the compacted documents."""
+    used = [0, 1, 129, 300, 64, 200, 0]
+    gaps = [5, 0, 7, 128, 3, 1, 9]
+    padded = [u + g for u, g in zip(used, gaps)]
+    cu = torch.tensor([0] + list(np.cumsum(padded)), dtype=torch.int32)
+    total, hq, hkv = int(cu[-1]), 8, 2
+    g = torch.Generator().manual_seed(11)
+    q = torch.randn(total, hq, dims[0], generator=g).bfloat16()
+    k = torch.randn(total, hkv, dims[0], generator=g).bfloat16()
+    v = torch.randn(total, hkv, dims[1], generator=g).bfloat16()
+    do = torch.randn(total, hq, dims[1], generator=g).bfloat16()
+    su = torch.tensor(used, dtype=torch.int32)
+    dev = "cuda"
+    kw = dict(causal=True, cu_seqlens_q=cu.to(dev), cu_seqlens_k=cu.to(dev),
+              max_seqlen_q=max(padded), max_seqlen_k=max(padded), seqused_q=su.to(dev),
+              seqused_k=su.to(dev))
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    nan = float("nan")
+    o = torch.full((total, hq, dims[1]), nan, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((hq, total), nan, device=dev)
+    attn.fwd(qd, kd, vd, out=o, lse=lse, **kw)
+    dq, dk, dv = (torch.full_like(t, nan) for t in (qd, kd, vd))
+    attn.bwd(qd, kd, vd, o, dod, lse, dq=dq, dk=dk, dv=dv, **kw)
+    torch.cuda.synchronize()
+    rows = torch.cat([torch.arange(int(cu[b]), int(cu[b]) + used[b]) for b in range(len(used))])
+    gap = torch.ones(total, dtype=torch.bool)
+    gap[rows] = False
+    for t in (o, dq, dk, dv):  # gap rows untouched
+        assert torch.isnan(t.cpu()[gap].float()).all()
+    assert torch.isnan(lse.cpu()[:, gap]).all()
+    cu_c = [0] + list(np.cumsum(used))
+    ref = Reference(q[rows], k[rows], v[rows], do[rows], causal=True,
+                    scale=1.0 / math.sqrt(dims[0]), cu_q=cu_c, cu_k=cu_c, dtype="bf16")
+    gate("o", o.cpu()[rows], ref.o, ref.floor["o"])
+    check_lse(lse.cpu()[:, rows], ref.lse)
+    for name, got, ex in (("dq", dq, ref.dq), ("dk", dk, ref.dk), ("dv", dv, ref.dv)):
+        gate(name, got.cpu()[rows], ex, ref.floor[name])
+        rel_l2(name, got.cpu()[rows], ex)
+
+
 def test_forward_bitwise_reproducible_and_stream_bound():
     q, k, v, _ = dense_inputs(1, 700, 700, 4, 4, 192, 128, "bf16")
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
