@@ -13,8 +13,9 @@
 //   warps 4..7  softmax: one TMEM lane (= query row) per thread; rescales O
 //               in TMEM when the running maximum grows, writes P (16-bit)
 //               into TMEM, and runs the epilogue.
-// TMEM columns: S buffers [0,128) and [128,256) (P overwrites the first 64
-// columns of its S buffer), O accumulator [256, 256 + DV_CTA).
+// TMEM columns: kSB S buffers of 128 columns (P overwrites the first 64
+// columns of its S buffer), then the O accumulator.  Three S buffers when O
+// is at most 128 columns wide: S(j+2) can then start before PV(j) finishes.
 // MMAs: S = Q K^T   SS, both K-major (128 x 128 x DQK)
 //       O += P V    TS, A = P from TMEM, B = V chunk (MN-major), N = 64 each.
 #include "kcommon.cuh"
@@ -33,7 +34,9 @@ struct FwdCfg {
   static constexpr int kKRingRaw = kMaxSlots - kQSlots - kVStages * kVCh;
   static constexpr int kKRing = kKRingRaw > 16 ? 16 : kKRingRaw;
   static constexpr int kSmem = (kQSlots + kVStages * kVCh + kKRing) * kSlotBytes + 1024;
-  static constexpr int kTmemO = 256;
+  static constexpr int kSB = DV_CTA <= 128 ? 3 : 2;  // S buffers
+  static constexpr int kTmemO = 128 * kSB;
+  static_assert(kTmemO + DV_CTA <= 512, "TMEM budget");
   static_assert(DQK % 64 == 0 && DV_CTA % 64 == 0 && DV_CTA <= 256, "head dim");
   static_assert(kKRing >= 2, "ring");
 };
@@ -49,7 +52,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
 
   __shared__ uint64_t kfull[C::kKRing], kempty[C::kKRing], vfull[C::kVStages], vempty[C::kVStages];
   // o_done[b]: PV of the key tiles that used S buffer b (one phase per use)
-  __shared__ uint64_t q_bar, s_full[2], p_full[2], o_done[2], drain_bar, drain_bar2;
+  __shared__ uint64_t q_bar, s_full[C::kSB], p_full[C::kSB], o_done[C::kSB], drain_bar, drain_bar2;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, skip_sh;
 
@@ -88,12 +91,11 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       mbar_init(&vempty[i], 1);
     }
     mbar_init(&q_bar, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kSB; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
     }
-    mbar_init(&o_done[0], 1);
-    mbar_init(&o_done[1], 1);
     mbar_init(&drain_bar, 1);
     mbar_init(&drain_bar2, 1);
     fence_barrier_init();
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       bool ok = s_role ? mbar_wait(&q_bar, 0, ab) : true;
       tc_fence_after();
       auto issue_s = [&](int jt) {
-        const uint32_t d = tmem + (uint32_t)((jt & 1) * 128);
+        const uint32_t d = tmem + (uint32_t)((jt % C::kSB) * 128);
 #pragma unroll
         for (int c = 0; c < C::kKCh; ++c, ++kcnt) {
           const uint32_t slot = kcnt % C::kKRing;
@@ -196,10 +198,10 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
             mma_ss(d, qa + 2 * k, kb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
           mma_commit(&kempty[slot]);
         }
-        mma_commit(&s_full[jt & 1]);
+        mma_commit(&s_full[jt % C::kSB]);
       };
       auto issue_pv = [&](int jt) {
-        if (!mbar_wait(&p_full[jt & 1], (jt >> 1) & 1u, ab)) {
+        if (!mbar_wait(&p_full[jt % C::kSB], (jt / C::kSB) & 1u, ab)) {
           ok = false;
           return;
         }
@@ -209,18 +211,19 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
           return;
         }
         tc_fence_after();
-        const uint32_t pa = tmem + (uint32_t)((jt & 1) * 128);
+        const uint32_t pa = tmem + (uint32_t)((jt % C::kSB) * 128);
         const uint64_t vb = vdesc + (uint64_t)(st * C::kVCh * (kSlotBytes >> 4));
         mma_ts(tmem + C::kTmemO, pa, vb, idesc_o, jt > 0 ? 1u : 0u);
 #pragma unroll
         for (int k = 1; k < 8; ++k) mma_ts(tmem + C::kTmemO, pa + k * 8, vb + k * 128, idesc_o, 1u);
         mma_commit(&vempty[st]);
-        mma_commit(&o_done[jt & 1]);
+        mma_commit(&o_done[jt % C::kSB]);
       };
       if (s_role) {
         for (int jt = 0; jt < n_kv && ok; ++jt) {
-          // S buffer jt&1 last held P(jt-2): wait until PV(jt-2) has read it
-          if (jt >= 2 && !mbar_wait(&o_done[jt & 1], ((jt - 2) >> 1) & 1u, ab)) break;
+          // S buffer jt%kSB last held P(jt-kSB): wait until PV(jt-kSB) has read it
+          if (jt >= C::kSB && !mbar_wait(&o_done[jt % C::kSB], ((jt - C::kSB) / C::kSB) & 1u, ab))
+            break;
           issue_s(jt);
         }
         mma_commit(&drain_bar);
@@ -247,12 +250,12 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
     bool ok = true;
     for (int jt = 0; jt < n_kv; ++jt) {
       const int k0 = (kt0 + jt) * kBlockN;
-      if (!mbar_wait_warp(&s_full[jt & 1], (jt >> 1) & 1u, ab)) {
+      if (!mbar_wait_warp(&s_full[jt % C::kSB], (jt / C::kSB) & 1u, ab)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sb = tmem + lane_off + (uint32_t)((jt & 1) * 128);
+      const uint32_t sb = tmem + lane_off + (uint32_t)((jt % C::kSB) * 128);
       float s[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       l_run = l_run * alpha + rs;
       // rescale O rows whose maximum grew (after PV(jt-1) has finished)
       if (__any_sync(0xffffffffu, grow && jt > 0)) {
-        if (!mbar_wait_warp(&o_done[(jt - 1) & 1], ((jt - 1) >> 1) & 1u, ab)) {
+        if (!mbar_wait_warp(&o_done[(jt - 1) % C::kSB], ((jt - 1) / C::kSB) & 1u, ab)) {
           ok = false;
           break;
         }
@@ -326,12 +329,13 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[jt & 1]);
+      mbar_arrive(&p_full[jt % C::kSB]);
     }
     // ------------------------------------------------------------ epilogue
-    // PV(n-2) and PV(n-1) used different S buffers, hence different barriers
-    if (ok && n_kv > 1) ok = mbar_wait_warp(&o_done[(n_kv - 2) & 1], ((n_kv - 2) >> 1) & 1u, ab);
-    if (ok && n_kv > 0) ok = mbar_wait_warp(&o_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1u, ab);
+    // the last PV of every S buffer, in order (each barrier is at most one
+    // phase behind: S(n-1) already waited for PV(n-1-kSB))
+    for (int t = n_kv > C::kSB ? n_kv - C::kSB : 0; t < n_kv && ok; ++t)
+      ok = mbar_wait_warp(&o_done[t % C::kSB], (t / C::kSB) & 1u, ab);
     if (ok) {
       tc_fence_after();
       const bool valid = i < sq.lq;
