@@ -220,7 +220,7 @@ struct BwdLayout {
   long long cap;  // score blocks
 };
 
-bool wide(const attn_params_t* p) { return p->d_qk > 256 || p->d_v > 256; }
+bool wide(const attn_params_t* p) { return attn::wide_backward(p->d_qk, p->d_v, p->window_left); }
 
 // Score blocks of the wide backward over all query heads: exact for dense
 // inputs; for packed (THD) inputs a bound that takes every document's keys

@@ -37,6 +37,14 @@ struct BwdArgs {
 constexpr int kWideTile = 128 * 64 * 2;
 constexpr int kWideBlock = 4 * kWideTile;
 
+// The backward materialises P and dS for head dims above 256 (the fused
+// kernels cannot hold them), and at head dim 256 with a sliding window: there
+// the fused path needs a dV-only and a dK-only launch that recompute the
+// scores, while this path runs each contraction once.
+inline bool wide_backward(int dqk, int dv, int window_left) {
+  return dqk > 256 || dv > 256 || (dqk == 256 && dv == 256 && window_left >= 0);
+}
+
 // Visible 128-key blocks of query tile qt: returns their count, first in kb0.
 __host__ __device__ inline int wide_blocks_of_qtile(const Seq& s, int qt, int& kb0) {
   const long long i0 = (long long)qt * 128;

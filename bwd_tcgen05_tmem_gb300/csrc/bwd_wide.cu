@@ -1,4 +1,5 @@
-// bwd_wide.cu -- backward for head dims above 256 (tcgen05 / TMEM / TMA).
+// bwd_wide.cu -- backward for head dims above 256, and for head dim 256 with a
+// sliding window (tcgen05 / TMEM / TMA).
 //
 // At head dim 512 one SM cannot hold what the fused kernels keep on chip:
 // the dK and dV accumulators of a 128-key tile need 2 x 512 TMEM columns
@@ -98,7 +99,7 @@ struct WideScoresCfg {
   static constexpr int kChunk = 64 * 128;  // 64 key rows x 64 columns
   static constexpr int kQBytes = kQCh * kSlotBytes;
   static constexpr int kRingRaw = (232448 - 2048 - kQBytes) / kChunk;
-  static constexpr int kRing = kRingRaw > 12 ? 12 : kRingRaw;
+  static constexpr int kRing = kRingRaw > 16 ? 16 : kRingRaw;
   static constexpr int kSmem = kQBytes + kRing * kChunk + 1024;
   // TMEM: buffer b holds S at 128b and dP at 128b + 64; dO at kTdO
   static constexpr int kTdO = 256;
@@ -629,10 +630,10 @@ __global__ void __launch_bounds__(384, 1)
 // ------------------------------------------------------------------ host side
 namespace {
 
-template <bool BF16>
+template <int D, bool BF16>
 cudaError_t launch_scores_t(const WideScoresParams& p, cudaStream_t st) {
-  using C = WideScoresCfg<512, 512>;
-  auto k = attn_bwd_wide_scores_kernel<512, 512, BF16>;
+  using C = WideScoresCfg<D, D>;
+  auto k = attn_bwd_wide_scores_kernel<D, D, BF16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const dim3 grid = tile_major(p.n_qtiles) ? dim3((unsigned)p.n_qtiles, (unsigned)p.hq, (unsigned)p.batch)
@@ -641,10 +642,10 @@ cudaError_t launch_scores_t(const WideScoresParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int KIND, bool BF16, bool G_F32>
+template <int D, int KIND, bool BF16, bool G_F32>
 cudaError_t launch_acc_t(const WideAccParams& p, cudaStream_t st) {
-  using C = WideAccCfg<512>;
-  auto k = attn_bwd_wide_acc_kernel<512, KIND, BF16, G_F32>;
+  using C = WideAccCfg<D>;
+  auto k = attn_bwd_wide_acc_kernel<D, KIND, BF16, G_F32>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned nh = (unsigned)(KIND == 0 ? p.hq : p.hkv);
@@ -655,17 +656,27 @@ cudaError_t launch_acc_t(const WideAccParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int D, int KIND>
+cudaError_t launch_acc_d(const WideAccParams& p, bool bf16, bool gf32, cudaStream_t st) {
+  if (bf16) return gf32 ? launch_acc_t<D, KIND, true, true>(p, st) : launch_acc_t<D, KIND, true, false>(p, st);
+  return gf32 ? launch_acc_t<D, KIND, false, true>(p, st) : launch_acc_t<D, KIND, false, false>(p, st);
+}
+
 template <int KIND>
-cudaError_t launch_acc(const WideAccParams& p, bool bf16, bool gf32, cudaStream_t st) {
-  if (bf16) return gf32 ? launch_acc_t<KIND, true, true>(p, st) : launch_acc_t<KIND, true, false>(p, st);
-  return gf32 ? launch_acc_t<KIND, false, true>(p, st) : launch_acc_t<KIND, false, false>(p, st);
+cudaError_t launch_acc(const WideAccParams& p, int d, bool bf16, bool gf32, cudaStream_t st) {
+  return d == 512 ? launch_acc_d<512, KIND>(p, bf16, gf32, st) : launch_acc_d<256, KIND>(p, bf16, gf32, st);
+}
+
+template <bool BF16>
+cudaError_t launch_scores(const WideScoresParams& p, int d, cudaStream_t st) {
+  return d == 512 ? launch_scores_t<512, BF16>(p, st) : launch_scores_t<256, BF16>(p, st);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* n_launches) {
   *n_launches = 0;
-  if (a.dqk != 512 || a.dv != 512) return cudaErrorNotSupported;
+  if (a.dqk != a.dv || (a.dqk != 512 && a.dqk != 256)) return cudaErrorNotSupported;
   const bool has_q = (a.thd ? a.total_q : a.batch * a.seqlen_q) > 0;
   const bool has_k = (a.thd ? a.total_k : a.batch * a.seqlen_k) > 0;
   const int nqt = (a.seqlen_q + 127) / 128, nkt = (a.seqlen_k + 127) / 128;
@@ -730,7 +741,8 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
       sp.n_qtiles = nqt;
       sp.scale_log2 = a.scale_log2;
       sp.status = a.status;
-      if ((e = a.bf16 ? launch_scores_t<true>(sp, st) : launch_scores_t<false>(sp, st)) != cudaSuccess)
+      if ((e = a.bf16 ? launch_scores<true>(sp, a.dqk, st) : launch_scores<false>(sp, a.dqk, st)) !=
+          cudaSuccess)
         return e;
       ++*n_launches;
     }
@@ -755,7 +767,7 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
     qp.n_tiles = nqt;
     qp.scale = a.scale;
     qp.status = a.status;
-    if ((e = launch_acc<0>(qp, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
+    if ((e = launch_acc<0>(qp, a.dqk, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
     ++*n_launches;
   }
   if ((stages & 4) && has_k) {
@@ -780,7 +792,7 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
     kp.n_tiles = nkt;
     kp.scale = a.scale;
     kp.status = a.status;
-    if ((e = launch_acc<1>(kp, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
+    if ((e = launch_acc<1>(kp, a.dqk, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
     ++*n_launches;
   }
   return cudaSuccess;

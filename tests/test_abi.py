@@ -172,3 +172,21 @@ def test_seqused_validation(lib):
     assert call_fwd(lib, p) == 1
     p.seqused_k = 0x7002  # misaligned
     assert call_fwd(lib, p) == 3
+
+
+@pytest.mark.parametrize("window,wide", [((-1, -1), False), ((100, 0), True), ((1023, 0), True)])
+def test_d256_backward_route_by_window(lib, window, wide):
+    """Head dim 256 materialises P/dS only with a sliding window (the fused path
+    would need two recomputing dK/dV launches); otherwise the workspace is the
+    status word and D alone."""
+    b, s, hq, hkv = 1, 700, 4, 1
+    q, k = fake((b, s, hq, 256)), fake((b, s, hkv, 256))
+    p = attn.make_params(q, k, k, o=q, causal=True, window=window)
+    base = 256 + -(-(b * s * hq * 4) // 256) * 256
+    need = lib.attn_bwd_workspace_size(ctypes.byref(p))
+    if not wide:
+        assert need == base
+    else:
+        blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
+        blocks = b * hq * _visible_blocks(s, s, True, window[0], window[1], False)
+        assert need == blk_off + blocks * 65536
