@@ -220,7 +220,11 @@ struct BwdLayout {
   long long cap;  // score blocks
 };
 
-bool wide(const attn_params_t* p) { return attn::wide_backward(p->d_qk, p->d_v, p->window_left); }
+long long wide_block_count(const attn_params_t* p);
+bool wide(const attn_params_t* p) {
+  if (p->d_qk < 256 || p->d_v < 256) return false;
+  return attn::wide_backward(p->d_qk, p->d_v, wide_block_count(p) * (long long)attn::kWideBlock);
+}
 
 // Score blocks of the wide backward over all query heads: exact for dense
 // inputs; for packed (THD) inputs a bound that takes every document's keys
@@ -439,6 +443,7 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
   a.d = dbuf;
   default_d_strides(p, a.d_sb, a.d_sh);
   if (wide(p)) {
+    a.wide = 1;
     a.wide_plan = (long long*)((char*)ws + lay.plan_off);
     a.wide_blocks = (uint8_t*)ws + lay.blk_off;
     a.wide_cap = lay.cap;

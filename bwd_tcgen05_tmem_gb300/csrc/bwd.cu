@@ -14,7 +14,7 @@ cudaError_t launch_dkv(const DkvParams& p, int dqk, int dv, int mode, bool bf16,
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_launches) {
   *n_launches = 0;
-  if (wide_backward(a.dqk, a.dv, a.geo.wl)) return launch_bwd_wide(a, st, stages, n_launches);
+  if (a.wide) return launch_bwd_wide(a, st, stages, n_launches);
   const bool has_q = (a.thd ? a.total_q : a.batch * a.seqlen_q) > 0;
   const bool has_k = (a.thd ? a.total_k : a.batch * a.seqlen_k) > 0;
   int bq[2], mode[2];

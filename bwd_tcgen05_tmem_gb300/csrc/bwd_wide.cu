@@ -1,5 +1,5 @@
-// bwd_wide.cu -- backward for head dims above 256, and for head dim 256 with a
-// sliding window (tcgen05 / TMEM / TMA).
+// bwd_wide.cu -- backward for head dims above 256, and for head dim 256 when
+// its score tiles fit the cap of wide_backward() (tcgen05 / TMEM / TMA).
 //
 // At head dim 512 one SM cannot hold what the fused kernels keep on chip:
 // the dK and dV accumulators of a 128-key tile need 2 x 512 TMEM columns

@@ -98,8 +98,8 @@ typedef struct {
 
 /* Bytes of workspace attn_fwd / attn_bwd need for `p` (always >= 256: the
  * status word lives at offset 0).  The workspace must be 256-byte aligned.
- * For head dims above 256 (and head dim 256 with a sliding window) the
- * backward also keeps P and dS of every visible
+ * For head dims above 256 (and head dim 256 when that takes at most 16 GiB)
+ * the backward also keeps P and dS of every visible
  * 128-query x 128-key tile (64 KiB each, all query heads) in the workspace:
  * the count is exact for dense inputs, and for THD it is a bound that takes
  * every document's keys as max_seqlen_k long (about 8.7 GB for batch 1,
@@ -127,8 +127,8 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
  * dQ = scale dS K; dK/dV are summed over the query heads of a GQA group
  * inside the kernel.  dq/dk/dv are fully overwritten (grad_dtype).  The
  * reduction order is fixed, so the backward is bitwise reproducible.
- * Head dim 512 (PR #3527: the d512 backward), and head dim 256 with a
- * sliding window (window_left >= 0): P and dS are written once to the
+ * Head dim 512 (PR #3527: the d512 backward), and head dim 256 when its P/dS
+ * blocks take at most 16 GiB: P and dS are written once to the
  * workspace (16-bit, as the fused kernels round them too) and the five
  * contractions run in three kernels; a workspace whose block table does not
  * fit sets ATTN_ERR_WORKSPACE in the status word.
@@ -146,7 +146,7 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
  *   attn_bwd_dkdv:       dK and dV, reduced over each GQA group (reads D).
  * The dq and dkdv stages require a preprocess on the same workspace, for the
  * same problem, earlier on the stream.  Where the backward materialises P and
- * dS (head dim 512; head dim 256 with a sliding window) the dq stage also
+ * dS (head dim 512; head dim 256 up to 16 GiB of blocks) the dq stage also
  * writes them into the workspace and the dkdv stage reads them: it then
  * requires the dq stage earlier on the stream as well.  Arguments a stage
  * does not use may be NULL.

@@ -174,12 +174,13 @@ def test_seqused_validation(lib):
     assert call_fwd(lib, p) == 3
 
 
-@pytest.mark.parametrize("window,wide", [((-1, -1), False), ((100, 0), True), ((1023, 0), True)])
-def test_d256_backward_route_by_window(lib, window, wide):
-    """Head dim 256 materialises P/dS only with a sliding window (the fused path
-    would need two recomputing dK/dV launches); otherwise the workspace is the
-    status word and D alone."""
-    b, s, hq, hkv = 1, 700, 4, 1
+@pytest.mark.parametrize("s,window,wide", [(700, (-1, -1), True), (700, (100, 0), True),
+                                           (65536, (-1, -1), False), (65536, (1023, 0), True)])
+def test_d256_backward_route_by_block_bytes(lib, s, window, wide):
+    """Head dim 256 materialises P/dS while the blocks take at most 16 GiB (the
+    fused path would need two recomputing dK/dV launches); beyond that the
+    workspace is the status word and D alone."""
+    b, hq, hkv = 1, 4, 1
     q, k = fake((b, s, hq, 256)), fake((b, s, hkv, 256))
     p = attn.make_params(q, k, k, o=q, causal=True, window=window)
     base = 256 + -(-(b * s * hq * 4) // 256) * 256
@@ -188,5 +189,10 @@ def test_d256_backward_route_by_window(lib, window, wide):
         assert need == base
     else:
         blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
-        blocks = b * hq * _visible_blocks(s, s, True, window[0], window[1], False)
+        nq, nk = (s + 127) // 128, (s + 127) // 128
+        if s <= 2048:
+            blocks = b * hq * _visible_blocks(s, s, True, window[0], window[1], False)
+        else:  # closed form: causal with a window of 1024 -> 9 blocks per query tile at most
+            blocks = b * hq * sum(min(qt, (1023 + 127) // 128 + 1) if qt > 8 else qt + 1
+                                  for qt in range(nq))
         assert need == blk_off + blocks * 65536
