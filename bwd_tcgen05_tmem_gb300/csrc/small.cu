@@ -222,34 +222,71 @@ cudaError_t launch_check(const CheckParams& p, cudaStream_t st) {
 namespace attn {
 
 // ----------------------------------------------------------------- CP relayout
-// One (token, head) row of d elements per warp pass; VEC = 16-byte vectors
-// (d * elem_bytes a multiple of 16 and 16-byte-aligned rows) or single
-// elements of elem_bytes.  Pure copy: every bit is preserved.
+// Rows are (token, head) pairs of d elements.  VEC: 16-byte vectors (d *
+// elem_bytes a multiple of 16 and 16-byte-aligned rows): a warp treats its
+// rows' vectors as one flat list, so every lane is busy whatever d is, and
+// keeps kU vectors in flight per lane; otherwise single elements of
+// elem_bytes.  Pure copy: every bit is preserved.
+// IDX: the index type of the row arithmetic (32-bit when every index fits).
+template <typename IDX>
+__device__ __forceinline__ void relayout_row_addr(const RelayoutParams& p, IDX r,
+                                                  const uint8_t*& src, uint8_t*& dst) {
+  const IDX chunk = (IDX)(p.seqlen / (2 * p.cp));
+  const int hpr = p.heads / p.cp;  // heads per rank on the head side
+  const IDX t = r / (IDX)p.heads;  // global token
+  const int h = (int)(r - t * (IDX)p.heads);
+  const IDX ch = t / chunk, u = t - ch * chunk;
+  // sequence side: owner rank and local token of global token t
+  const int64_t srank = (int64_t)ch < p.cp ? (int64_t)ch : 2 * p.cp - 1 - (int64_t)ch;
+  const int64_t stok = (int64_t)ch < p.cp ? (int64_t)u : (int64_t)(chunk + u);
+  const int64_t seq_off = srank * p.seq_s[0] + stok * p.seq_s[1] + (int64_t)h * p.seq_s[2];
+  const int64_t head_off = (int64_t)(h / hpr) * p.head_s[0] + (int64_t)t * p.head_s[1] +
+                           (int64_t)(h % hpr) * p.head_s[2];
+  src = p.src + (p.to_heads ? seq_off : head_off) * p.elem_bytes;
+  dst = p.dst + (p.to_heads ? head_off : seq_off) * p.elem_bytes;
+}
+
+// VEC requires rows * (d * elem_bytes / 16) < 2^32 (checked at launch): its
+// index arithmetic is 32-bit.
 template <bool VEC>
 __global__ void __launch_bounds__(256) attn_relayout_kernel(const RelayoutParams p) {
   const int lane = threadIdx.x & 31;
-  const int64_t chunk = p.seqlen / (2 * p.cp);
-  const int hpr = p.heads / p.cp;  // heads per rank on the head side
   const int64_t rows = p.seqlen * p.heads;
   const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int row_bytes = p.d * p.elem_bytes;
-  for (int64_t r = warp_id; r < rows; r += nwarps) {
-    const int64_t t = r / p.heads;  // global token
-    const int h = (int)(r - t * p.heads);
-    const int64_t ch = t / chunk, u = t - ch * chunk;
-    // sequence side: owner rank and local token of global token t
-    const int64_t srank = ch < p.cp ? ch : 2 * p.cp - 1 - ch;
-    const int64_t stok = ch < p.cp ? u : chunk + u;
-    const int64_t seq_off = srank * p.seq_s[0] + stok * p.seq_s[1] + (int64_t)h * p.seq_s[2];
-    const int64_t head_off = (int64_t)(h / hpr) * p.head_s[0] + t * p.head_s[1] +
-                             (int64_t)(h % hpr) * p.head_s[2];
-    const uint8_t* src = p.src + (p.to_heads ? seq_off : head_off) * p.elem_bytes;
-    uint8_t* dst = p.dst + (p.to_heads ? head_off : seq_off) * p.elem_bytes;
-    if (VEC) {
-      for (int c = lane * 16; c < row_bytes; c += 32 * 16)
-        *reinterpret_cast<uint4*>(dst + c) = *reinterpret_cast<const uint4*>(src + c);
-    } else {
+  if (VEC) {
+    constexpr int kU = 4;
+    const uint32_t vpr = (uint32_t)row_bytes / 16;  // vectors per row
+    const uint32_t nvec = (uint32_t)rows * vpr;      // all vectors, row-major
+    const uint32_t per_warp = 32 * kU;
+    for (int64_t base = warp_id * per_warp; base < nvec; base += nwarps * per_warp) {
+      uint4 val[kU];
+      uint8_t* dsts[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int64_t vi64 = base + u * 32 + lane;
+        dsts[u] = nullptr;
+        if (vi64 < nvec) {
+          const uint32_t vi = (uint32_t)vi64;
+          const uint32_t r = vi / vpr;
+          const int c = (int)(vi - r * vpr) * 16;
+          const uint8_t* src;
+          uint8_t* dst;
+          relayout_row_addr<uint32_t>(p, r, src, dst);
+          val[u] = *reinterpret_cast<const uint4*>(src + c);
+          dsts[u] = dst + c;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (dsts[u]) *reinterpret_cast<uint4*>(dsts[u]) = val[u];
+    }
+  } else {
+    for (int64_t r = warp_id; r < rows; r += nwarps) {
+      const uint8_t* src;
+      uint8_t* dst;
+      relayout_row_addr<int64_t>(p, r, src, dst);
       for (int c = lane * p.elem_bytes; c < row_bytes; c += 32 * p.elem_bytes) {
         if (p.elem_bytes == 4)
           *reinterpret_cast<uint32_t*>(dst + c) = *reinterpret_cast<const uint32_t*>(src + c);
@@ -270,6 +307,7 @@ cudaError_t launch_relayout(const RelayoutParams& p, int num_sms, cudaStream_t s
              ((uintptr_t)p.dst % 16) == 0;
   for (int i = 0; i < 3; ++i)
     vec = vec && (p.seq_s[i] * p.elem_bytes) % 16 == 0 && (p.head_s[i] * p.elem_bytes) % 16 == 0;
+  vec = vec && rows * (p.d * p.elem_bytes / 16) < (int64_t(1) << 32);
   if (vec)
     attn_relayout_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(p);
   else

@@ -155,7 +155,7 @@ def test_forward_bitwise_reproducible_and_stream_bound():
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("d", [128, 512])
+@pytest.mark.parametrize("d", [128, 256, 512])
 def test_backward_bitwise_reproducible(d):
     q, k, v, do = dense_inputs(1, 500, 500, 4, 2, d, d, "bf16")
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
@@ -334,7 +334,7 @@ def test_cp_ring_equals_direct_path():
         assert err.item() < 1e-2
 
 
-@pytest.mark.parametrize("dims", [(192, 128), (512, 512)])
+@pytest.mark.parametrize("dims", [(192, 128), (256, 256), (512, 512)])
 def test_backward_stages_equal_full_call(dims):
     q, k, v, do = dense_inputs(1, 300, 300, 4, 2, dims[0], dims[1], "bf16")
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
@@ -349,7 +349,7 @@ def test_backward_stages_equal_full_call(dims):
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("d", [128, 512])
+@pytest.mark.parametrize("d", [128, 256, 512])
 def test_fp32_gradient_accumulate(d):
     q, k, v, do = dense_inputs(1, 300, 300, 2, 2, d, d, "bf16")
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
