@@ -89,7 +89,7 @@ def test_dense(case):
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
-@pytest.mark.parametrize("dims", [(128, 128), (192, 128), (64, 64), (512, 512)])
+@pytest.mark.parametrize("dims", [(128, 128), (192, 128), (64, 64), (256, 256), (512, 512)])
 def test_thd_varlen(dtype, dims):
     lens = [0, 1, 129, 300, 64, 200, 0]
     w = synth.Workload("t", 0, 0, 8, 2, dims[0], dims[1], dtype=dtype, thd_total=1)
@@ -224,7 +224,8 @@ def test_bad_cu_seqlens_reports_status():
 
 
 @pytest.mark.parametrize("cp,s,dims", [(8, 640, (192, 128)), (2, 520, (128, 128)),
-                                       (4, 1024, (64, 64)), (2, 520, (512, 512))])
+                                       (4, 1024, (64, 64)), (2, 520, (512, 512)),
+                                       (2, 512, (256, 256))])
 def test_cp_ring_emulation_matches_full_attention(cp, s, dims):
     """Dual-chunk-swap ring: FP32 partials + LSE merge + per-step backward."""
     from bwd_tcgen05_tmem_gb300 import cp as cpmod
