@@ -57,9 +57,10 @@ def flops(w, lengths=None):
     bwd = 2 * nv * (3 * w.d_qk + 2 * w.d_v)
     # per-kernel attribution of the algorithmic work (sums to fwd + bwd):
     # head dims <= 256: dK/dV kernel S, dP, dV, dK; dQ kernel dQ (its S/dP
-    # recompute is not credited).  Above 256 the dq stage runs the scores
-    # kernel (S, dP) and the dQ GEMM, the dkdv stage the dV and dK GEMMs.
-    if w.d_qk > 256:
+    # recompute is not credited).  On the materialising path (head dims 256
+    # and 512 in these workloads) the dq stage runs the scores kernel (S, dP)
+    # and the dQ GEMM, the dkdv stage the dV and dK GEMMs.
+    if w.d_qk >= 256:
         kern = {"fwd": fwd, "dq": 2 * nv * (2 * w.d_qk + w.d_v), "dkdv": 2 * nv * (w.d_qk + w.d_v)}
     else:
         kern = {"fwd": fwd, "dkdv": 2 * nv * (2 * w.d_qk + 2 * w.d_v), "dq": 2 * nv * w.d_qk}
