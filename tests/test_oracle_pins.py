@@ -468,3 +468,33 @@ def test_a2a_head_shards_equal_full():
         np.testing.assert_allclose(dq, fdq[:, hs], atol=1e-14)
         np.testing.assert_allclose(dk, fdk[:, gs], atol=1e-14)
         np.testing.assert_allclose(dv, fdv[:, gs], atol=1e-14)
+
+
+@pytest.mark.parametrize("ncp", [1, 2, 3, 4, 8])
+def test_ring_pieces_cover_every_causal_pair_once(ncp):
+    """The p2p ring schedule of the CP emulation: over all ranks and steps, every
+    causally visible (query, key) pair of the global sequence is computed by
+    exactly one piece, with the piece's causal flag set exactly when it holds
+    the diagonal (the rank's own chunk pair at step 0)."""
+    from bwd_tcgen05_tmem_gb300 import cp as cpmod
+    c = 5
+    s = 2 * ncp * c
+    local = lambda r: np.concatenate([np.arange(r * c, (r + 1) * c),  # noqa: E731
+                                      np.arange((2 * ncp - 1 - r) * c, (2 * ncp - r) * c)])
+    count = np.zeros((s, s), dtype=int)
+    for pcs in cpmod.ring_pieces(ncp, c):
+        for pc in pcs:
+            qg = local(pc.rank)[pc.q_rows[0]:pc.q_rows[0] + pc.q_rows[1]]
+            kg = local(pc.src)[pc.k_rows[0]:pc.k_rows[0] + pc.k_rows[1]]
+            for a, i in enumerate(qg):
+                for b_, j in enumerate(kg):
+                    # visibility inside the piece: causal pieces are top-left over the
+                    # rank's local concatenation, full pieces see every key
+                    if not pc.causal or b_ <= a:
+                        count[i, j] += 1
+            if pc.causal:
+                assert pc.rank == pc.src
+            else:  # a full piece lies entirely below the diagonal
+                assert qg.min() > kg.max()
+    expect = np.tril(np.ones((s, s), dtype=int))
+    np.testing.assert_array_equal(count, expect)
