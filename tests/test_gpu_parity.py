@@ -142,6 +142,31 @@ def test_thd_padded_seqused(dims):
         rel_l2(name, got.cpu()[rows], ex)
 
 
+@pytest.mark.parametrize("dims", [(192, 128), (256, 256), (512, 512)])
+def test_sbhd_strides_equal_bshd(dims):
+    """Tensors are addressed through their actual strides (TransformerEngine
+    PR #3527: graphs built from each tensor's actual strides, so sbhd is
+    served without a transpose): SBHD-laid-out inputs, outputs and gradients
+    give bit-identical results to contiguous BSHD."""
+    b, s, hq, hkv = 2, 300, 4, 2
+    q, k, v, do = dense_inputs(b, s, s, hq, hkv, dims[0], dims[1], "bf16")
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = attn.fwd(qd, kd, vd)
+    g = attn.bwd(qd, kd, vd, o, dod, lse)
+    sb = lambda t: t.permute(1, 0, 2, 3).contiguous().permute(1, 0, 2, 3)  # noqa: E731
+    qs, ks, vs, dos = (sb(t) for t in (qd, kd, vd, dod))
+    assert qs.stride(1) == b * hq * dims[0]  # token-major in memory
+    o_s = sb(torch.empty_like(o))
+    lse_s = torch.empty_like(lse)
+    attn.fwd(qs, ks, vs, out=o_s, lse=lse_s)
+    gs = [sb(torch.empty_like(t)) for t in (qd, kd, vd)]
+    attn.bwd(qs, ks, vs, o_s, dos, lse_s, dq=gs[0], dk=gs[1], dv=gs[2])
+    torch.cuda.synchronize()
+    assert torch.equal(o_s, o) and torch.equal(lse_s, lse)
+    for a_, b_ in zip(gs, g):
+        assert torch.equal(a_, b_)
+
+
 def test_forward_bitwise_reproducible_and_stream_bound():
     q, k, v, _ = dense_inputs(1, 700, 700, 4, 4, 192, 128, "bf16")
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
