@@ -167,6 +167,47 @@ def test_sbhd_strides_equal_bshd(dims):
         assert torch.equal(a_, b_)
 
 
+@pytest.mark.parametrize("dims", [(192, 128), (512, 512)])
+def test_cuda_graph_replay_matches_eager(dims):
+    """attn_fwd + attn_bwd captured in a CUDA graph: replays on new input values,
+    with the outputs poisoned before each replay, equal eager calls bit for bit
+    (pointers, stream and workspace are bound per call, nothing else is kept)."""
+    b, s, hq, hkv = 1, 384, 4, 2
+    q, k, v, do = (t.cuda() for t in dense_inputs(b, s, s, hq, hkv, dims[0], dims[1], "bf16"))
+    o, lse = torch.empty(b, s, hq, dims[1], dtype=q.dtype, device="cuda"), \
+        torch.empty(b, hq, s, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fws = torch.empty(attn.workspace_size("fwd", q, k, v), dtype=torch.uint8, device="cuda")
+    bws = torch.empty(attn.workspace_size("bwd", q, k, v), dtype=torch.uint8, device="cuda")
+
+    def step():
+        attn.fwd(q, k, v, out=o, lse=lse, workspace=fws)
+        attn.bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=bws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    g = torch.Generator(device="cuda").manual_seed(5)
+    for _ in range(2):
+        for t in (q, k, v, do):
+            t.copy_(torch.randn(t.shape, generator=g, device="cuda").to(t.dtype))
+        for t in (o, dq, dk, dv):
+            t.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (o, lse, dq, dk, dv)]
+        step()  # eager on the same inputs
+        torch.cuda.synchronize()
+        for a_, b_ in zip(got, (o, lse, dq, dk, dv)):
+            assert torch.equal(a_, b_)
+
+
 def test_forward_bitwise_reproducible_and_stream_bound():
     q, k, v, _ = dense_inputs(1, 700, 700, 4, 4, 192, 128, "bf16")
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
