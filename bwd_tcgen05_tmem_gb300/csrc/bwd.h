@@ -71,7 +71,7 @@ struct WidePlanParams {
 };
 
 struct WideScoresParams {
-  CUtensorMap tm_q, tm_k, tm_v;  // q: 128-row boxes, k/v: 64-row boxes
+  CUtensorMap tm_q, tm_k, tm_v;  // 128-row boxes
   MapOrder oq, ok, ov;
   Geometry geo;
   const float* lse;

@@ -10,7 +10,7 @@
 // backward; PR #3510 backward chain) into three kernels:
 //
 //   scores  query-stationary, per 128-row query tile and visible 128-key
-//           block (as two 64-key sub-tiles):
+//           block:
 //             S  = Q K^T      (SS MMA, Q resident in shared memory)
 //             dP = dO V^T     (TS MMA, dO resident in TMEM as operand A)
 //             P  = exp(scale S - LSE),  dS = P (dP - D)   (softmax warps)
@@ -92,17 +92,22 @@ __global__ void __launch_bounds__(256) attn_wide_plan_kernel(const WidePlanParam
 }
 
 // ------------------------------------------------------------------ scores
+// Per visible 128-key block: S (N = 128, SS) and dP (N = 128, TS).  Each score
+// MMA covers the whole block: an M = 128 MMA with N = 64 occupies the tensor
+// pipe as long as one with N = 128, so splitting the block into 64-key halves
+// would halve the rate.  TMEM holds one S, one dP and dO; S and dP have their
+// own full / free barriers, so S of block n+1 runs while the softmax waits for
+// dP of block n, and dP of block n+1 while it computes P.
 template <int DQK, int DV>
 struct WideScoresCfg {
   static constexpr int kQCh = DQK / 64;
   static constexpr int kVCh = DV / 64;
-  static constexpr int kChunk = 64 * 128;  // 64 key rows x 64 columns
+  static constexpr int kChunk = kSlotBytes;  // 128 key rows x 64 columns
   static constexpr int kQBytes = kQCh * kSlotBytes;
   static constexpr int kRingRaw = (232448 - 2048 - kQBytes) / kChunk;
-  static constexpr int kRing = kRingRaw > 16 ? 16 : kRingRaw;
+  static constexpr int kRing = kRingRaw > 12 ? 12 : kRingRaw;
   static constexpr int kSmem = kQBytes + kRing * kChunk + 1024;
-  // TMEM: buffer b holds S at 128b and dP at 128b + 64; dO at kTdO
-  static constexpr int kTdO = 256;
+  static constexpr int kTS = 0, kTdP = 128, kTdO = 256;  // TMEM columns
   static_assert(kTdO + DV / 2 <= 512, "TMEM budget");
   static_assert(kRing >= 4, "ring");
 };
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sRing = smem + C::kQBytes;
 
   __shared__ uint64_t rfull[C::kRing], rempty[C::kRing];
-  __shared__ uint64_t q_bar, do_ready, sdp_full[2], buf_free[2], drain_bar;
+  __shared__ uint64_t q_bar, do_ready, s_full, dp_full, s_free, dp_free, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, skip_sh;
 
@@ -136,7 +141,6 @@ __global__ void __launch_bounds__(384, 1)
   int kb0 = 0;
   const int n_kb = wide_blocks_of_qtile(sq, qt, kb0);
   if (n_kb == 0) return;  // nothing visible: no block (the dQ kernel writes zeros)
-  const int n_sub = 2 * n_kb;
   if (threadIdx.x == 0) skip_sh = status_set(p.status) ? 1 : 0;
   __syncthreads();
   if (skip_sh) return;
@@ -150,10 +154,10 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&q_bar, 1);
     mbar_init(&do_ready, 256);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&buf_free[i], 256);
-    }
+    mbar_init(&s_full, 1);
+    mbar_init(&dp_full, 1);
+    mbar_init(&s_free, 256);
+    mbar_init(&dp_free, 256);
     mbar_init(&drain_bar, 1);
     fence_barrier_init();
   }
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Q once; then per 64-key sub-tile its K chunks and V chunks (ring)
+    // Q once; then per block its K chunks and V chunks (ring)
     if (elect_one_lane()) {
       int c1, c2, c3;
       map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
@@ -176,8 +180,8 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
       uint32_t cnt = 0;
       bool ok = true;
-      for (int u = 0; u < n_sub && ok; ++u) {
-        const int krow = sq.k_start + kb0 * 128 + u * 64;
+      for (int n = 0; n < n_kb && ok; ++n) {
+        const int krow = sq.k_start + (kb0 + n) * 128;
         int k1, k2, k3, v1, v2, v3;
         map_coords(p.ok, 0, g, krow, tb, k1, k2, k3);
         map_coords(p.ov, 0, g, krow, tb, v1, v2, v3);
@@ -206,43 +210,54 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_lane()) {
-      constexpr uint32_t idesc = make_idesc(128, 64, BF16, false, false);
+      constexpr uint32_t idesc = make_idesc(128, 128, BF16, false, false);
       const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
       const uint64_t rdesc = make_sdesc(smem_u32(sRing), 16, 1024);
       uint32_t cnt = 0;
       bool ok = mbar_wait(&q_bar, 0, ab) && mbar_wait(&do_ready, 0, ab);
       tc_fence_after();
-      for (int u = 0; u < n_sub && ok; ++u) {
-        const int bf = u & 1;
-        // buffer bf last held sub-tile u-2: the softmax must have loaded it
-        if (u >= 2 && !mbar_wait(&buf_free[bf], ((u - 2) >> 1) & 1u, ab)) break;
+      // next ring chunk (K or V rows of the block), in load order
+      auto chunk = [&]() -> uint64_t {
+        const uint32_t slot = cnt % C::kRing;
+        if (!mbar_wait(&rfull[slot], (cnt / C::kRing) & 1u, ab)) {
+          ok = false;
+          return 0ull;
+        }
         tc_fence_after();
-        const uint32_t dS = tmem + (uint32_t)(128 * bf);
-        const uint32_t dP = dS + 64;
+        return rdesc + (uint64_t)((slot * C::kChunk) >> 4);
+      };
+      auto release = [&]() {
+        mma_commit(&rempty[cnt % C::kRing]);
+        ++cnt;
+      };
+      for (int n = 0; n < n_kb && ok; ++n) {
+        // S of block n-1 must be in the softmax's registers before S is overwritten
+        if (n > 0 && !mbar_wait(&s_free, (n - 1) & 1u, ab)) break;
+        tc_fence_after();
+        for (int c = 0; c < C::kQCh && ok; ++c) {  // S += Q_c K_c^T
+          const uint64_t kd = chunk();
+          if (!ok) break;
+          const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
 #pragma unroll
-        for (int c = 0; c < C::kQCh + C::kVCh; ++c) {
-          const uint32_t slot = cnt % C::kRing;
-          if (!mbar_wait(&rfull[slot], (cnt / C::kRing) & 1u, ab)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t kd = rdesc + (uint64_t)((slot * C::kChunk) >> 4);
-          if (c < C::kQCh) {  // S += Q_c K_c^T
-            const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss(dS, qa + 2 * k, kd + 2 * k, idesc, (c | k) ? 1u : 0u);
-          } else {  // dP += dO_c V_c^T, dO from TMEM (2 elements per column)
-            const int cv = c - C::kQCh;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ts(dP, tmem + C::kTdO + cv * 32 + k * 8, kd + 2 * k, idesc, (cv | k) ? 1u : 0u);
-          }
-          mma_commit(&rempty[slot]);
-          ++cnt;
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + C::kTS, qa + 2 * k, kd + 2 * k, idesc, (c | k) ? 1u : 0u);
+          release();
         }
         if (!ok) break;
-        mma_commit(&sdp_full[bf]);
+        mma_commit(&s_full);
+        if (n > 0 && !mbar_wait(&dp_free, (n - 1) & 1u, ab)) break;
+        tc_fence_after();
+        for (int c = 0; c < C::kVCh && ok; ++c) {  // dP += dO_c V_c^T, dO from TMEM
+          const uint64_t vd = chunk();
+          if (!ok) break;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + C::kTdP, tmem + C::kTdO + c * 32 + k * 8, vd + 2 * k, idesc,
+                   (c | k) ? 1u : 0u);
+          release();
+        }
+        if (!ok) break;
+        mma_commit(&dp_full);
       }
       mma_commit(&drain_bar);
       mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
@@ -250,7 +265,7 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / dS
     const int wq = (warp - 4) & 3;  // TMEM lane quadrant
-    const int wg = (warp - 4) >> 2;  // half of the 64 keys of a sub-tile
+    const int wg = (warp - 4) >> 2;  // 64-key half of a block = its P/dS sub-tile
     const int r = wq * 32 + lane;
     const int i = q0 + r;
     const bool valid = i < sq.lq;
@@ -299,44 +314,63 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t* blk0 = p.blocks + (size_t)(ok ? first : 0) * kWideBlock;
     const float sl2 = p.scale_log2;
     const int sw = r & 7;  // 128-byte swizzle phase of row r
-    for (int u = 0; u < n_sub && ok; ++u) {
-      const int bf = u & 1;
-      if (!mbar_wait_warp(&sdp_full[bf], (u >> 1) & 1u, ab)) {
+    for (int n = 0; n < n_kb && ok; ++n) {
+      if (!mbar_wait_warp(&s_full, n & 1u, ab)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[32], pr[32];
-      tmem_ld32(tmem + lane_off + 128 * bf + 32 * wg, sr);
-      tmem_ld32(tmem + lane_off + 128 * bf + 64 + 32 * wg, pr);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&buf_free[bf]);
-      const long long k0 = (long long)kb0 * 128 + u * 64 + 32 * wg;
-      const long long lo = vlo - k0, hi = vhi - k0;
-      const bool full = lo <= 0 && hi >= 31;
-      uint32_t pw[16], dw[16];
+      float e[64];
+      {
+        uint32_t sa[32], sb[32];  // S columns 0..31 and 32..63 of this half
+        tmem_ld32(tmem + lane_off + C::kTS + 64 * wg, sa);
+        tmem_ld32(tmem + lane_off + C::kTS + 64 * wg + 32, sb);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&s_free);
+        const long long k0 = (long long)(kb0 + n) * 128 + 64 * wg;
+        const long long lo = vlo - k0, hi = vhi - k0;
+        const bool full = lo <= 0 && hi >= 63;
 #pragma unroll
-      for (int t = 0; t < 32; t += 2) {
-        float e0 = ex2(fmaf(__uint_as_float(sr[t]), sl2, -l2));
-        float e1 = ex2(fmaf(__uint_as_float(sr[t + 1]), sl2, -l2));
-        if (!full) {
-          if (t < lo || t > hi) e0 = 0.0f;
-          if (t + 1 < lo || t + 1 > hi) e1 = 0.0f;
+        for (int t = 0; t < 64; ++t) {
+          float x = ex2(fmaf(__uint_as_float(t < 32 ? sa[t] : sb[t - 32]), sl2, -l2));
+          if (!full && (t < lo || t > hi)) x = 0.0f;
+          e[t] = x;
         }
-        pw[t / 2] = Pack<BF16>::two(e0, e1);
-        dw[t / 2] = Pack<BF16>::two(e0 * (__uint_as_float(pr[t]) - dd),
-                                    e1 * (__uint_as_float(pr[t + 1]) - dd));
       }
-      uint8_t* prow = blk0 + (size_t)(u >> 1) * kWideBlock + (u & 1) * kWideTile + r * 128;
+      uint8_t* prow = blk0 + (size_t)n * kWideBlock + wg * kWideTile + r * 128;
       uint8_t* drow = prow + 2 * kWideTile;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int pc = ((4 * wg + cc) ^ sw) * 16;
+      for (int cc = 0; cc < 8; ++cc) {
+        const int pc = (cc ^ sw) * 16;
+        const float* x = e + 8 * cc;
         *reinterpret_cast<uint4*>(prow + pc) =
-            make_uint4(pw[4 * cc], pw[4 * cc + 1], pw[4 * cc + 2], pw[4 * cc + 3]);
-        *reinterpret_cast<uint4*>(drow + pc) =
-            make_uint4(dw[4 * cc], dw[4 * cc + 1], dw[4 * cc + 2], dw[4 * cc + 3]);
+            make_uint4(Pack<BF16>::two(x[0], x[1]), Pack<BF16>::two(x[2], x[3]),
+                       Pack<BF16>::two(x[4], x[5]), Pack<BF16>::two(x[6], x[7]));
+      }
+      if (!mbar_wait_warp(&dp_full, n & 1u, ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t pa[32], pb[32];  // dP columns 0..31 and 32..63 of this half
+      tmem_ld32(tmem + lane_off + C::kTdP + 64 * wg, pa);
+      tmem_ld32(tmem + lane_off + C::kTdP + 64 * wg + 32, pb);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&dp_free);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const int pc = (cc ^ sw) * 16;
+        uint32_t w[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int c = 8 * cc + 2 * t;
+          const float d0 = __uint_as_float(c < 32 ? pa[c] : pb[c - 32]);
+          const float d1 = __uint_as_float(c + 1 < 32 ? pa[c + 1] : pb[c - 31]);
+          w[t] = Pack<BF16>::two(e[c] * (d0 - dd), e[c + 1] * (d1 - dd));
+        }
+        *reinterpret_cast<uint4*>(drow + pc) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     tc_fence_before();
@@ -718,8 +752,8 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
     if (has_k) {
       WideScoresParams sp;
       sp.tm_q = a.tm_q128;
-      sp.tm_k = a.tm_k64;
-      sp.tm_v = a.tm_v64;
+      sp.tm_k = a.tm_k128;
+      sp.tm_v = a.tm_v128;
       sp.oq = a.oq;
       sp.ok = a.ok;
       sp.ov = a.ov;
