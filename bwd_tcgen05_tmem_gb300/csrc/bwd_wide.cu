@@ -93,11 +93,14 @@ __global__ void __launch_bounds__(256) attn_wide_plan_kernel(const WidePlanParam
 
 // ------------------------------------------------------------------ scores
 // Per visible 128-key block: S (N = 128, SS) and dP (N = 128, TS).  Each score
-// MMA covers the whole block: an M = 128 MMA with N = 64 occupies the tensor
-// pipe as long as one with N = 128, so splitting the block into 64-key halves
-// would halve the rate.  TMEM holds one S, one dP and dO; S and dP have their
-// own full / free barriers, so S of block n+1 runs while the softmax waits for
-// dP of block n, and dP of block n+1 while it computes P.
+// MMA covers the whole block: one thread needs about 60 cycles to issue a
+// tcgen05.mma, so an M = 128 MMA with N = 64 (32 cycles of tensor work) would
+// leave the pipe idle half the time.  TMEM holds one S, one dP and dO; S and
+// dP have their own full / free barriers, so S of block n+1 runs while the
+// softmax waits for dP of block n, and dP of block n+1 while it computes P.
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 4..11 softmax (one query row per TMEM lane, the two
+// warpgroups take the two 64-key halves of a block).
 template <int DQK, int DV>
 struct WideScoresCfg {
   static constexpr int kQCh = DQK / 64;
@@ -172,96 +175,104 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Q once; then per block its K chunks and V chunks (ring)
-    if (elect_one_lane()) {
-      int c1, c2, c3;
-      map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
+    int c1, c2, c3;
+    map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
+    if (elect_sync()) {
       mbar_arrive_tx(&q_bar, C::kQBytes);
       for (int c = 0; c < C::kQCh; ++c)
         tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
-      uint32_t cnt = 0;
-      bool ok = true;
-      for (int n = 0; n < n_kb && ok; ++n) {
-        const int krow = sq.k_start + (kb0 + n) * 128;
-        int k1, k2, k3, v1, v2, v3;
-        map_coords(p.ok, 0, g, krow, tb, k1, k2, k3);
-        map_coords(p.ov, 0, g, krow, tb, v1, v2, v3);
+    }
+    __syncwarp();
+    uint32_t cnt = 0;
+    bool ok = true;
+    for (int n = 0; n < n_kb && ok; ++n) {
+      const int krow = sq.k_start + (kb0 + n) * 128;
+      int k1, k2, k3, v1, v2, v3;
+      map_coords(p.ok, 0, g, krow, tb, k1, k2, k3);
+      map_coords(p.ov, 0, g, krow, tb, v1, v2, v3);
 #pragma unroll
-        for (int c = 0; c < C::kQCh + C::kVCh; ++c) {
-          const uint32_t slot = cnt % C::kRing;
-          if (!mbar_wait(&rempty[slot], ((cnt / C::kRing) & 1u) ^ 1u, ab)) {
-            ok = false;
-            break;
-          }
+      for (int c = 0; c < C::kQCh + C::kVCh; ++c) {
+        const uint32_t slot = cnt % C::kRing;
+        if (!mbar_wait_warp(&rempty[slot], ((cnt / C::kRing) & 1u) ^ 1u, ab)) {
+          ok = false;
+          break;
+        }
+        if (elect_sync()) {
           mbar_arrive_tx(&rfull[slot], C::kChunk);
           if (c < C::kQCh)
             tma_load_4d(sRing + slot * C::kChunk, &p.tm_k, &rfull[slot], c * 64, k1, k2, k3);
           else
             tma_load_4d(sRing + slot * C::kChunk, &p.tm_v, &rfull[slot], (c - C::kQCh) * 64, v1,
                         v2, v3);
-          ++cnt;
         }
+        __syncwarp();
+        ++cnt;
       }
-      // let the copies in flight land before the CTA exits
-      mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
-      const uint32_t first = cnt > (uint32_t)C::kRing ? cnt - C::kRing : 0u;
-      for (uint32_t c = first; c < cnt; ++c)
-        mbar_wait_quiet(&rfull[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
     }
+    // let the copies in flight land before the CTA exits
+    mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
+    const uint32_t first = cnt > (uint32_t)C::kRing ? cnt - C::kRing : 0u;
+    for (uint32_t c = first; c < cnt; ++c)
+      mbar_wait_quiet(&rfull[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (elect_one_lane()) {
-      constexpr uint32_t idesc = make_idesc(128, 128, BF16, false, false);
-      const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
-      const uint64_t rdesc = make_sdesc(smem_u32(sRing), 16, 1024);
-      uint32_t cnt = 0;
-      bool ok = mbar_wait(&q_bar, 0, ab) && mbar_wait(&do_ready, 0, ab);
+    constexpr uint32_t idesc = make_idesc(128, 128, BF16, false, false);
+    const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
+    const uint64_t rdesc = make_sdesc(smem_u32(sRing), 16, 1024);
+    uint32_t cnt = 0;
+    bool ok = mbar_wait_warp(&q_bar, 0, ab) && mbar_wait_warp(&do_ready, 0, ab);
+    tc_fence_after();
+    // next ring chunk (K or V rows of the block), in load order
+    auto chunk = [&]() -> uint64_t {
+      const uint32_t slot = cnt % C::kRing;
+      if (!mbar_wait_warp(&rfull[slot], (cnt / C::kRing) & 1u, ab)) {
+        ok = false;
+        return 0ull;
+      }
       tc_fence_after();
-      // next ring chunk (K or V rows of the block), in load order
-      auto chunk = [&]() -> uint64_t {
-        const uint32_t slot = cnt % C::kRing;
-        if (!mbar_wait(&rfull[slot], (cnt / C::kRing) & 1u, ab)) {
-          ok = false;
-          return 0ull;
-        }
-        tc_fence_after();
-        return rdesc + (uint64_t)((slot * C::kChunk) >> 4);
-      };
-      auto release = [&]() {
-        mma_commit(&rempty[cnt % C::kRing]);
-        ++cnt;
-      };
-      for (int n = 0; n < n_kb && ok; ++n) {
-        // S of block n-1 must be in the softmax's registers before S is overwritten
-        if (n > 0 && !mbar_wait(&s_free, (n - 1) & 1u, ab)) break;
-        tc_fence_after();
-        for (int c = 0; c < C::kQCh && ok; ++c) {  // S += Q_c K_c^T
-          const uint64_t kd = chunk();
-          if (!ok) break;
-          const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
+      return rdesc + (uint64_t)((slot * C::kChunk) >> 4);
+    };
+    for (int n = 0; n < n_kb && ok; ++n) {
+      // S of block n-1 must be in the softmax's registers before S is overwritten
+      if (n > 0 && !mbar_wait_warp(&s_free, (n - 1) & 1u, ab)) break;
+      tc_fence_after();
+      for (int c = 0; c < C::kQCh && ok; ++c) {  // S += Q_c K_c^T
+        const uint64_t kd = chunk();
+        if (!ok) break;
+        const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
+        if (elect_sync()) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + C::kTS, qa + 2 * k, kd + 2 * k, idesc, (c | k) ? 1u : 0u);
-          release();
+          mma_commit(&rempty[cnt % C::kRing]);
+          if (c == C::kQCh - 1) mma_commit(&s_full);
         }
+        __syncwarp();
+        ++cnt;
+      }
+      if (!ok) break;
+      if (n > 0 && !mbar_wait_warp(&dp_free, (n - 1) & 1u, ab)) break;
+      tc_fence_after();
+      for (int c = 0; c < C::kVCh && ok; ++c) {  // dP += dO_c V_c^T, dO from TMEM
+        const uint64_t vd = chunk();
         if (!ok) break;
-        mma_commit(&s_full);
-        if (n > 0 && !mbar_wait(&dp_free, (n - 1) & 1u, ab)) break;
-        tc_fence_after();
-        for (int c = 0; c < C::kVCh && ok; ++c) {  // dP += dO_c V_c^T, dO from TMEM
-          const uint64_t vd = chunk();
-          if (!ok) break;
+        if (elect_sync()) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ts(tmem + C::kTdP, tmem + C::kTdO + c * 32 + k * 8, vd + 2 * k, idesc,
                    (c | k) ? 1u : 0u);
-          release();
+          mma_commit(&rempty[cnt % C::kRing]);
+          if (c == C::kVCh - 1) mma_commit(&dp_full);
         }
-        if (!ok) break;
-        mma_commit(&dp_full);
+        __syncwarp();
+        ++cnt;
       }
+    }
+    if (elect_sync()) {
       mma_commit(&drain_bar);
       mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
     }
+    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / dS
     const int wq = (warp - 4) & 3;  // TMEM lane quadrant

@@ -243,6 +243,17 @@ __device__ __forceinline__ void tmem_st_wait() {
 __device__ __forceinline__ uint32_t elect_one_lane() {
   return (threadIdx.x & 31u) == 0u;
 }
+// One lane of a converged warp (the lowest active one, the same lane every
+// time the whole warp calls it).  Issuer loops run on the whole warp, so their
+// addresses and descriptors stay warp-uniform, and issue each tcgen05.mma /
+// commit / TMA copy from the elected lane.
+__device__ __forceinline__ bool elect_sync() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
