@@ -99,6 +99,8 @@ WORKLOADS = {
         Workload("thd_h32_kv8_t65536_d128_bf16", 0, 0, 32, 8, 128, 128, dtype="bf16",
                  thd_total=65536),
         Workload("b1_h16_kv4_s16384_d512", 1, 16384, 16, 4, 512, 512),
+        # the same heads at 4K: a profiling case (inputs above L2, ~2 GB of P/dS)
+        Workload("b1_h16_kv4_s4096_d512", 1, 4096, 16, 4, 512, 512),
         Workload("b1_h16_kv4_s16384_d256_w1024", 1, 16384, 16, 4, 256, 256,
                  window=(1023, 0)),
     ]
