@@ -142,17 +142,22 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // per query tile: the ring chunks (score-only operand), then the stage
-    if (elect_one_lane() && n_it > 0) {
-      int c1, c2, c3;
+    // the whole warp runs the loop (indices stay warp-uniform); one elected
+    // lane issues the copies
+    if (n_it > 0) {
+      int c1, c2, c3, v1, v2, v3;
       map_coords(p.ok, 0, g, sq.k_start + k0, tb, c1, c2, c3);
-      mbar_arrive_tx(&kv_bar, (C::kKSlots + C::kVSlots) * kSlotBytes);
-      for (int c = 0; c < C::kKSlots; ++c)
-        tma_load_4d(sK + c * kSlotBytes, &p.tm_k, &kv_bar, c * 64, c1, c2, c3);
-      if (C::kDK) {
-        map_coords(p.ov, 0, g, sq.k_start + k0, tb, c1, c2, c3);
-        for (int c = 0; c < C::kVSlots; ++c)
-          tma_load_4d(sV + c * kSlotBytes, &p.tm_v, &kv_bar, c * 64, c1, c2, c3);
+      map_coords(p.ov, 0, g, sq.k_start + k0, tb, v1, v2, v3);
+      if (elect_sync()) {
+        mbar_arrive_tx(&kv_bar, (C::kKSlots + C::kVSlots) * kSlotBytes);
+        for (int c = 0; c < C::kKSlots; ++c)
+          tma_load_4d(sK + c * kSlotBytes, &p.tm_k, &kv_bar, c * 64, c1, c2, c3);
+        if (C::kDK) {
+          for (int c = 0; c < C::kVSlots; ++c)
+            tma_load_4d(sV + c * kSlotBytes, &p.tm_v, &kv_bar, c * 64, v1, v2, v3);
+        }
       }
+      __syncwarp();
       uint32_t rcnt = 0;
       int it = 0;
       bool ok = true;
@@ -168,35 +173,41 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < nch; ++c, ++rcnt) {
             const uint32_t slot = rcnt % C::kRing;
-            if (!mbar_wait(&rempty[slot], ((rcnt / C::kRing) & 1u) ^ 1u, ab)) {
+            if (!mbar_wait_warp(&rempty[slot], ((rcnt / C::kRing) & 1u) ^ 1u, ab)) {
               ok = false;
               break;
             }
-            mbar_arrive_tx(&rfull[slot], C::kChunk);
-            if (C::kQStaged)
-              tma_load_4d(sRing + slot * C::kChunk, m, &rfull[slot], c * 64, dc1, dc2, dc3);
-            else
-              tma_load_4d(sRing + slot * C::kChunk, m, &rfull[slot], c * 64, qc1, qc2, qc3);
+            if (elect_sync()) {
+              mbar_arrive_tx(&rfull[slot], C::kChunk);
+              if (C::kQStaged)
+                tma_load_4d(sRing + slot * C::kChunk, m, &rfull[slot], c * 64, dc1, dc2, dc3);
+              else
+                tma_load_4d(sRing + slot * C::kChunk, m, &rfull[slot], c * 64, qc1, qc2, qc3);
+            }
+            __syncwarp();
           }
           if (!ok) break;
         }
         const int st = it % C::kStages;
-        if (!mbar_wait(&sempty[st], ((it / C::kStages) & 1) ^ 1, ab)) {
+        if (!mbar_wait_warp(&sempty[st], ((it / C::kStages) & 1) ^ 1, ab)) {
           ok = false;
           break;
         }
-        mbar_arrive_tx(&sfull[st], C::kStageBytes);
-        uint8_t* dst = sStage + st * C::kStageBytes;
-        if constexpr (C::kQStaged) {
+        if (elect_sync()) {
+          mbar_arrive_tx(&sfull[st], C::kStageBytes);
+          uint8_t* dst = sStage + st * C::kStageBytes;
+          if constexpr (C::kQStaged) {
 #pragma unroll
-          for (int c = 0; c < C::kQCh; ++c)
-            tma_load_4d(dst + kQOff + c * C::kChunk, &p.tm_q, &sfull[st], c * 64, qc1, qc2, qc3);
-        }
-        if constexpr (C::kDStaged) {
+            for (int c = 0; c < C::kQCh; ++c)
+              tma_load_4d(dst + kQOff + c * C::kChunk, &p.tm_q, &sfull[st], c * 64, qc1, qc2, qc3);
+          }
+          if constexpr (C::kDStaged) {
 #pragma unroll
-          for (int c = 0; c < C::kDoCh; ++c)
-            tma_load_4d(dst + kDOff + c * C::kChunk, &p.tm_do, &sfull[st], c * 64, dc1, dc2, dc3);
+            for (int c = 0; c < C::kDoCh; ++c)
+              tma_load_4d(dst + kDOff + c * C::kChunk, &p.tm_do, &sfull[st], c * 64, dc1, dc2, dc3);
+          }
         }
+        __syncwarp();
       }
       mbar_wait_quiet(&kv_bar, 0, kWaitLimitNs);
       const uint32_t first = rcnt > (uint32_t)C::kRing ? rcnt - C::kRing : 0u;
@@ -208,7 +219,8 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (elect_one_lane() && n_it > 0) {
+    // the whole warp runs the loop; the elected lane issues every MMA and commit
+    if (n_it > 0) {
       constexpr uint32_t idesc_s = make_idesc(128, BQ, BF16, false, false);
       constexpr uint32_t idesc_v = make_idesc(128, DV, BF16, false, true);
       constexpr uint32_t idesc_k = make_idesc(128, DQK, BF16, false, true);
@@ -218,28 +230,27 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t stdesc_mn = make_sdesc(smem_u32(sStage), C::kChunk, 1024);  // MN-major view
       const uint64_t rdesc = make_sdesc(smem_u32(sRing), 16, 1024);
       uint32_t rcnt = 0;
-      bool ok = mbar_wait(&kv_bar, 0, ab);
+      bool ok = mbar_wait_warp(&kv_bar, 0, ab);
       tc_fence_after();
       // ring chunks are consumed one by one in load order and released as soon
       // as their score MMAs complete; the stage is held until issue_acc
       auto ring_chunk = [&]() -> uint64_t {
         const uint32_t slot = rcnt % C::kRing;
-        if (!mbar_wait(&rfull[slot], (rcnt / C::kRing) & 1u, ab)) {
+        if (!mbar_wait_warp(&rfull[slot], (rcnt / C::kRing) & 1u, ab)) {
           ok = false;
           return 0ull;
         }
         tc_fence_after();
         return rdesc + (uint64_t)((slot * C::kChunk) >> 4);
       };
-      auto ring_release = [&]() {
+      auto ring_release = [&]() {  // called by the elected lane
         mma_commit(&rempty[rcnt % C::kRing]);
-        ++rcnt;
       };
       // The stage of tile `it` is awaited only right before its first use:
       // the producer loads a tile's ring chunks before its stage, so waiting
       // for the stage first would deadlock once the ring is full.
       auto wait_stage = [&](int it) {
-        if (!mbar_wait(&sfull[it % C::kStages], (it / C::kStages) & 1, ab)) ok = false;
+        if (!mbar_wait_warp(&sfull[it % C::kStages], (it / C::kStages) & 1, ab)) ok = false;
         tc_fence_after();
       };
       auto issue_scores = [&](int it) {
@@ -260,9 +271,14 @@ __global__ void __launch_bounds__(384, 1)
             qb = ring_chunk();
             if (!ok) return;
           }
+          if (elect_sync()) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mma_ss(tmem + C::kTS, ka + 2 * k, qb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
-          if constexpr (!C::kQStaged) ring_release();
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + C::kTS, ka + 2 * k, qb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+            if constexpr (!C::kQStaged) ring_release();
+          }
+          __syncwarp();
+          if constexpr (!C::kQStaged) ++rcnt;
         }
         // dP^T = V dO^T
         if constexpr (C::kDK) {
@@ -280,12 +296,18 @@ __global__ void __launch_bounds__(384, 1)
               db = ring_chunk();
               if (!ok) return;
             }
+            if (elect_sync()) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss(tmem + C::kTdP, va + 2 * k, db + 2 * k, idesc_s, (c | k) ? 1u : 0u);
-            if constexpr (!C::kDStaged) ring_release();
+              for (int k = 0; k < 4; ++k)
+                mma_ss(tmem + C::kTdP, va + 2 * k, db + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+              if constexpr (!C::kDStaged) ring_release();
+            }
+            __syncwarp();
+            if constexpr (!C::kDStaged) ++rcnt;
           }
         }
-        mma_commit(&sdp_full);
+        if (elect_sync()) mma_commit(&sdp_full);
+        __syncwarp();
       };
       auto issue_acc = [&](int it) {
         const int st = it % C::kStages;
@@ -293,36 +315,42 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) return;
         const uint32_t st_off = (uint32_t)((st * C::kStageBytes) >> 4);
         const uint32_t first = it > 0 ? 1u : 0u;
-        if constexpr (C::kDV) {  // dV += P^T dO   (dO stage MN-major, N = DV)
-          const uint64_t db = stdesc_mn + st_off + (uint64_t)(kDOff >> 4);
-          mma_ts(tmem + C::kTdV, tmem + C::kTP, db, idesc_v, first);
+        if (elect_sync()) {
+          if constexpr (C::kDV) {  // dV += P^T dO   (dO stage MN-major, N = DV)
+            const uint64_t db = stdesc_mn + st_off + (uint64_t)(kDOff >> 4);
+            mma_ts(tmem + C::kTdV, tmem + C::kTP, db, idesc_v, first);
 #pragma unroll
-          for (int k = 1; k < BQ / 16; ++k)
-            mma_ts(tmem + C::kTdV, tmem + C::kTP + k * 8, db + k * 128, idesc_v, 1u);
-        }
-        if constexpr (C::kDK) {  // dK += dS^T Q   (Q stage MN-major, N = DQK)
-          const uint64_t qb = stdesc_mn + st_off + (uint64_t)(kQOff >> 4);
-          mma_ts(tmem + C::kTdK, tmem + C::kTdS, qb, idesc_k, first);
+            for (int k = 1; k < BQ / 16; ++k)
+              mma_ts(tmem + C::kTdV, tmem + C::kTP + k * 8, db + k * 128, idesc_v, 1u);
+          }
+          if constexpr (C::kDK) {  // dK += dS^T Q   (Q stage MN-major, N = DQK)
+            const uint64_t qb = stdesc_mn + st_off + (uint64_t)(kQOff >> 4);
+            mma_ts(tmem + C::kTdK, tmem + C::kTdS, qb, idesc_k, first);
 #pragma unroll
-          for (int k = 1; k < BQ / 16; ++k)
-            mma_ts(tmem + C::kTdK, tmem + C::kTdS + k * 8, qb + k * 128, idesc_k, 1u);
+            for (int k = 1; k < BQ / 16; ++k)
+              mma_ts(tmem + C::kTdK, tmem + C::kTdS + k * 8, qb + k * 128, idesc_k, 1u);
+          }
+          mma_commit(&sempty[st]);
+          mma_commit(&acc_done);
         }
-        mma_commit(&sempty[st]);
-        mma_commit(&acc_done);
+        __syncwarp();
       };
       if (ok) issue_scores(0);
       for (int it = 0; it < n_it && ok; ++it) {
         if (it + 1 < n_it) {
-          if (!mbar_wait(&sc_free, it & 1u, ab)) break;
+          if (!mbar_wait_warp(&sc_free, it & 1u, ab)) break;
           issue_scores(it + 1);
           if (!ok) break;
         }
-        if (!mbar_wait(&pds_full, it & 1u, ab)) break;
+        if (!mbar_wait_warp(&pds_full, it & 1u, ab)) break;
         tc_fence_after();
         issue_acc(it);
       }
-      mma_commit(&drain_bar);
-      mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+      if (elect_sync()) {
+        mma_commit(&drain_bar);
+        mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+      }
+      __syncwarp();
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ LSE / D loader

@@ -112,15 +112,20 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // per key tile: V chunks (ring), then the K stage
-    if (elect_one_lane() && n_kv > 0) {
-      int c1, c2, c3;
+    // the whole warp runs the loop (indices stay warp-uniform); one elected
+    // lane issues the copies
+    if (n_kv > 0) {
+      int c1, c2, c3, o1, o2, o3;
       map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
-      mbar_arrive_tx(&q_bar, (C::kQSlots + C::kDoSlots) * kSlotBytes);
-      for (int c = 0; c < C::kQSlots; ++c)
-        tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
-      map_coords(p.odo, 0, h, sq.q_start + q0, tb, c1, c2, c3);
-      for (int c = 0; c < C::kDoSlots; ++c)
-        tma_load_4d(sDo + c * kSlotBytes, &p.tm_do, &q_bar, c * 64, c1, c2, c3);
+      map_coords(p.odo, 0, h, sq.q_start + q0, tb, o1, o2, o3);
+      if (elect_sync()) {
+        mbar_arrive_tx(&q_bar, (C::kQSlots + C::kDoSlots) * kSlotBytes);
+        for (int c = 0; c < C::kQSlots; ++c)
+          tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
+        for (int c = 0; c < C::kDoSlots; ++c)
+          tma_load_4d(sDo + c * kSlotBytes, &p.tm_do, &q_bar, c * 64, o1, o2, o3);
+      }
+      __syncwarp();
       uint32_t vcnt = 0;
       int jt = 0;
       bool ok = true;
@@ -131,25 +136,31 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
 #pragma unroll
         for (int c = 0; c < C::kVCh; ++c, ++vcnt) {
           const uint32_t slot = vcnt % C::kVRing;
-          if (!mbar_wait(&vempty[slot], ((vcnt / C::kVRing) & 1u) ^ 1u, ab)) {
+          if (!mbar_wait_warp(&vempty[slot], ((vcnt / C::kVRing) & 1u) ^ 1u, ab)) {
             ok = false;
             break;
           }
-          mbar_arrive_tx(&vfull[slot], C::kChunk);
-          tma_load_4d(sV + slot * C::kChunk, &p.tm_v, &vfull[slot], c * 64, d1, d2, d3);
+          if (elect_sync()) {
+            mbar_arrive_tx(&vfull[slot], C::kChunk);
+            tma_load_4d(sV + slot * C::kChunk, &p.tm_v, &vfull[slot], c * 64, d1, d2, d3);
+          }
+          __syncwarp();
         }
         if (!ok) break;
         const int st = jt % C::kKStages;
-        if (!mbar_wait(&kempty[st], ((jt / C::kKStages) & 1) ^ 1, ab)) {
+        if (!mbar_wait_warp(&kempty[st], ((jt / C::kKStages) & 1) ^ 1, ab)) {
           ok = false;
           break;
         }
         map_coords(p.ok, 0, g, krow, tb, d1, d2, d3);
-        mbar_arrive_tx(&kfull[st], C::kKStage);
+        if (elect_sync()) {
+          mbar_arrive_tx(&kfull[st], C::kKStage);
 #pragma unroll
-        for (int c = 0; c < C::kKCh; ++c)
-          tma_load_4d(sK + st * C::kKStage + c * C::kChunk, &p.tm_k, &kfull[st], c * 64, d1, d2,
-                      d3);
+          for (int c = 0; c < C::kKCh; ++c)
+            tma_load_4d(sK + st * C::kKStage + c * C::kChunk, &p.tm_k, &kfull[st], c * 64, d1, d2,
+                        d3);
+        }
+        __syncwarp();
       }
       mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
       const uint32_t first = vcnt > (uint32_t)C::kVRing ? vcnt - C::kVRing : 0u;
@@ -161,7 +172,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (elect_one_lane() && n_kv > 0) {
+    // the whole warp runs the loop; the elected lane issues every MMA and commit
+    if (n_kv > 0) {
       constexpr uint32_t idesc_s = make_idesc(128, BKV, BF16, false, false);
       constexpr uint32_t idesc_q = make_idesc(128, DQK, BF16, false, true);
       const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
@@ -170,62 +182,75 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
       const uint64_t kdesc_mn = make_sdesc(smem_u32(sK), C::kChunk, 1024);
       const uint64_t vdesc = make_sdesc(smem_u32(sV), 16, 1024);
       uint32_t vcnt = 0;
-      bool ok = mbar_wait(&q_bar, 0, ab);
+      bool ok = mbar_wait_warp(&q_bar, 0, ab);
       tc_fence_after();
       auto issue_scores = [&](int jt) {
 #pragma unroll
         for (int c = 0; c < C::kVCh; ++c, ++vcnt) {  // dP = dO V^T
           const uint32_t slot = vcnt % C::kVRing;
-          if (!mbar_wait(&vfull[slot], (vcnt / C::kVRing) & 1u, ab)) {
+          if (!mbar_wait_warp(&vfull[slot], (vcnt / C::kVRing) & 1u, ab)) {
             ok = false;
             return;
           }
           tc_fence_after();
           const uint64_t da = ddesc + (uint64_t)(c * (kSlotBytes >> 4));
           const uint64_t vb = vdesc + (uint64_t)(slot * (C::kChunk >> 4));
+          if (elect_sync()) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + C::kTdP, da + 2 * k, vb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
-          mma_commit(&vempty[slot]);
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + C::kTdP, da + 2 * k, vb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+            mma_commit(&vempty[slot]);
+          }
+          __syncwarp();
         }
         const int st = jt % C::kKStages;  // S = Q K^T
-        if (!mbar_wait(&kfull[st], (jt / C::kKStages) & 1, ab)) {
+        if (!mbar_wait_warp(&kfull[st], (jt / C::kKStages) & 1, ab)) {
           ok = false;
           return;
         }
         tc_fence_after();
+        if (elect_sync()) {
 #pragma unroll
-        for (int c = 0; c < C::kKCh; ++c) {
-          const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
-          const uint64_t kb = kdesc + (uint64_t)((st * C::kKStage + c * C::kChunk) >> 4);
+          for (int c = 0; c < C::kKCh; ++c) {
+            const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
+            const uint64_t kb = kdesc + (uint64_t)((st * C::kKStage + c * C::kChunk) >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mma_ss(tmem, qa + 2 * k, kb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem, qa + 2 * k, kb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+          }
+          mma_commit(&sdp_full);
         }
-        mma_commit(&sdp_full);
+        __syncwarp();
       };
       auto issue_dq = [&](int jt) {  // dQ += dS K  (K stage read MN-major, N = DQK)
         const int st = jt % C::kKStages;
         const uint64_t kb = kdesc_mn + (uint64_t)((st * C::kKStage) >> 4);
-        mma_ts(tmem + C::kTdQ, tmem + C::kTdS, kb, idesc_q, jt > 0 ? 1u : 0u);
+        if (elect_sync()) {
+          mma_ts(tmem + C::kTdQ, tmem + C::kTdS, kb, idesc_q, jt > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 1; k < BKV / 16; ++k)
-          mma_ts(tmem + C::kTdQ, tmem + C::kTdS + k * 8, kb + k * 128, idesc_q, 1u);
-        mma_commit(&kempty[st]);
-        mma_commit(&dq_done);
+          for (int k = 1; k < BKV / 16; ++k)
+            mma_ts(tmem + C::kTdQ, tmem + C::kTdS + k * 8, kb + k * 128, idesc_q, 1u);
+          mma_commit(&kempty[st]);
+          mma_commit(&dq_done);
+        }
+        __syncwarp();
       };
       if (ok) issue_scores(0);
       for (int jt = 0; jt < n_kv && ok; ++jt) {
         if (jt + 1 < n_kv) {
-          if (!mbar_wait(&sc_free, jt & 1u, ab)) break;
+          if (!mbar_wait_warp(&sc_free, jt & 1u, ab)) break;
           issue_scores(jt + 1);
           if (!ok) break;
         }
-        if (!mbar_wait(&ds_full, jt & 1u, ab)) break;
+        if (!mbar_wait_warp(&ds_full, jt & 1u, ab)) break;
         tc_fence_after();
         issue_dq(jt);
       }
-      mma_commit(&drain_bar);
-      mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+      if (elect_sync()) {
+        mma_commit(&drain_bar);
+        mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+      }
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / dS

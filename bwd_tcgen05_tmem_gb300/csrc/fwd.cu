@@ -111,15 +111,20 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // load order = MMA order: K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1)
-    if (elect_one_lane() && n_kv > 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
+    // the whole warp runs the loop (indices stay warp-uniform); one elected
+    // lane issues the copies
+    if (n_kv > 0) {
       int c1, c2, c3;
       map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
-      mbar_arrive_tx(&q_bar, C::kQSlots * kSlotBytes);
-      for (int c = 0; c < C::kQSlots; ++c)
-        tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
+      if (elect_sync()) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        mbar_arrive_tx(&q_bar, C::kQSlots * kSlotBytes);
+        for (int c = 0; c < C::kQSlots; ++c)
+          tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
+      }
+      __syncwarp();
       uint32_t kcnt = 0;
       int vcnt = 0;
       bool ok = true;
@@ -129,27 +134,33 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
         for (int c = 0; c < C::kKCh; ++c, ++kcnt) {
           const uint32_t slot = kcnt % C::kKRing;
-          if (!mbar_wait(&kempty[slot], ((kcnt / C::kKRing) & 1u) ^ 1u, ab)) {
+          if (!mbar_wait_warp(&kempty[slot], ((kcnt / C::kKRing) & 1u) ^ 1u, ab)) {
             ok = false;
             return;
           }
-          mbar_arrive_tx(&kfull[slot], kSlotBytes);
-          tma_load_4d(sK + slot * kSlotBytes, &p.tm_k, &kfull[slot], c * 64, d1, d2, d3);
+          if (elect_sync()) {
+            mbar_arrive_tx(&kfull[slot], kSlotBytes);
+            tma_load_4d(sK + slot * kSlotBytes, &p.tm_k, &kfull[slot], c * 64, d1, d2, d3);
+          }
+          __syncwarp();
         }
       };
       auto load_v = [&](int jt) {
         int d1, d2, d3;
         map_coords(p.ov, 0, g, sq.k_start + (kt0 + jt) * kBlockN, tb, d1, d2, d3);
         const int st = vcnt % C::kVStages;
-        if (!mbar_wait(&vempty[st], ((vcnt / C::kVStages) & 1) ^ 1, ab)) {
+        if (!mbar_wait_warp(&vempty[st], ((vcnt / C::kVStages) & 1) ^ 1, ab)) {
           ok = false;
           return;
         }
-        mbar_arrive_tx(&vfull[st], C::kVCh * kSlotBytes);
+        if (elect_sync()) {
+          mbar_arrive_tx(&vfull[st], C::kVCh * kSlotBytes);
 #pragma unroll
-        for (int c = 0; c < C::kVCh; ++c)
-          tma_load_4d(sV + (st * C::kVCh + c) * kSlotBytes, &p.tm_v, &vfull[st],
-                      split * DV_CTA + c * 64, d1, d2, d3);
+          for (int c = 0; c < C::kVCh; ++c)
+            tma_load_4d(sV + (st * C::kVCh + c) * kSlotBytes, &p.tm_v, &vfull[st],
+                        split * DV_CTA + c * 64, d1, d2, d3);
+        }
+        __syncwarp();
         ++vcnt;
       };
       load_k(0);
@@ -170,8 +181,9 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
     // warp 1 issues S = Q K^T, warp 2 issues O += P V: each blocks on its own
     // barriers while the other keeps the tensor pipe fed.  Descriptors are
     // built once; per MMA only small constant offsets are added (the
-    // start-address field counts 16-byte units).
-    if (elect_one_lane() && n_kv > 0) {
+    // start-address field counts 16-byte units).  The whole warp runs the
+    // loop; the elected lane issues every MMA and commit.
+    if (n_kv > 0) {
       const bool s_role = warp == 1;
       constexpr uint32_t idesc_s = make_idesc(128, 128, BF16, false, false);
       constexpr uint32_t idesc_o = make_idesc(128, DV_CTA, BF16, false, true);
@@ -179,60 +191,70 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       const uint64_t kdesc = make_sdesc(smem_u32(sK), 16, 1024);
       const uint64_t vdesc = make_sdesc(smem_u32(sV), kSlotBytes, 1024);
       uint32_t kcnt = 0;
-      bool ok = s_role ? mbar_wait(&q_bar, 0, ab) : true;
+      bool ok = s_role ? mbar_wait_warp(&q_bar, 0, ab) : true;
       tc_fence_after();
       auto issue_s = [&](int jt) {
         const uint32_t d = tmem + (uint32_t)((jt % C::kSB) * 128);
 #pragma unroll
         for (int c = 0; c < C::kKCh; ++c, ++kcnt) {
           const uint32_t slot = kcnt % C::kKRing;
-          if (!mbar_wait(&kfull[slot], (kcnt / C::kKRing) & 1u, ab)) {
+          if (!mbar_wait_warp(&kfull[slot], (kcnt / C::kKRing) & 1u, ab)) {
             ok = false;
             return;
           }
           tc_fence_after();
           const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
           const uint64_t kb = kdesc + (uint64_t)(slot * (kSlotBytes >> 4));
+          if (elect_sync()) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(d, qa + 2 * k, kb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
-          mma_commit(&kempty[slot]);
+            for (int k = 0; k < 4; ++k)
+              mma_ss(d, qa + 2 * k, kb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+            mma_commit(&kempty[slot]);
+            if (c == C::kKCh - 1) mma_commit(&s_full[jt % C::kSB]);
+          }
+          __syncwarp();
         }
-        mma_commit(&s_full[jt % C::kSB]);
       };
       auto issue_pv = [&](int jt) {
-        if (!mbar_wait(&p_full[jt % C::kSB], (jt / C::kSB) & 1u, ab)) {
+        if (!mbar_wait_warp(&p_full[jt % C::kSB], (jt / C::kSB) & 1u, ab)) {
           ok = false;
           return;
         }
         const int st = jt % C::kVStages;
-        if (!mbar_wait(&vfull[st], (jt / C::kVStages) & 1, ab)) {
+        if (!mbar_wait_warp(&vfull[st], (jt / C::kVStages) & 1, ab)) {
           ok = false;
           return;
         }
         tc_fence_after();
         const uint32_t pa = tmem + (uint32_t)((jt % C::kSB) * 128);
         const uint64_t vb = vdesc + (uint64_t)(st * C::kVCh * (kSlotBytes >> 4));
-        mma_ts(tmem + C::kTmemO, pa, vb, idesc_o, jt > 0 ? 1u : 0u);
+        if (elect_sync()) {
+          mma_ts(tmem + C::kTmemO, pa, vb, idesc_o, jt > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 1; k < 8; ++k) mma_ts(tmem + C::kTmemO, pa + k * 8, vb + k * 128, idesc_o, 1u);
-        mma_commit(&vempty[st]);
-        mma_commit(&o_done[jt % C::kSB]);
+          for (int k = 1; k < 8; ++k)
+            mma_ts(tmem + C::kTmemO, pa + k * 8, vb + k * 128, idesc_o, 1u);
+          mma_commit(&vempty[st]);
+          mma_commit(&o_done[jt % C::kSB]);
+        }
+        __syncwarp();
       };
       if (s_role) {
         for (int jt = 0; jt < n_kv && ok; ++jt) {
           // S buffer jt%kSB last held P(jt-kSB): wait until PV(jt-kSB) has read it
-          if (jt >= C::kSB && !mbar_wait(&o_done[jt % C::kSB], ((jt - C::kSB) / C::kSB) & 1u, ab))
+          if (jt >= C::kSB &&
+              !mbar_wait_warp(&o_done[jt % C::kSB], ((jt - C::kSB) / C::kSB) & 1u, ab))
             break;
           issue_s(jt);
         }
-        mma_commit(&drain_bar);
-        mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
       } else {
         for (int jt = 0; jt < n_kv && ok; ++jt) issue_pv(jt);
-        mma_commit(&drain_bar2);
-        mbar_wait_quiet(&drain_bar2, 0, kWaitLimitNs);
       }
+      uint64_t* drain = s_role ? &drain_bar : &drain_bar2;
+      if (elect_sync()) {
+        mma_commit(drain);
+        mbar_wait_quiet(drain, 0, kWaitLimitNs);
+      }
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
