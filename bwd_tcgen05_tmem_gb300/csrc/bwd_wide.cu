@@ -489,7 +489,9 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ producer
     const long long T_b = p.plan[b + 1] - p.plan[b];
     const long long pre0 = wide_row_prefix(sq, KIND == 0 ? tile : qt0);  // whole warp
-    if (elect_one_lane() && n_steps > 0) {
+    // the whole warp runs the loop (its values stay warp-uniform); one elected
+    // lane issues the copies
+    if (n_steps > 0) {
       const CUtensorMap* bmap = (KIND == 1 && which == 1) ? &p.tm_b1 : &p.tm_b0;
       const MapOrder bord = (KIND == 1 && which == 1) ? p.ob1 : p.ob0;
       uint32_t bcnt = 0;
@@ -515,40 +517,49 @@ __global__ void __launch_bounds__(384, 1)
           bhead = h;
         }
         if (blk < 0 || blk >= p.cap) {
-          raise_status(p.status, DEV_WORKSPACE);
-          *(volatile int*)&abort_flag = 1;
+          if (elect_sync()) {
+            raise_status(p.status, DEV_WORKSPACE);
+            *(volatile int*)&abort_flag = 1;
+          }
+          __syncwarp();
           ok = false;
           break;
         }
         const uint8_t* src = p.blocks + (size_t)blk * kWideBlock;
         const int as = s % C::kNA;
-        if (!mbar_wait(&aempty[as], ((s / C::kNA) & 1) ^ 1, ab)) {
+        if (!mbar_wait_warp(&aempty[as], ((s / C::kNA) & 1) ^ 1, ab)) {
           ok = false;
           break;
         }
-        mbar_arrive_tx(&afull[as], C::kA);
         uint8_t* adst = sA + as * C::kA;
-        if (KIND == 0) {  // dS sub-tile `half`: 128 query rows x 64 keys
-          bulk_load(adst, src + 2 * kWideTile + half * kWideTile, kWideTile, &afull[as]);
-        } else {  // query rows [64 half, 64 half + 64) of both 64-key sub-tiles
-          const uint8_t* t0 = src + (which ? 2 * kWideTile : 0) + half * (kWideTile / 2);
-          bulk_load(adst, t0, kWideTile / 2, &afull[as]);
-          bulk_load(adst + kWideTile / 2, t0 + kWideTile, kWideTile / 2, &afull[as]);
+        if (elect_sync()) {
+          mbar_arrive_tx(&afull[as], C::kA);
+          if (KIND == 0) {  // dS sub-tile `half`: 128 query rows x 64 keys
+            bulk_load(adst, src + 2 * kWideTile + half * kWideTile, kWideTile, &afull[as]);
+          } else {  // query rows [64 half, 64 half + 64) of both 64-key sub-tiles
+            const uint8_t* t0 = src + (which ? 2 * kWideTile : 0) + half * (kWideTile / 2);
+            bulk_load(adst, t0, kWideTile / 2, &afull[as]);
+            bulk_load(adst + kWideTile / 2, t0 + kWideTile, kWideTile / 2, &afull[as]);
+          }
         }
+        __syncwarp();
         int c1, c2, c3;
         map_coords(bord, 0, bhead, brow, tb, c1, c2, c3);
 #pragma unroll
         for (int nh = 0; nh < C::kNH; ++nh, ++bcnt) {
           const uint32_t q = bcnt % C::kNB;
-          if (!mbar_wait(&bempty[q], ((bcnt / C::kNB) & 1u) ^ 1u, ab)) {
+          if (!mbar_wait_warp(&bempty[q], ((bcnt / C::kNB) & 1u) ^ 1u, ab)) {
             ok = false;
             break;
           }
-          mbar_arrive_tx(&bfull[q], C::kQuad);
+          if (elect_sync()) {
+            mbar_arrive_tx(&bfull[q], C::kQuad);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tma_load_4d(sB + q * C::kQuad + c * C::kChunk, bmap, &bfull[q], (4 * nh + c) * 64, c1,
-                        c2, c3);
+            for (int c = 0; c < 4; ++c)
+              tma_load_4d(sB + q * C::kQuad + c * C::kChunk, bmap, &bfull[q], (4 * nh + c) * 64,
+                          c1, c2, c3);
+          }
+          __syncwarp();
         }
         if (KIND == 1 && half == 1) {  // next query tile (then next head)
           int kbq;
@@ -569,7 +580,8 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (elect_one_lane() && n_steps > 0) {
+    // the whole warp runs the loop; the elected lane issues every MMA and commit
+    if (n_steps > 0) {
       constexpr uint32_t idesc = make_idesc(128, 256, BF16, KIND == 1, true);
       const uint64_t adesc = KIND == 0 ? make_sdesc(smem_u32(sA), 16, 1024)
                                        : make_sdesc(smem_u32(sA), kWideTile / 2, 1024);
@@ -578,29 +590,36 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       for (int s = 0; s < n_steps && ok; ++s) {
         const int as = s % C::kNA;
-        if (!mbar_wait(&afull[as], (s / C::kNA) & 1, ab)) break;
+        if (!mbar_wait_warp(&afull[as], (s / C::kNA) & 1, ab)) break;
         tc_fence_after();
         const uint64_t ad = adesc + (uint64_t)((as * C::kA) >> 4);
 #pragma unroll
         for (int nh = 0; nh < C::kNH; ++nh, ++bcnt) {
           const uint32_t q = bcnt % C::kNB;
-          if (!mbar_wait(&bfull[q], (bcnt / C::kNB) & 1u, ab)) {
+          if (!mbar_wait_warp(&bfull[q], (bcnt / C::kNB) & 1u, ab)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t bd = bdesc + (uint64_t)((q * C::kQuad) >> 4);
+          if (elect_sync()) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + 256 * nh, ad + (KIND == 0 ? 2 * k : 128 * k), bd + 128 * k, idesc,
-                   (s | k) ? 1u : 0u);
-          mma_commit(&bempty[q]);
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + 256 * nh, ad + (KIND == 0 ? 2 * k : 128 * k), bd + 128 * k, idesc,
+                     (s | k) ? 1u : 0u);
+            mma_commit(&bempty[q]);
+          }
+          __syncwarp();
         }
-        mma_commit(&aempty[as]);
+        if (elect_sync()) mma_commit(&aempty[as]);
+        __syncwarp();
       }
-      mma_commit(&acc_done);
-      mma_commit(&drain_bar);
-      mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+      if (elect_sync()) {
+        mma_commit(&acc_done);
+        mma_commit(&drain_bar);
+        mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+      }
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue

@@ -240,9 +240,6 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 // ----------------------------------------------------------------- misc
-__device__ __forceinline__ uint32_t elect_one_lane() {
-  return (threadIdx.x & 31u) == 0u;
-}
 // One lane of a converged warp (the lowest active one, the same lane every
 // time the whole warp calls it).  Issuer loops run on the whole warp, so their
 // addresses and descriptors stay warp-uniform, and issue each tcgen05.mma /
