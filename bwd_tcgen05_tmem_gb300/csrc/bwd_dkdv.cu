@@ -19,7 +19,9 @@
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
 // MMA issuer, warp 2 loads LSE_i / D_i into shared memory, warps 4..11 two
-// softmax warpgroups splitting the BQ query columns.
+// softmax warpgroups splitting the BQ query columns.  The producer and issuer
+// warps run their loops on all 32 lanes and issue each copy, MMA and commit
+// from an elect.sync lane.
 #include "bwd.h"
 
 namespace attn {

@@ -14,7 +14,8 @@
 // columns [w*BKV/2, (w+1)*BKV/2) of every tile (the backward needs no row
 // reduction, so splitting columns is free).  The softmax signals "scores
 // consumed" right after loading S/dP so the next tile's S/dP MMAs overlap the
-// exponentials.
+// exponentials.  The producer and issuer warps run their loops on all 32
+// lanes and issue each copy, MMA and commit from an elect.sync lane.
 // TMEM: S [0,BKV)  dP [BKV,2BKV)  dS [2BKV, 2.5BKV) (16-bit, 2 per column)
 //       dQ [kTdQ, kTdQ + DQK).
 #include "bwd.h"

@@ -8,8 +8,10 @@
 // One CTA owns 128 query rows of one (sequence, query head) and, for head dim
 // 512, one half of the value columns.  Warp roles (256 threads):
 //   warp 0      TMA producer: Q once, then K chunks (ring) and V tiles (stages)
-//   warp 1      TMEM allocator and S-MMA issuer (one thread)
-//   warp 2      PV-MMA issuer (one thread)
+//   warp 1      TMEM allocator and S-MMA issuer
+//   warp 2      PV-MMA issuer
+//   (warps 0-2 run their loops on all 32 lanes and issue each copy, MMA and
+//   commit from an elect.sync lane)
 //   warps 4..7  softmax: one TMEM lane (= query row) per thread; rescales O
 //               in TMEM when the running maximum grows, writes P (16-bit)
 //               into TMEM, and runs the epilogue.
