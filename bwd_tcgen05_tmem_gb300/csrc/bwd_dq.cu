@@ -10,7 +10,7 @@
 // the result is bitwise reproducible.
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer, warps 4..11 two softmax warpgroups; warpgroup w owns key
+// S/dP issuer, warp 2 dQ issuer, warps 4..11 two softmax warpgroups; warpgroup w owns key
 // columns [w*BKV/2, (w+1)*BKV/2) of every tile (the backward needs no row
 // reduction, so splitting columns is free).  The softmax signals "scores
 // consumed" right after loading S/dP so the next tile's S/dP MMAs overlap the
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
   uint8_t* sV = sK + C::kKStages * C::kKStage;
 
   __shared__ uint64_t kfull[C::kKStages], kempty[C::kKStages], vfull[C::kVRing], vempty[C::kVRing];
-  __shared__ uint64_t q_bar, sdp_full, sc_free, ds_full, dq_done, drain_bar;
+  __shared__ uint64_t q_bar, sdp_full, sc_free, ds_full, dq_done, drain_bar, drain_bar2;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, skip_sh;
 
@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
     mbar_init(&ds_full, 256);
     mbar_init(&dq_done, 1);
     mbar_init(&drain_bar, 1);
+    mbar_init(&drain_bar2, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -171,10 +172,14 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
       for (int v = nk > C::kKStages ? nk - C::kKStages : 0; v < nk; ++v)
         mbar_wait_quiet(&kfull[v % C::kKStages], (v / C::kKStages) & 1, kWaitLimitNs);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // the whole warp runs the loop; the elected lane issues every MMA and commit
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 1 issues S and dP, warp 2 issues dQ += dS K: one thread issues a
+    // tcgen05.mma about every 60 cycles, so each product gets its own issuer.
+    // Each warp runs its loop on all lanes; the elected lane issues the MMAs
+    // and commits.
     if (n_kv > 0) {
+      const bool sc_role = warp == 1;
       constexpr uint32_t idesc_s = make_idesc(128, BKV, BF16, false, false);
       constexpr uint32_t idesc_q = make_idesc(128, DQK, BF16, false, true);
       const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
@@ -183,7 +188,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
       const uint64_t kdesc_mn = make_sdesc(smem_u32(sK), C::kChunk, 1024);
       const uint64_t vdesc = make_sdesc(smem_u32(sV), 16, 1024);
       uint32_t vcnt = 0;
-      bool ok = mbar_wait_warp(&q_bar, 0, ab);
+      bool ok = sc_role ? mbar_wait_warp(&q_bar, 0, ab) : true;
       tc_fence_after();
       auto issue_scores = [&](int jt) {
 #pragma unroll
@@ -236,20 +241,25 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
         }
         __syncwarp();
       };
-      if (ok) issue_scores(0);
-      for (int jt = 0; jt < n_kv && ok; ++jt) {
-        if (jt + 1 < n_kv) {
-          if (!mbar_wait_warp(&sc_free, jt & 1u, ab)) break;
-          issue_scores(jt + 1);
-          if (!ok) break;
+      if (sc_role) {
+        for (int jt = 0; jt < n_kv && ok; ++jt) {
+          // S/dP of tile jt overwrite those of jt-1: the softmax must hold them
+          if (jt > 0 && !mbar_wait_warp(&sc_free, (jt - 1) & 1u, ab)) break;
+          issue_scores(jt);
         }
-        if (!mbar_wait_warp(&ds_full, jt & 1u, ab)) break;
-        tc_fence_after();
-        issue_dq(jt);
+      } else {
+        for (int jt = 0; jt < n_kv && ok; ++jt) {
+          if (!mbar_wait_warp(&ds_full, jt & 1u, ab)) break;
+          // the K stage of tile jt: loaded (its S MMAs ran), released below
+          if (!mbar_wait_warp(&kfull[jt % C::kKStages], (jt / C::kKStages) & 1, ab)) break;
+          tc_fence_after();
+          issue_dq(jt);
+        }
       }
+      uint64_t* drain = sc_role ? &drain_bar : &drain_bar2;
       if (elect_sync()) {
-        mma_commit(&drain_bar);
-        mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+        mma_commit(drain);
+        mbar_wait_quiet(drain, 0, kWaitLimitNs);
       }
       __syncwarp();
     }
