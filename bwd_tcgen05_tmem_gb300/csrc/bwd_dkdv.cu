@@ -18,7 +18,8 @@
 // 512 TMEM columns next to the score tiles).
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer, warp 2 loads LSE_i / D_i into shared memory, warps 4..11 two
+// score-MMA issuer, warp 2 loads LSE_i / D_i into shared memory, warp 3
+// accumulate-MMA issuer, warps 4..11 two
 // softmax warpgroups splitting the BQ query columns.  The producer and issuer
 // warps run their loops on all 32 lanes and issue each copy, MMA and commit
 // from an elect.sync lane.
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(384, 1)
   constexpr int kDOff = C::kQStaged ? C::kQCh * C::kChunk : 0;
 
   __shared__ uint64_t sfull[C::kStages], sempty[C::kStages], rfull[C::kRing], rempty[C::kRing];
-  __shared__ uint64_t kv_bar, sdp_full, sc_free, pds_full, acc_done, drain_bar;
+  __shared__ uint64_t kv_bar, sdp_full, sc_free, pds_full, acc_done, drain_bar, drain_bar2;
   __shared__ uint64_t ld_full[2], ld_empty[2];
   __shared__ __align__(16) float s_lse2[2][BQ];
   __shared__ __align__(16) float s_d[2][C::kDK ? BQ : 4];
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&pds_full, 256);
     mbar_init(&acc_done, 1);
     mbar_init(&drain_bar, 1);
+    mbar_init(&drain_bar2, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ld_full[s], 32);
       mbar_init(&ld_empty[s], 256);
@@ -219,10 +221,14 @@ __global__ void __launch_bounds__(384, 1)
       for (int v = ns > C::kStages ? ns - C::kStages : 0; v < ns; ++v)
         mbar_wait_quiet(&sfull[v % C::kStages], (v / C::kStages) & 1, kWaitLimitNs);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // the whole warp runs the loop; the elected lane issues every MMA and commit
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 1 issues the score MMAs (S^T, dP^T), warp 3 the accumulate MMAs
+    // (dV, dK): one thread issues a tcgen05.mma about every 60 cycles, so each
+    // gets its own issuer.  Each warp runs its loop on all lanes; the elected
+    // lane issues the MMAs and commits.
     if (n_it > 0) {
+      const bool sc_role = warp == 1;
       constexpr uint32_t idesc_s = make_idesc(128, BQ, BF16, false, false);
       constexpr uint32_t idesc_v = make_idesc(128, DV, BF16, false, true);
       constexpr uint32_t idesc_k = make_idesc(128, DQK, BF16, false, true);
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t stdesc_mn = make_sdesc(smem_u32(sStage), C::kChunk, 1024);  // MN-major view
       const uint64_t rdesc = make_sdesc(smem_u32(sRing), 16, 1024);
       uint32_t rcnt = 0;
-      bool ok = mbar_wait_warp(&kv_bar, 0, ab);
+      bool ok = sc_role ? mbar_wait_warp(&kv_bar, 0, ab) : true;
       tc_fence_after();
       // ring chunks are consumed one by one in load order and released as soon
       // as their score MMAs complete; the stage is held until issue_acc
@@ -337,20 +343,23 @@ __global__ void __launch_bounds__(384, 1)
         }
         __syncwarp();
       };
-      if (ok) issue_scores(0);
-      for (int it = 0; it < n_it && ok; ++it) {
-        if (it + 1 < n_it) {
-          if (!mbar_wait_warp(&sc_free, it & 1u, ab)) break;
-          issue_scores(it + 1);
-          if (!ok) break;
+      if (sc_role) {
+        for (int it = 0; it < n_it && ok; ++it) {
+          // S^T/dP^T of tile it overwrite those of it-1: the softmax must hold them
+          if (it > 0 && !mbar_wait_warp(&sc_free, (it - 1) & 1u, ab)) break;
+          issue_scores(it);
         }
-        if (!mbar_wait_warp(&pds_full, it & 1u, ab)) break;
-        tc_fence_after();
-        issue_acc(it);
+      } else {
+        for (int it = 0; it < n_it && ok; ++it) {
+          if (!mbar_wait_warp(&pds_full, it & 1u, ab)) break;
+          tc_fence_after();
+          issue_acc(it);
+        }
       }
+      uint64_t* drain = sc_role ? &drain_bar : &drain_bar2;
       if (elect_sync()) {
-        mma_commit(&drain_bar);
-        mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+        mma_commit(drain);
+        mbar_wait_quiet(drain, 0, kWaitLimitNs);
       }
       __syncwarp();
     }
