@@ -16,6 +16,9 @@ description and review notes; PR #3699 for keyless rows):
   key sets, as a context-parallel ring uses it.
 * ``naive``: the unfused reduced-precision implementation whose error against
   ``fwd``/``bwd`` is the accuracy floor of the 2x criterion.
+* ``bwd_kv`` / ``naive_kv``: ``bwd``'s and ``naive``'s dK, dV restricted to
+  selected key rows (every query row that sees one still gets its complete
+  forward), for checking deep accumulations of full-size problems.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against things other
 than itself: torch's float64 attention and autograd (library routines), central
@@ -81,6 +84,12 @@ def _load():
         lib.oracle_naive.argtypes = [ci, i32p, i32p, ci, ci, ci, ci, fp, fp, fp, fp,
                                      ci, ci, ci, ci, cd, ci, fp, fp, fp, fp, fp, ci]
         lib.oracle_naive.restype = ci
+        lib.oracle_bwd_kv.argtypes = [ci, i32p, i32p, ci, ci, ci, ci, dp, dp, dp, dp,
+                                      ci, ci, ci, ci, cd, u8p, u8p, dp, dp, ci]
+        lib.oracle_bwd_kv.restype = ci
+        lib.oracle_naive_kv.argtypes = [ci, i32p, i32p, ci, ci, ci, ci, fp, fp, fp, fp,
+                                        ci, ci, ci, ci, cd, ci, u8p, u8p, fp, fp, ci]
+        lib.oracle_naive_kv.restype = ci
         _lib = lib
         return lib
 
@@ -218,6 +227,73 @@ def naive(q, k, v, cu_q, cu_k, *, scale, dtype="bf16", dout=None, causal=True,
     if dout is None:
         return o, lse
     return o, lse, dq, dk, dvv
+
+
+def _key_sel(key_rows, tk):
+    sel = np.zeros(tk, np.uint8)
+    sel[np.asarray(list(key_rows), dtype=np.int64)] = 1
+    return sel
+
+
+def _group_sel(groups, hkv):
+    if groups is None:
+        return None
+    sel = np.zeros(hkv, np.uint8)
+    sel[list(groups)] = 1
+    return sel
+
+
+def bwd_kv(q, k, v, dout, cu_q, cu_k, *, scale, key_rows, causal=True, bottom_right=False,
+           window=(-1, -1), groups=None, nthreads=None):
+    """Exact dK, dV (float64) of the key rows ``key_rows`` (global rows of the
+    packed K) and, optionally, only the key/value heads ``groups``; the other
+    entries of the returned arrays are 0.  Same definition as ``bwd``."""
+    lib = _load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    cu_q, cu_k = _cu(cu_q), _cu(cu_k)
+    tq, hq, dqk = q.shape
+    tk, hkv, dv = v.shape
+    dk = np.zeros((tk, hkv, dqk))
+    dvv = np.zeros((tk, hkv, dv))
+    ks = _key_sel(key_rows, tk)
+    gs = _group_sel(groups, hkv)
+    rc = lib.oracle_bwd_kv(len(cu_q) - 1, _ptr(cu_q, ctypes.c_int32), _ptr(cu_k, ctypes.c_int32),
+                           hq, hkv, dqk, dv, _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                           _ptr(v, ctypes.c_double), _ptr(dout, ctypes.c_double), int(causal),
+                           int(bottom_right), int(window[0]), int(window[1]), float(scale),
+                           _ptr(ks, ctypes.c_uint8),
+                           None if gs is None else _ptr(gs, ctypes.c_uint8),
+                           _ptr(dk, ctypes.c_double), _ptr(dvv, ctypes.c_double),
+                           _nthreads(nthreads))
+    _check(rc, "bwd_kv")
+    return dk, dvv
+
+
+def naive_kv(q, k, v, dout, cu_q, cu_k, *, scale, key_rows, dtype="bf16", causal=True,
+             bottom_right=False, window=(-1, -1), groups=None, nthreads=None):
+    """The naive implementation's dK, dV (float32) of the key rows ``key_rows``
+    (and key/value heads ``groups``); other entries are 0.  Same arithmetic as
+    ``naive`` except the order of the FP32 sums over query rows."""
+    lib = _load()
+    code = _DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    cu_q, cu_k = _cu(cu_q), _cu(cu_k)
+    tq, hq, dqk = q.shape
+    tk, hkv, dv = v.shape
+    dk = np.zeros((tk, hkv, dqk), np.float32)
+    dvv = np.zeros((tk, hkv, dv), np.float32)
+    ks = _key_sel(key_rows, tk)
+    gs = _group_sel(groups, hkv)
+    fptr = lambda a: _ptr(a, ctypes.c_float)  # noqa: E731
+    rc = lib.oracle_naive_kv(len(cu_q) - 1, _ptr(cu_q, ctypes.c_int32),
+                             _ptr(cu_k, ctypes.c_int32), hq, hkv, dqk, dv, fptr(q), fptr(k),
+                             fptr(v), fptr(dout), int(causal), int(bottom_right),
+                             int(window[0]), int(window[1]), float(scale), code,
+                             _ptr(ks, ctypes.c_uint8),
+                             None if gs is None else _ptr(gs, ctypes.c_uint8),
+                             fptr(dk), fptr(dvv), _nthreads(nthreads))
+    _check(rc, "naive_kv")
+    return dk, dvv
 
 
 def dense_cu(batch, seqlen):

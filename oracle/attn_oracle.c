@@ -349,6 +349,50 @@ typedef struct {
     int do_bwd;
 } naive_ctx_t;
 
+/* Forward of one query row of the naive implementation: rounded scores, an
+ * FP32 softmax rounded to T (p[j] = 0 for masked keys), O = rnd(P V).  Writes
+ * p[0..Lk), o_row[0..dv) and *lse_out (-inf for a row with no visible key). */
+static void naive_fwd_row(const ocfg_t *c, int dt, const float *q, const float *k,
+                          const float *v, long b, int h, long i, float *p, float *acc,
+                          float *o_row, float *lse_out)
+{
+    int g = h / (c->hq / c->hkv);
+    long q0 = c->cu_q[b], k0 = c->cu_k[b];
+    long Lq = c->cu_q[b + 1] - q0, Lk = c->cu_k[b + 1] - k0;
+    const float *qi = q + ((q0 + i) * c->hq + h) * (long)c->dqk;
+    float m = -INFINITY;
+    for (long j = 0; j < Lk; ++j) {
+        if (!visible(c, i, j, Lq, Lk)) { p[j] = -INFINITY; continue; }
+        const float *kj = k + ((k0 + j) * c->hkv + g) * (long)c->dqk;
+        float a = 0.0f;
+        for (int t = 0; t < c->dqk; ++t) a += qi[t] * kj[t];
+        float sv = rnd_t(rnd_t(a, dt) * (float)c->scale, dt);
+        p[j] = sv;
+        if (sv > m) m = sv;
+    }
+    for (int t = 0; t < c->dv; ++t) o_row[t] = 0.0f;
+    if (m == -INFINITY) {
+        *lse_out = -INFINITY;
+        for (long j = 0; j < Lk; ++j) p[j] = 0.0f;
+        return;
+    }
+    float l = 0.0f;
+    for (long j = 0; j < Lk; ++j) {
+        float e = (p[j] == -INFINITY) ? 0.0f : expf(p[j] - m);
+        p[j] = e;
+        l += e;
+    }
+    *lse_out = m + logf(l);
+    for (long j = 0; j < Lk; ++j) p[j] = rnd_t(p[j] / l, dt);
+    for (int t = 0; t < c->dv; ++t) acc[t] = 0.0f;
+    for (long j = 0; j < Lk; ++j) {
+        if (p[j] == 0.0f) continue;
+        const float *vj = v + ((k0 + j) * c->hkv + g) * (long)c->dv;
+        for (int t = 0; t < c->dv; ++t) acc[t] += p[j] * vj[t];
+    }
+    for (int t = 0; t < c->dv; ++t) o_row[t] = rnd_t(acc[t], dt);
+}
+
 static void naive_item(long item, void *vctx)
 {
     naive_ctx_t *x = (naive_ctx_t *)vctx;
@@ -365,38 +409,9 @@ static void naive_item(long item, void *vctx)
     float *acc = (float *)malloc(sizeof(float) * (c->dqk > c->dv ? c->dqk : c->dv));
     for (long i = 0; i < Lq; ++i) {
         const float *qi = x->q + ((q0 + i) * c->hq + h) * (long)c->dqk;
-        float m = -INFINITY;
-        for (long j = 0; j < Lk; ++j) {
-            if (!visible(c, i, j, Lq, Lk)) { p[j] = -INFINITY; continue; }
-            const float *kj = x->k + ((k0 + j) * c->hkv + g) * (long)c->dqk;
-            float a = 0.0f;
-            for (int t = 0; t < c->dqk; ++t) a += qi[t] * kj[t];
-            float sv = rnd_t(rnd_t(a, dt) * (float)c->scale, dt);
-            p[j] = sv;
-            if (sv > m) m = sv;
-        }
         float *oi = x->o + ((q0 + i) * c->hq + h) * (long)c->dv;
-        for (int t = 0; t < c->dv; ++t) oi[t] = 0.0f;
-        if (m == -INFINITY) {
-            x->lse[(long)h * Tq + q0 + i] = -INFINITY;
-            for (long j = 0; j < Lk; ++j) p[j] = 0.0f;
-        } else {
-            float l = 0.0f;
-            for (long j = 0; j < Lk; ++j) {
-                float e = (p[j] == -INFINITY) ? 0.0f : expf(p[j] - m);
-                p[j] = e;
-                l += e;
-            }
-            x->lse[(long)h * Tq + q0 + i] = m + logf(l);
-            for (long j = 0; j < Lk; ++j) p[j] = rnd_t(p[j] / l, dt);
-            for (int t = 0; t < c->dv; ++t) acc[t] = 0.0f;
-            for (long j = 0; j < Lk; ++j) {
-                if (p[j] == 0.0f) continue;
-                const float *vj = x->v + ((k0 + j) * c->hkv + g) * (long)c->dv;
-                for (int t = 0; t < c->dv; ++t) acc[t] += p[j] * vj[t];
-            }
-            for (int t = 0; t < c->dv; ++t) oi[t] = rnd_t(acc[t], dt);
-        }
+        naive_fwd_row(c, dt, x->q, x->k, x->v, b, h, i, p, acc, oi,
+                      &x->lse[(long)h * Tq + q0 + i]);
         if (!x->do_bwd) continue;
         const float *doi = x->dout + ((q0 + i) * c->hq + h) * (long)c->dv;
         float D = 0.0f;
@@ -478,6 +493,245 @@ int oracle_naive(int nseq, const int32_t *cu_q, const int32_t *cu_k, int hq, int
         free(dv_h);
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* dK / dV of selected key rows only, exact (FP64) and naive.  The same       */
+/* definitions as oracle_bwd and oracle_naive above, evaluated only for the  */
+/* keys j of sequence b with key_sel[cu_k[b] + j] != 0; the other rows of    */
+/* dk / dv are left as they are.  Every query row that sees a selected key   */
+/* still needs its own complete forward (LSE, O and so D), so the cost is    */
+/* one forward per such row.  The rows are split into work items of          */
+/* (sequence, key/value head, block of query rows); each item sums its rows  */
+/* into its own partial and the partials are added in item order at the end, */
+/* so the result does not depend on the number of threads.                   */
+
+enum { KV_ROWS = 256 };  /* query rows per work item */
+
+typedef struct {
+    const ocfg_t *c;
+    int naive, dtype;
+    const double *q, *k, *v, *dout;     /* exact: FP64 inputs */
+    const float *fq, *fk, *fv, *fdout;  /* naive: T-representable floats */
+    const long *sel;      /* selected keys: global key rows, grouped by sequence */
+    const long *sel_lo;   /* [nseq + 1]: sequence b's entries are [sel_lo[b], sel_lo[b+1]) */
+    long n_sel;
+    const long *it_b, *it_i0;
+    const int *it_g;
+    double *pdk, *pdv;    /* exact partials [item][n_sel][d]          */
+    float *fdk, *fdv;     /* naive partials [item][grp][n_sel][d]     */
+} kv_ctx_t;
+
+static void kv_item(long item, void *vctx)
+{
+    kv_ctx_t *x = (kv_ctx_t *)vctx;
+    const ocfg_t *c = x->c;
+    long b = x->it_b[item], i0 = x->it_i0[item];
+    int g = x->it_g[item];
+    int grp = c->hq / c->hkv;
+    long q0 = c->cu_q[b], k0 = c->cu_k[b];
+    long Lq = c->cu_q[b + 1] - q0, Lk = c->cu_k[b + 1] - k0;
+    long i1 = i0 + KV_ROWS < Lq ? i0 + KV_ROWS : Lq;
+    long s0 = x->sel_lo[b], s1 = x->sel_lo[b + 1];
+    long nd = c->dqk > c->dv ? c->dqk : c->dv;
+    double *s = (double *)malloc(sizeof(double) * (Lk > 0 ? Lk : 1));
+    double *orow = (double *)malloc(sizeof(double) * c->dv);
+    float *p = (float *)malloc(sizeof(float) * (Lk > 0 ? Lk : 1));
+    float *acc = (float *)malloc(sizeof(float) * nd);
+    float *fo = (float *)malloc(sizeof(float) * c->dv);
+    for (int hh = 0; hh < grp; ++hh) {
+        int h = g * grp + hh;
+        for (long i = i0; i < i1; ++i) {
+            int any = 0;  /* does row i see a selected key? */
+            for (long e = s0; e < s1 && !any; ++e)
+                any = visible(c, i, x->sel[e] - k0, Lq, Lk);
+            if (!any) continue;
+            if (!x->naive) {
+                double lse;
+                fwd_row(c, x->q, x->k, x->v, b, h, i, s, orow, &lse);
+                if (lse == -INFINITY) continue;
+                const double *qi = x->q + ((q0 + i) * c->hq + h) * (long)c->dqk;
+                const double *doi = x->dout + ((q0 + i) * c->hq + h) * (long)c->dv;
+                double D = 0.0;
+                for (int t = 0; t < c->dv; ++t) D += doi[t] * orow[t];
+                for (long e = s0; e < s1; ++e) {
+                    long j = x->sel[e] - k0;
+                    if (s[j] == -INFINITY) continue;
+                    double pj = exp(s[j] - lse);
+                    const double *vj = x->v + ((k0 + j) * c->hkv + g) * (long)c->dv;
+                    double dp = 0.0;
+                    for (int t = 0; t < c->dv; ++t) dp += doi[t] * vj[t];
+                    double ds = pj * (dp - D);
+                    double *dkj = x->pdk + ((size_t)item * x->n_sel + e) * c->dqk;
+                    double *dvj = x->pdv + ((size_t)item * x->n_sel + e) * c->dv;
+                    for (int t = 0; t < c->dqk; ++t) dkj[t] += c->scale * ds * qi[t];
+                    for (int t = 0; t < c->dv; ++t) dvj[t] += pj * doi[t];
+                }
+            } else {
+                int dt = x->dtype;
+                float lse;
+                naive_fwd_row(c, dt, x->fq, x->fk, x->fv, b, h, i, p, acc, fo, &lse);
+                const float *qi = x->fq + ((q0 + i) * c->hq + h) * (long)c->dqk;
+                const float *doi = x->fdout + ((q0 + i) * c->hq + h) * (long)c->dv;
+                float D = 0.0f;
+                for (int t = 0; t < c->dv; ++t) D += doi[t] * fo[t];
+                D = rnd_t(D, dt);
+                for (long e = s0; e < s1; ++e) {
+                    long j = x->sel[e] - k0;
+                    if (p[j] == 0.0f) continue;
+                    const float *vj = x->fv + ((k0 + j) * c->hkv + g) * (long)c->dv;
+                    float a = 0.0f;
+                    for (int t = 0; t < c->dv; ++t) a += doi[t] * vj[t];
+                    float dpv = rnd_t(a, dt);
+                    float ds = rnd_t(p[j] * (dpv - D), dt);
+                    float *dkj = x->fdk + (((size_t)item * grp + hh) * x->n_sel + e) * c->dqk;
+                    float *dvj = x->fdv + (((size_t)item * grp + hh) * x->n_sel + e) * c->dv;
+                    if (ds != 0.0f)
+                        for (int t = 0; t < c->dqk; ++t) dkj[t] += ds * qi[t];
+                    for (int t = 0; t < c->dv; ++t) dvj[t] += p[j] * doi[t];
+                }
+            }
+        }
+    }
+    free(fo);
+    free(acc);
+    free(p);
+    free(orow);
+    free(s);
+}
+
+static int kv_run(const ocfg_t *c, int naive, int dtype, const void *q, const void *k,
+                  const void *v, const void *dout, const uint8_t *key_sel,
+                  const uint8_t *group_sel, void *dk, void *dv_out, int nthreads)
+{
+    int rc = check_cfg(c);
+    if (rc) return rc;
+    long Tk = c->cu_k[c->nseq];
+    int grp = c->hq / c->hkv;
+    long *sel_lo = (long *)calloc((size_t)c->nseq + 1, sizeof(long));
+    long n_sel = 0;
+    for (long j = 0; j < Tk; ++j) n_sel += key_sel[j] != 0;
+    long *sel = (long *)malloc(sizeof(long) * (n_sel > 0 ? n_sel : 1));
+    long n_items = 0, e = 0;
+    for (int b = 0; b < c->nseq; ++b) {
+        sel_lo[b] = e;
+        for (long j = c->cu_k[b]; j < c->cu_k[b + 1]; ++j)
+            if (key_sel[j]) sel[e++] = j;
+        long Lq = c->cu_q[b + 1] - c->cu_q[b];
+        for (int g = 0; g < c->hkv; ++g)
+            if (!group_sel || group_sel[g]) n_items += (Lq + KV_ROWS - 1) / KV_ROWS;
+    }
+    sel_lo[c->nseq] = e;
+    long *it_b = (long *)malloc(sizeof(long) * (n_items > 0 ? n_items : 1));
+    long *it_i0 = (long *)malloc(sizeof(long) * (n_items > 0 ? n_items : 1));
+    int *it_g = (int *)malloc(sizeof(int) * (n_items > 0 ? n_items : 1));
+    long it = 0;
+    for (int b = 0; b < c->nseq; ++b) {
+        long Lq = c->cu_q[b + 1] - c->cu_q[b];
+        for (int g = 0; g < c->hkv; ++g) {
+            if (group_sel && !group_sel[g]) continue;
+            for (long i0 = 0; i0 < Lq; i0 += KV_ROWS) {
+                it_b[it] = b;
+                it_g[it] = g;
+                it_i0[it] = i0;
+                ++it;
+            }
+        }
+    }
+    size_t np = (size_t)(n_items > 0 ? n_items : 1) * (size_t)(n_sel > 0 ? n_sel : 1);
+    kv_ctx_t x;
+    memset(&x, 0, sizeof(x));
+    x.c = c; x.naive = naive; x.dtype = dtype;
+    x.sel = sel; x.sel_lo = sel_lo; x.n_sel = n_sel;
+    x.it_b = it_b; x.it_i0 = it_i0; x.it_g = it_g;
+    if (!naive) {
+        x.q = (const double *)q; x.k = (const double *)k; x.v = (const double *)v;
+        x.dout = (const double *)dout;
+        x.pdk = (double *)calloc(np * c->dqk, sizeof(double));
+        x.pdv = (double *)calloc(np * c->dv, sizeof(double));
+        if (!x.pdk || !x.pdv) rc = -3;
+    } else {
+        x.fq = (const float *)q; x.fk = (const float *)k; x.fv = (const float *)v;
+        x.fdout = (const float *)dout;
+        x.fdk = (float *)calloc(np * grp * c->dqk, sizeof(float));
+        x.fdv = (float *)calloc(np * grp * c->dv, sizeof(float));
+        if (!x.fdk || !x.fdv) rc = -3;
+    }
+    if (!rc) run_pool(n_items, nthreads, kv_item, &x);
+    /* add the partials of each (selected key, kv head) in item order */
+    for (long e2 = 0; e2 < n_sel && !rc; ++e2) {
+        long j = sel[e2];
+        int b = 0;
+        while (c->cu_k[b + 1] <= j) ++b;
+        for (int g = 0; g < c->hkv; ++g) {
+            if (group_sel && !group_sel[g]) continue;
+            if (!naive) {
+                double *dkj = (double *)dk + (j * c->hkv + g) * (long)c->dqk;
+                double *dvj = (double *)dv_out + (j * c->hkv + g) * (long)c->dv;
+                for (int t = 0; t < c->dqk; ++t) dkj[t] = 0.0;
+                for (int t = 0; t < c->dv; ++t) dvj[t] = 0.0;
+                for (long m = 0; m < n_items; ++m) {
+                    if (it_b[m] != b || it_g[m] != g) continue;
+                    const double *pk = x.pdk + ((size_t)m * n_sel + e2) * c->dqk;
+                    const double *pv = x.pdv + ((size_t)m * n_sel + e2) * c->dv;
+                    for (int t = 0; t < c->dqk; ++t) dkj[t] += pk[t];
+                    for (int t = 0; t < c->dv; ++t) dvj[t] += pv[t];
+                }
+            } else {
+                /* as oracle_naive: per query head FP32 sums rounded, then summed */
+                float *dkj = (float *)dk + (j * c->hkv + g) * (long)c->dqk;
+                float *dvj = (float *)dv_out + (j * c->hkv + g) * (long)c->dv;
+                for (int t = 0; t < c->dqk; ++t) {
+                    float sum = 0.0f;
+                    for (int hh = 0; hh < grp; ++hh) {
+                        float a = 0.0f;
+                        for (long m = 0; m < n_items; ++m)
+                            if (it_b[m] == b && it_g[m] == g)
+                                a += x.fdk[(((size_t)m * grp + hh) * n_sel + e2) * c->dqk + t];
+                        sum += rnd_t(rnd_t(a, dtype) * (float)c->scale, dtype);
+                    }
+                    dkj[t] = rnd_t(sum, dtype);
+                }
+                for (int t = 0; t < c->dv; ++t) {
+                    float sum = 0.0f;
+                    for (int hh = 0; hh < grp; ++hh) {
+                        float a = 0.0f;
+                        for (long m = 0; m < n_items; ++m)
+                            if (it_b[m] == b && it_g[m] == g)
+                                a += x.fdv[(((size_t)m * grp + hh) * n_sel + e2) * c->dv + t];
+                        sum += rnd_t(a, dtype);
+                    }
+                    dvj[t] = rnd_t(sum, dtype);
+                }
+            }
+        }
+    }
+    free(x.pdk); free(x.pdv); free(x.fdk); free(x.fdv);
+    free(it_g); free(it_i0); free(it_b); free(sel); free(sel_lo);
+    return rc;
+}
+
+/* Exact dK / dV (FP64) of the selected key rows; dk [Tk][hkv][dqk],
+ * dv [Tk][hkv][dv], only the selected rows (and selected groups) written. */
+int oracle_bwd_kv(int nseq, const int32_t *cu_q, const int32_t *cu_k, int hq, int hkv,
+                  int dqk, int dv, const double *q, const double *k, const double *v,
+                  const double *dout, int causal, int bottom_right, int wl, int wr,
+                  double scale, const uint8_t *key_sel, const uint8_t *group_sel,
+                  double *dk, double *dv_out, int nthreads)
+{
+    ocfg_t c = {nseq, cu_q, cu_k, hq, hkv, dqk, dv, causal, bottom_right, wl, wr, scale};
+    return kv_run(&c, 0, 0, q, k, v, dout, key_sel, group_sel, dk, dv_out, nthreads);
+}
+
+/* The naive implementation's dK / dV of the selected key rows (FP32). */
+int oracle_naive_kv(int nseq, const int32_t *cu_q, const int32_t *cu_k, int hq, int hkv,
+                    int dqk, int dv, const float *q, const float *k, const float *v,
+                    const float *dout, int causal, int bottom_right, int wl, int wr,
+                    double scale, int dtype, const uint8_t *key_sel, const uint8_t *group_sel,
+                    float *dk, float *dv_out, int nthreads)
+{
+    ocfg_t c = {nseq, cu_q, cu_k, hq, hkv, dqk, dv, causal, bottom_right, wl, wr, scale};
+    return kv_run(&c, 1, dtype, q, k, v, dout, key_sel, group_sel, dk, dv_out, nthreads);
 }
 
 /* Round float values to T in place (used to make T-representable inputs). */

@@ -498,3 +498,101 @@ def test_ring_pieces_cover_every_causal_pair_once(ncp):
                 assert qg.min() > kg.max()
     expect = np.tril(np.ones((s, s), dtype=int))
     np.testing.assert_array_equal(count, expect)
+
+
+# ---------------------------------------------------------------- subsets
+# The head / group / key-row selections the full-size GPU tests use to keep the
+# oracle's cost down: each must give torch's float64 autograd values on what it
+# selects and leave the rest untouched.
+
+
+def test_head_and_group_selection_match_torch():
+    s, hq, hkv, d = 23, 6, 3, 8
+    q, k, v, do = rand(s, hq, d), rand(s, hkv, d), rand(s, hkv, d), rand(s, hq, d)
+    kw = dict(scale=0.4, causal=True, window=(9, -1))
+    o_t, lse_t, dq_t, dk_t, dv_t = torch_ref(q, k, v, dout=do, **kw)
+    o, lse = oracle.fwd(q, k, v, [0, s], [0, s], heads=[1, 4], **kw)
+    np.testing.assert_allclose(o[:, [1, 4]], o_t[:, [1, 4]], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[[1, 4]], lse_t[[1, 4]], rtol=0, atol=1e-12)
+    assert np.all(o[:, [0, 2, 3, 5]] == 0) and np.all(np.isnan(lse[[0, 2, 3, 5]]))
+    dq, dk, dvv = oracle.bwd(q, k, v, do, [0, s], [0, s], groups=[2], **kw)
+    np.testing.assert_allclose(dq[:, 4:6], dq_t[:, 4:6], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk[:, 2], dk_t[:, 2], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dvv[:, 2], dv_t[:, 2], rtol=0, atol=1e-11)
+    assert np.all(dq[:, :4] == 0) and np.all(dk[:, :2] == 0) and np.all(dvv[:, :2] == 0)
+
+
+KV_CASES = [
+    # (L, hq, hkv, causal, window, bottom_right (Lq != Lk))
+    (600, 2, 1, True, (-1, -1), None),
+    (600, 4, 2, True, (90, 0), None),
+    (520, 2, 2, False, (70, 40), None),
+    (300, 2, 1, True, (-1, -1), 450),
+]
+
+
+@pytest.mark.parametrize("case", KV_CASES)
+def test_bwd_kv_matches_torch_autograd(case):
+    """Selected key rows (first, middle and last blocks; several row blocks of
+    work per head) equal torch's float64 gradients; other rows stay 0."""
+    lq, hq, hkv, causal, window, lk = case
+    lk = lk or lq
+    d, dv = 12, 8
+    q, k, v, do = rand(lq, hq, d), rand(lk, hkv, d), rand(lk, hkv, dv), rand(lq, hq, dv)
+    br = lk != lq
+    kw = dict(scale=0.3, causal=causal, window=window, bottom_right=br)
+    _, _, _, dk_t, dv_t = torch_ref(q, k, v, dout=do, **kw)
+    rows = list(range(0, 5)) + list(range(lk // 2, lk // 2 + 7)) + [lk - 1]
+    dk, dvv = oracle.bwd_kv(q, k, v, do, [0, lq], [0, lk], key_rows=rows, **kw)
+    np.testing.assert_allclose(dk[rows], dk_t[rows], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dvv[rows], dv_t[rows], rtol=0, atol=1e-11)
+    other = np.setdiff1d(np.arange(lk), rows)
+    assert np.all(dk[other] == 0) and np.all(dvv[other] == 0)
+    # a group selection computes only that kv head
+    dk1, _ = oracle.bwd_kv(q, k, v, do, [0, lq], [0, lk], key_rows=rows, groups=[hkv - 1], **kw)
+    np.testing.assert_allclose(dk1[rows, hkv - 1], dk_t[rows, hkv - 1], rtol=0, atol=1e-11)
+    if hkv > 1:
+        assert np.all(dk1[:, 0] == 0)
+
+
+def test_bwd_kv_thd_equals_per_document_torch():
+    lens = [0, 300, 1, 280]
+    cu = np.cumsum([0] + lens)
+    t, hq, hkv, d = cu[-1], 2, 1, 8
+    q, k, v, do = rand(t, hq, d), rand(t, hkv, d), rand(t, hkv, d), rand(t, hq, d)
+    rows = [1, 2, 299, 300, 301, 302, 580]
+    dk, dvv = oracle.bwd_kv(q, k, v, do, cu, cu, key_rows=rows, scale=0.35, causal=True)
+    for b in range(len(lens)):
+        a, e = cu[b], cu[b + 1]
+        if e == a:
+            continue
+        _, _, _, dk_t, dv_t = torch_ref(q[a:e], k[a:e], v[a:e], dout=do[a:e], scale=0.35,
+                                        causal=True)
+        sel = [r - a for r in rows if a <= r < e]
+        np.testing.assert_allclose(dk[a:e][sel], dk_t[sel], rtol=0, atol=1e-11)
+        np.testing.assert_allclose(dvv[a:e][sel], dv_t[sel], rtol=0, atol=1e-11)
+
+
+def test_naive_kv_without_rounding_matches_exact_and_floor_works():
+    """No rounding (FP32 type): naive_kv equals the exact subset to FP32
+    accuracy.  With BF16 its floor accepts the rounded exact dK/dV of the
+    selected rows and rejects a 1 % softmax-scale error (TransformerEngine
+    PR #3527's mutation test, on a key subset)."""
+    s, hq, hkv, d = 700, 2, 1, 16
+    q, k, v, do = (_bf16(rand(s, h, d)) for h in (hq, hkv, hkv, hq))
+    rows = list(range(0, 128)) + list(range(400, 420))
+    kw = dict(scale=0.25, causal=True, key_rows=rows)
+    ek, ev = oracle.bwd_kv(q, k, v, do, [0, s], [0, s], **kw)
+    fk, fv = oracle.naive_kv(q, k, v, do, [0, s], [0, s], dtype="fp32", **kw)
+    np.testing.assert_allclose(fk[rows], ek[rows], atol=5e-5)
+    np.testing.assert_allclose(fv[rows], ev[rows], atol=5e-5)
+    nk, nv = oracle.naive_kv(q, k, v, do, [0, s], [0, s], dtype="bf16", **kw)
+    floors = [np.max(np.abs(nk[rows] - ek[rows])), np.max(np.abs(nv[rows] - ev[rows]))]
+    assert all(1e-5 < f < 0.1 for f in floors), floors
+    for x, e, f in ((ek, ek, floors[0]), (ev, ev, floors[1])):
+        assert np.max(np.abs(_bf16(x[rows]) - e[rows])) <= 2 * f
+    mk, mv = oracle.bwd_kv(q, k, v, do, [0, s], [0, s], scale=0.25 * 1.01, causal=True,
+                           key_rows=rows)
+    rejected = [np.max(np.abs(_bf16(m[rows]) - e[rows])) > 2 * f
+                for m, e, f in ((mk, ek, floors[0]), (mv, ev, floors[1]))]
+    assert any(rejected), rejected
