@@ -7,9 +7,15 @@ benchmark uses, on outputs the oracle can compute exactly from a sub-problem:
 * key rows [a, S) at the end of a causal sequence only receive gradient from
   query rows >= a, so their dK/dV come out exact from the query block [a, S);
 * with MHA a head is independent of the others, and with GQA a key/value head
-  together with its query heads is.
+  together with its query heads is;
+* dK/dV of any key block, including the deepest accumulations (key block 0 of
+  a causal sequence sums over every query tile of every head of its group),
+  come out exact from the oracle's key-subset backward, which runs the full
+  forward of every query row that sees a selected key.
 Every sample is gated with the 2x-naive criterion against the naive
-implementation run on the same sub-problem, and gradients by relative L2.
+implementation run on the same sub-problem (or key subset), and gradients by
+relative L2.  The GPU results come from one call at the full size, in the
+launch configuration the benchmark uses.
 """
 import math
 
@@ -64,13 +70,42 @@ def check_block(got, ref, tail_keys=None):
             rel_l2(name, got[name], ex)
 
 
+_RUNS = {}
+
+
 def run_dense(w):
+    """One full-size forward + backward of workload `w` on the GPU (cached for
+    the tests of this module; inputs and results on the CPU)."""
+    if w.name in _RUNS:
+        return _RUNS[w.name]
     inp = synth.make_inputs(w)
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
     o, lse = attn.fwd(q, k, v, causal=True, scale=w.scale, window=w.window)
     g = attn.bwd(q, k, v, o, do, lse, causal=True, scale=w.scale, window=w.window)
     torch.cuda.synchronize()
-    return inp, o.cpu(), lse.cpu(), [t.cpu() for t in g]
+    _RUNS[w.name] = (inp, o.cpu(), lse.cpu(), [t.cpu() for t in g])
+    del q, k, v, do, o, lse, g
+    torch.cuda.empty_cache()
+    return _RUNS[w.name]
+
+
+def check_key_blocks(q, k, v, do, dk, dv, key_rows, *, scale, window=(-1, -1), dtype="bf16",
+                     cu=None):
+    """dK/dV of `key_rows` against the oracle's key-subset backward and the
+    naive floor on the same subset.  q/k/v/do: CPU tensors [T, H, d] of one
+    problem (a head group, or all heads); dk/dv: the GPU's gradients, same
+    layout.  `cu`: sequence offsets (None: one sequence)."""
+    t = q.shape[0]
+    cu = [0, t] if cu is None else cu
+    qs, ks, vs, ds = (f64(x) for x in (q, k, v, do))
+    kw = dict(scale=scale, causal=True, window=window, key_rows=key_rows)
+    ek, ev = oracle.bwd_kv(qs, ks, vs, ds, cu, cu, **kw)
+    nk, nv = oracle.naive_kv(qs, ks, vs, ds, cu, cu, dtype=dtype, **kw)
+    rows = np.asarray(list(key_rows))
+    for name, got, ex, nv_ in (("dk", dk, ek, nk), ("dv", dv, ev, nv)):
+        g_ = f64(got)[rows]
+        gate(name, g_, ex[rows], np.max(np.abs(nv_[rows] - ex[rows])))
+        rel_l2(name, g_, ex[rows])
 
 
 def test_b2_h32_s4096_d192_128_two_full_heads():
@@ -164,3 +199,79 @@ def test_thd_h32_kv8_t65536_d128_sampled_documents(dtype):
             got = dict(o=o[a:b, hs], lse=lse[hs, a:b], dq=dq[a:b, hs], dk=dk[a:b, g:g + 1],
                        dv=dv[a:b, g:g + 1])
             check_block(got, ref, tail_keys=slice(0, b - a))
+
+
+# ------------------------------------------------------------------ deep dK/dV
+# Key block 0 of a causal sequence is the deepest accumulation of the dK/dV
+# kernels (every query tile of every query head of its group); a middle block
+# gets half of them.  These tests check those blocks at the full sizes.
+
+
+def test_b1_h32_s32768_d192_128_deep_key_blocks():
+    """Key blocks 0 and 96 (512 and 320 query tiles of 64 rows) and the last
+    block, heads 0 and 31, against the oracle over all 32768 query rows."""
+    w = synth.WORKLOADS["b1_h32_s32768_d192_128"]
+    inp, _, _, (_, dk, dv) = run_dense(w)
+    S = w.seqlen
+    heads = [0, w.heads_q - 1]  # MHA: each head is its own group
+    key_rows = list(range(0, 128)) + list(range(12288, 12416)) + list(range(S - 128, S))
+    sl = lambda t: t[0][:, heads]  # noqa: E731
+    check_key_blocks(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["dout"]), sl(dk), sl(dv),
+                     key_rows, scale=w.scale)
+
+
+def test_b1_h16_kv4_s16384_d512_deep_key_blocks():
+    """d512 GQA: key blocks 0, 64 and the last one of kv head 3, summed over its
+    four query heads and all their query tiles (the materialising dK/dV GEMMs)."""
+    w = synth.WORKLOADS["b1_h16_kv4_s16384_d512"]
+    inp, _, _, (_, dk, dv) = run_dense(w)
+    S = w.seqlen
+    grp = w.heads_q // w.heads_kv
+    g = w.heads_kv - 1
+    hs = slice(g * grp, (g + 1) * grp)
+    key_rows = list(range(0, 128)) + list(range(8192, 8320)) + list(range(S - 128, S))
+    check_key_blocks(inp["q"][0, :, hs], inp["k"][0, :, g:g + 1], inp["v"][0, :, g:g + 1],
+                     inp["dout"][0, :, hs], dk[0, :, g:g + 1], dv[0, :, g:g + 1], key_rows,
+                     scale=w.scale)
+
+
+def test_b1_h16_kv4_s16384_d256_window1024_deep_key_blocks():
+    """Windowed d256: interior key blocks, whose dK/dV sum over every query tile
+    the window lets see them, for all four query heads of kv heads 0 and 3."""
+    w = synth.WORKLOADS["b1_h16_kv4_s16384_d256_w1024"]
+    inp, _, _, (_, dk, dv) = run_dense(w)
+    grp = w.heads_q // w.heads_kv
+    key_rows = list(range(0, 128)) + list(range(8064, 8192)) + list(range(12000, 12128))
+    for g in (0, w.heads_kv - 1):
+        hs = slice(g * grp, (g + 1) * grp)
+        check_key_blocks(inp["q"][0, :, hs], inp["k"][0, :, g:g + 1], inp["v"][0, :, g:g + 1],
+                         inp["dout"][0, :, hs], dk[0, :, g:g + 1], dv[0, :, g:g + 1], key_rows,
+                         scale=w.scale, window=w.window)
+
+
+def test_thd_h32_kv8_t65536_d128_longest_document_deep_key_blocks():
+    """Packed THD: the first, a middle and the last key block of the longest
+    document, kv heads 0 and 7 with their query heads."""
+    w = synth.WORKLOADS["thd_h32_kv8_t65536_d128_bf16"]
+    inp = synth.make_inputs(w)
+    cu = inp["cu_seqlens"]
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
+    cud = cu.cuda()
+    kw = dict(causal=True, scale=w.scale, cu_seqlens_q=cud, cu_seqlens_k=cud,
+              max_seqlen_q=inp["max_seqlen"], max_seqlen_k=inp["max_seqlen"])
+    o, lse = attn.fwd(q, k, v, **kw)
+    _, dk, dv = attn.bwd(q, k, v, o, do, lse, **kw)
+    torch.cuda.synchronize()
+    dk, dv = dk.cpu(), dv.cpu()
+    lens = (cu[1:] - cu[:-1]).tolist()
+    doc = max(range(len(lens)), key=lambda i: lens[i])
+    a, b = int(cu[doc]), int(cu[doc + 1])
+    n = b - a
+    mid = (n // 2) // 128 * 128
+    key_rows = list(range(0, 128)) + list(range(mid, mid + 128)) + list(range(n - 128, n))
+    grp = w.heads_q // w.heads_kv
+    for g in (0, w.heads_kv - 1):
+        hs = slice(g * grp, (g + 1) * grp)
+        check_key_blocks(inp["q"][a:b, hs], inp["k"][a:b, g:g + 1], inp["v"][a:b, g:g + 1],
+                         inp["dout"][a:b, hs], dk[a:b, g:g + 1], dv[a:b, g:g + 1], key_rows,
+                         scale=w.scale)
