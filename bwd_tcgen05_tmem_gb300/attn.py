@@ -30,7 +30,10 @@ _STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
 EXPORTED = ["attn_fwd_workspace_size", "attn_bwd_workspace_size", "attn_fwd", "attn_bwd",
             "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkdv", "attn_bwd_noalloc",
             "attn_lse_merge", "attn_cp_relayout",
-            "attn_query_status", "attn_last_error", "attn_last_launch_count"]
+            "attn_query_status", "attn_last_error", "attn_last_launch_count",
+            "attn_debug_inject"]
+# attn_debug_inject kernel bits (test only)
+DEBUG_FWD, DEBUG_DQ, DEBUG_DKDV, DEBUG_SCORES = 1, 2, 4, 8
 
 
 class AttnError(RuntimeError):
@@ -103,6 +106,8 @@ def load():
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_last_launch_count.argtypes = []
         lib.attn_last_launch_count.restype = ctypes.c_int
+        lib.attn_debug_inject.argtypes = [ctypes.c_uint, ctypes.c_int, ctypes.c_uint64]
+        lib.attn_debug_inject.restype = None
         _lib = lib
         return lib
 
@@ -307,6 +312,13 @@ def lse_merge(o_parts, lse_parts, row0, nrows, rows, *, out=None, lse_out=None,
     _check(lib.attn_lse_merge(n, optrs, lptrs, r0, nr, int(rows), int(heads), int(dvd),
                               _ptr(out), _code(out.dtype), _ptr(lse_out), _stream(stream)))
     return out, lse_out
+
+
+def debug_inject(kernel_mask, drop_load, wait_limit_ns=0):
+    """TEST ONLY: arm attn_debug_inject for the next attn_fwd / attn_bwd call on
+    this thread (the first CTA of each selected kernel leaves out load
+    ``drop_load`` and waits at most ``wait_limit_ns``; 0 keeps 2 s)."""
+    load().attn_debug_inject(int(kernel_mask), int(drop_load), int(wait_limit_ns))
 
 
 def query_status(workspace, stream=None):

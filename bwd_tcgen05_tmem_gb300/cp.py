@@ -134,8 +134,19 @@ class CPRing:
         self.dv = [torch.zeros((1, rows, *v.shape[2:]), dtype=torch.float32, device=dev)
                    for _ in range(cp)]
         self.fwd_ws = [torch.empty(256, dtype=torch.uint8, device=dev) for _ in range(cp)]
-        need = max(attn.workspace_size("bwd", self.q[0], self.k[0], self.v[0]), 256)
-        self.bwd_ws = [torch.empty(need, dtype=torch.uint8, device=dev) for _ in range(cp)]
+        # one backward workspace per rank and query-row set: D (the preprocess)
+        # depends only on the query rows, so it is computed once per rank for
+        # all of its rows and once for its second chunk, and every ring step
+        # then runs only the dq and dkdv stages on the matching workspace
+        c = self.chunk
+        need = max(256, *(attn.workspace_size("bwd", self.q[0][:, q0:q0 + nq],
+                                              self.k[0][:, k0:k0 + nk], self.v[0][:, k0:k0 + nk],
+                                              causal=cz)
+                          for (q0, nq), (k0, nk), cz in (((0, 2 * c), (0, 2 * c), True),
+                                                         ((0, 2 * c), (0, c), False),
+                                                         ((c, c), (0, 2 * c), False))))
+        self.bwd_ws = [{rq: torch.empty(need, dtype=torch.uint8, device=dev)
+                        for rq in ((0, 2 * c), (c, c))} for _ in range(cp)]
         self.streams = _Streams(cp, dev)
         self.launches = 0
 
@@ -153,16 +164,30 @@ class CPRing:
                          out=self.o_part[r][i], lse=self.lse_part[r][i],
                          workspace=self.fwd_ws[r], stream=st)
                 n += attn.last_launch_count()
-            attn.lse_merge([t[0] for t in self.o_part[r]], [t[0] for t in self.lse_part[r]],
-                           [pc.q_rows[0] for pc in pcs], [pc.q_rows[1] for pc in pcs],
-                           2 * self.chunk, out=self.o[r][0], lse_out=self.lse[r][0], stream=st)
-            n += attn.last_launch_count()
+            n += self.merge(r, st)
         self.streams.join()
         self.launches = n
         return self.o, self.lse
 
+    def merge(self, r, stream=None):
+        """LSE-merge rank r's ring-step partials into its O / LSE; returns the
+        number of kernels launched."""
+        pcs = self.pieces[r]
+        attn.lse_merge([t[0] for t in self.o_part[r]], [t[0] for t in self.lse_part[r]],
+                       [pc.q_rows[0] for pc in pcs], [pc.q_rows[1] for pc in pcs],
+                       2 * self.chunk, out=self.o[r][0], lse_out=self.lse[r][0], stream=stream)
+        return attn.last_launch_count()
+
+    def merge_all(self):
+        """Every rank's merge, in order on the current stream (to time the merge
+        kernel alone)."""
+        for r in range(self.cp):
+            self.merge(r)
+
     def backward(self):
-        """Per ring step attn_bwd with the merged LSE/O and FP32 gradients.
+        """Per ring step the dq and dkdv stages of attn_bwd with the merged
+        LSE/O and FP32 gradients; D = rowsum(dO * O) of the merged O comes from
+        one preprocess per rank and query-row set.
 
         Step 0 of every rank covers all of its query rows and all of its own key
         rows, so the step-0 calls (run first) overwrite every gradient element
@@ -176,23 +201,34 @@ class CPRing:
         cp = self.cp
         done = [[None] * cp for _ in range(cp)]
         self.streams.fork()
+
+        def call(r, pc, stage, accumulate):
+            q0, nq = pc.q_rows
+            k0, nk = pc.k_rows
+            lse = self.lse[r][:, :, q0:]  # rows q0.. of the merged LSE, head stride `rows`
+            attn.bwd(self.q[r][:, q0:q0 + nq], self.k[pc.src][:, k0:k0 + nk],
+                     self.v[pc.src][:, k0:k0 + nk], self.o[r][:, q0:q0 + nq],
+                     self.do[r][:, q0:q0 + nq], lse, causal=pc.causal, scale=self.scale,
+                     dq=self.dq[r][:, q0:q0 + nq], dk=self.dk[pc.src][:, k0:k0 + nk],
+                     dv=self.dv[pc.src][:, k0:k0 + nk], grad_dtype=torch.float32,
+                     accumulate=accumulate, lse_strides=(0, rows),
+                     workspace=self.bwd_ws[r][pc.q_rows], stream=self.streams.s[r], stage=stage)
+            return attn.last_launch_count()
+
+        for r in range(cp):  # D of every query-row set the rank's steps use, once
+            seen = set()
+            for pc in self.pieces[r]:
+                if pc.q_rows not in seen:
+                    seen.add(pc.q_rows)
+                    n += call(r, pc, "preprocess", False)
         for s in range(cp):
             for r in range(cp):
                 st = self.streams.s[r]
                 if s > 0:
                     st.wait_event(done[s - 1][(r - 1) % cp])
                 pc = self.pieces[r][s]
-                q0, nq = pc.q_rows
-                k0, nk = pc.k_rows
-                lse = self.lse[r][:, :, q0:]  # rows q0.. of the merged LSE, head stride `rows`
-                attn.bwd(self.q[r][:, q0:q0 + nq], self.k[pc.src][:, k0:k0 + nk],
-                         self.v[pc.src][:, k0:k0 + nk], self.o[r][:, q0:q0 + nq],
-                         self.do[r][:, q0:q0 + nq], lse, causal=pc.causal, scale=self.scale,
-                         dq=self.dq[r][:, q0:q0 + nq], dk=self.dk[pc.src][:, k0:k0 + nk],
-                         dv=self.dv[pc.src][:, k0:k0 + nk], grad_dtype=torch.float32,
-                         accumulate=s > 0, lse_strides=(0, rows), workspace=self.bwd_ws[r],
-                         stream=st)
-                n += attn.last_launch_count()
+                n += call(r, pc, "dq", s > 0)
+                n += call(r, pc, "dkdv", s > 0)
                 done[s][r] = torch.cuda.Event()
                 done[s][r].record(st)
         self.streams.join()
@@ -253,46 +289,71 @@ class CPAllGather:
                    for _ in range(cp)]
         self.dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
         self.dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
-        self.fwd_ws = torch.empty(256, dtype=torch.uint8, device=dev)
+        self.fwd_ws = [torch.empty(256, dtype=torch.uint8, device=dev) for _ in range(cp)]
         need = max(attn.workspace_size("bwd", self.q[0][:, :self.chunk], k[:, k0:k1],
                                        v[:, k0:k1], causal=True, bottom_right=True,
                                        window=self.window)
                    for pcs in self.pieces for _, _, (k0, k1) in pcs)
-        self.bwd_ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        # one workspace per call: the calls' preprocess and dq stages overlap
+        self.bwd_ws = [[torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+                        for _ in pcs] for pcs in self.pieces]
+        self.streams = _Streams(cp, dev)
         self.launches = 0
 
     def forward(self):
-        """One call per local query chunk, in order on the current stream (the
-        calls are large enough to fill the GPU one at a time)."""
+        """One call per local query chunk; rank r runs on stream r, so the
+        ranks' calls overlap (each writes only its own O and LSE rows)."""
         n = 0
+        self.streams.fork()
         for r, pcs in enumerate(self.pieces):
             for _, (q0, nq), (k0, k1) in pcs:
                 attn.fwd(self.q[r][:, q0:q0 + nq], self.k_full[:, k0:k1], self.v_full[:, k0:k1],
                          causal=True, bottom_right=True, window=self.window, scale=self.scale,
                          out=self.o[r][:, q0:q0 + nq], lse=self.lse[r][:, :, q0:q0 + nq],
-                         lse_strides=(0, 2 * self.chunk), workspace=self.fwd_ws)
+                         lse_strides=(0, 2 * self.chunk), workspace=self.fwd_ws[r],
+                         stream=self.streams.s[r])
                 n += attn.last_launch_count()
+        self.streams.join()
         self.launches = n
         return self.o, self.lse
 
     def backward(self):
         """dQ per chunk; dK/dV summed over every chunk's trimmed range.  The
         library's accumulate flag covers all three gradients, so the FP32
-        buffers start from zero.  Every call adds into the shared dK/dV, so
-        the calls run in order on the current stream."""
+        buffers start from zero.  Rank r runs on stream r: the preprocess and
+        dq stages of all calls overlap; every dkdv stage adds into the shared
+        dK/dV, so those run one after another (each waits for the previous
+        one through an event)."""
         for t in (*self.dq, self.dk, self.dv):
             t.zero_()
         n = 0
         rows = 2 * self.chunk
+        self.streams.fork()
+        prev = None
         for r, pcs in enumerate(self.pieces):
-            for _, (q0, nq), (k0, k1) in pcs:
+            st = self.streams.s[r]
+
+            def call(i, stage):
+                _, (q0, nq), (k0, k1) = pcs[i]
                 attn.bwd(self.q[r][:, q0:q0 + nq], self.k_full[:, k0:k1], self.v_full[:, k0:k1],
                          self.o[r][:, q0:q0 + nq], self.do[r][:, q0:q0 + nq],
                          self.lse[r][:, :, q0:], causal=True, bottom_right=True,
                          window=self.window, scale=self.scale, dq=self.dq[r][:, q0:q0 + nq],
                          dk=self.dk[:, k0:k1], dv=self.dv[:, k0:k1], grad_dtype=torch.float32,
-                         accumulate=True, lse_strides=(0, rows), workspace=self.bwd_ws)
-                n += attn.last_launch_count()
+                         accumulate=True, lse_strides=(0, rows), workspace=self.bwd_ws[r][i],
+                         stream=st, stage=stage)
+                return attn.last_launch_count()
+
+            for i in range(len(pcs)):  # independent: every call has its own rows
+                n += call(i, "preprocess")
+                n += call(i, "dq")
+            for i in range(len(pcs)):  # shared dK/dV: one after another
+                if prev is not None:
+                    st.wait_event(prev)
+                n += call(i, "dkdv")
+                prev = torch.cuda.Event()
+                prev.record(st)
+        self.streams.join()
         self.launches += n
         return self.dq, self.dk, self.dv
 

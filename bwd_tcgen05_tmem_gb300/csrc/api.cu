@@ -24,6 +24,28 @@ namespace {
 thread_local char g_err[512] = "";
 thread_local int g_launches = 0;
 
+// Test-only fault injection armed by attn_debug_inject for the next call on
+// this thread (then cleared).
+struct Inject {
+  unsigned mask;
+  int drop_load;
+  unsigned long long wait_ns;
+};
+thread_local Inject g_inject = {0u, -1, 0ull};
+
+Inject take_inject() {
+  const Inject r = g_inject;
+  g_inject = Inject{0u, -1, 0ull};
+  return r;
+}
+
+attn::DebugInject inject_for(const Inject& in, unsigned kernel_bit) {
+  attn::DebugInject d;
+  d.wait_ns = (in.mask & kernel_bit) ? in.wait_ns : 0ull;
+  d.drop_load = (in.mask & kernel_bit) ? in.drop_load : -1;
+  return d;
+}
+
 attn_status_t fail(attn_status_t s, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -286,6 +308,7 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
                        void* o, float* lse, void* ws, size_t ws_bytes, attn_stream_t stream) {
   g_err[0] = 0;
   g_launches = 0;
+  const Inject inj = take_inject();
   attn_status_t s = check_params(p);
   if (s) return s;
   cudaStream_t st = (cudaStream_t)stream;
@@ -340,6 +363,7 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
   fp.n_split = p->d_v > 256 ? p->d_v / 256 : 1;
   fp.scale_log2 = p->softmax_scale * 1.4426950408889634f;
   fp.status = status;
+  fp.dbg = inject_for(inj, ATTN_DEBUG_FWD);
   if (fp.n_qtiles == 0) return ATTN_OK;
   if (fp.n_qtiles > 65535 || p->batch > 65535)
     return fail(ATTN_ERR_UNSUPPORTED, "sequence or batch too large for the grid");
@@ -361,6 +385,7 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
                        void* dv, void* ws, size_t ws_bytes, attn_stream_t stream, int stages) {
   g_err[0] = 0;
   g_launches = 0;
+  const Inject inj = take_inject();
   attn_status_t s = check_params(p);
   if (s) return s;
   if (p->o_dtype != p->dtype)
@@ -432,6 +457,9 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
   a.scale = p->softmax_scale;
   a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
   a.status = status;
+  a.dbg_dq = inject_for(inj, ATTN_DEBUG_DQ);
+  a.dbg_dkdv = inject_for(inj, ATTN_DEBUG_DKDV);
+  a.dbg_scores = inject_for(inj, ATTN_DEBUG_SCORES);
   a.num_sms = num_sms();
   a.seqlen_q = p->seqlen_q;
   a.seqlen_k = p->seqlen_k;
@@ -549,7 +577,7 @@ attn_status_t attn_bwd_noalloc(const attn_params_t* p, const void* q, const void
                                void* dq, void* dk, void* dv, attn_stream_t stream) {
   g_err[0] = 0;
   g_launches = 0;
-  if (!p) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
+  if (attn_status_t s0 = check_params(p)) return s0;
   const size_t need = attn_bwd_workspace_size(p);
   if (need > kNoAllocScratchBytes)
     return fail(ATTN_ERR_WORKSPACE,
@@ -678,6 +706,10 @@ attn_status_t attn_query_status(const void* ws, attn_stream_t stream) {
 }
 
 const char* attn_last_error(void) { return g_err; }
+
+void attn_debug_inject(unsigned kernel_mask, int drop_load, uint64_t wait_limit_ns) {
+  g_inject = Inject{kernel_mask, drop_load, (unsigned long long)wait_limit_ns};
+}
 
 int attn_last_launch_count(void) { return g_launches; }
 

@@ -69,6 +69,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_lau
     dq.scale = a.scale;
     dq.scale_log2 = a.scale_log2;
     dq.status = a.status;
+    dq.dbg = a.dbg_dq;
     if (dq.n_qtiles > 65535 || a.batch > 65535 || a.hq > 65535) return cudaErrorInvalidValue;
     if ((e = launch_dq(dq, a.dqk, a.dv, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
     ++*n_launches;
@@ -103,6 +104,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_lau
       kp.scale = a.scale;
       kp.scale_log2 = a.scale_log2;
       kp.status = a.status;
+      kp.dbg = a.dbg_dkdv;
       if (kp.n_ktiles > 65535 || a.batch > 65535) return cudaErrorInvalidValue;
       if ((e = launch_dkv(kp, a.dqk, a.dv, mode[i], a.bf16, a.g_f32, st)) != cudaSuccess) return e;
       ++*n_launches;

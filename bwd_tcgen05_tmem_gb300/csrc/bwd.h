@@ -29,6 +29,9 @@ struct BwdArgs {
   long long* wide_plan;
   uint8_t* wide_blocks;
   long long wide_cap;
+  // test-only fault injection (attn_debug_inject), per kernel: dQ / dK-dV
+  // kernels, or the scores kernel and the dQ / dK-dV GEMMs of the wide path
+  DebugInject dbg_dq, dbg_dkdv, dbg_scores;
 };
 
 // ---------------------------------------------------------------- wide path
@@ -86,6 +89,7 @@ struct WideScoresParams {
   int batch, hq, hkv, n_qtiles;
   float scale_log2;
   int* status;
+  DebugInject dbg;
 };
 
 // dQ (kind 0: per query tile) and dV / dK (kind 1: per key tile) GEMMs over
@@ -105,6 +109,7 @@ struct WideAccParams {
   int batch, hq, hkv, n_tiles;
   float scale;
   int* status;
+  DebugInject dbg;
 };
 
 // q-stationary kernel: dQ = scale * sum_j dS_ij k_j
@@ -122,6 +127,7 @@ struct DqParams {
   int batch, hq, hkv, n_qtiles;
   float scale, scale_log2;
   int* status;
+  DebugInject dbg;
 };
 
 // kv-stationary kernel: dV = sum P^T dO, dK = scale * sum dS^T Q over the group
@@ -139,6 +145,7 @@ struct DkvParams {
   int batch, hq, hkv, n_ktiles;
   float scale, scale_log2;
   int* status;
+  DebugInject dbg;
 };
 
 cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* n_launches);

@@ -111,7 +111,9 @@ __global__ void __launch_bounds__(384, 1)
   const int n_qt = (i1 >= i0) ? (int)(i1 / BQ) - qt0 + 1 : 0;
   const int n_it = n_qt * grp;  // iterations: head-major over the group, then query tiles
 
-  Abort ab{&abort_flag, p.status};
+  const unsigned long long lim = wait_limit(p.dbg);
+  const int drop = dropped_load(p.dbg);
+  Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < C::kStages; ++i) {
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
-        if (elect_sync()) {
+        if (it != drop && elect_sync()) {  // drop: test-only injected missing load
           mbar_arrive_tx(&sfull[st], C::kStageBytes);
           uint8_t* dst = sStage + st * C::kStageBytes;
           if constexpr (C::kQStaged) {
@@ -213,13 +215,13 @@ __global__ void __launch_bounds__(384, 1)
         }
         __syncwarp();
       }
-      mbar_wait_quiet(&kv_bar, 0, kWaitLimitNs);
+      mbar_wait_quiet(&kv_bar, 0, lim);
       const uint32_t first = rcnt > (uint32_t)C::kRing ? rcnt - C::kRing : 0u;
       for (uint32_t c = first; c < rcnt; ++c)
-        mbar_wait_quiet(&rfull[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
+        mbar_wait_quiet(&rfull[c % C::kRing], (c / C::kRing) & 1u, lim);
       const int ns = ok ? n_it : it;  // stages issued
       for (int v = ns > C::kStages ? ns - C::kStages : 0; v < ns; ++v)
-        mbar_wait_quiet(&sfull[v % C::kStages], (v / C::kStages) & 1, kWaitLimitNs);
+        mbar_wait_quiet(&sfull[v % C::kStages], (v / C::kStages) & 1, lim);
     }
   } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------ MMA issuers
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(384, 1)
       uint64_t* drain = sc_role ? &drain_bar : &drain_bar2;
       if (elect_sync()) {
         mma_commit(drain);
-        mbar_wait_quiet(drain, 0, kWaitLimitNs);
+        mbar_wait_quiet(drain, 0, lim);
       }
       __syncwarp();
     }

@@ -83,7 +83,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
   const int kt0 = (j1 >= j0) ? (int)(j0 / BKV) : 0;
   const int n_kv = (j1 >= j0) ? (int)(j1 / BKV) - kt0 + 1 : 0;
 
-  Abort ab{&abort_flag, p.status};
+  const unsigned long long lim = wait_limit(p.dbg);
+  const int drop = dropped_load(p.dbg);
+  Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < C::kKStages; ++i) {
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
           break;
         }
         map_coords(p.ok, 0, g, krow, tb, d1, d2, d3);
-        if (elect_sync()) {
+        if (jt != drop && elect_sync()) {  // drop: test-only injected missing load
           mbar_arrive_tx(&kfull[st], C::kKStage);
 #pragma unroll
           for (int c = 0; c < C::kKCh; ++c)
@@ -164,13 +166,13 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
         }
         __syncwarp();
       }
-      mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
+      mbar_wait_quiet(&q_bar, 0, lim);
       const uint32_t first = vcnt > (uint32_t)C::kVRing ? vcnt - C::kVRing : 0u;
       for (uint32_t c = first; c < vcnt; ++c)
-        mbar_wait_quiet(&vfull[c % C::kVRing], (c / C::kVRing) & 1u, kWaitLimitNs);
+        mbar_wait_quiet(&vfull[c % C::kVRing], (c / C::kVRing) & 1u, lim);
       const int nk = ok ? n_kv : jt;  // K stages issued
       for (int v = nk > C::kKStages ? nk - C::kKStages : 0; v < nk; ++v)
-        mbar_wait_quiet(&kfull[v % C::kKStages], (v / C::kKStages) & 1, kWaitLimitNs);
+        mbar_wait_quiet(&kfull[v % C::kKStages], (v / C::kKStages) & 1, lim);
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
       uint64_t* drain = sc_role ? &drain_bar : &drain_bar2;
       if (elect_sync()) {
         mma_commit(drain);
-        mbar_wait_quiet(drain, 0, kWaitLimitNs);
+        mbar_wait_quiet(drain, 0, lim);
       }
       __syncwarp();
     }

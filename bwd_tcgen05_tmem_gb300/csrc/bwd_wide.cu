@@ -148,7 +148,9 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   if (skip_sh) return;
 
-  Abort ab{&abort_flag, p.status};
+  const unsigned long long lim = wait_limit(p.dbg);
+  const int drop = dropped_load(p.dbg);
+  Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < C::kRing; ++i) {
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
-        if (elect_sync()) {
+        if ((int)cnt != drop && elect_sync()) {  // drop: test-only injected missing load
           mbar_arrive_tx(&rfull[slot], C::kChunk);
           if (c < C::kQCh)
             tma_load_4d(sRing + slot * C::kChunk, &p.tm_k, &rfull[slot], c * 64, k1, k2, k3);
@@ -210,10 +212,10 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
     // let the copies in flight land before the CTA exits
-    mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
+    mbar_wait_quiet(&q_bar, 0, lim);
     const uint32_t first = cnt > (uint32_t)C::kRing ? cnt - C::kRing : 0u;
     for (uint32_t c = first; c < cnt; ++c)
-      mbar_wait_quiet(&rfull[c % C::kRing], (c / C::kRing) & 1u, kWaitLimitNs);
+      mbar_wait_quiet(&rfull[c % C::kRing], (c / C::kRing) & 1u, lim);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = make_idesc(128, 128, BF16, false, false);
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     if (elect_sync()) {
       mma_commit(&drain_bar);
-      mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+      mbar_wait_quiet(&drain_bar, 0, lim);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -462,7 +464,9 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   if (skip_sh) return;
 
-  Abort ab{&abort_flag, p.status};
+  const unsigned long long lim = wait_limit(p.dbg);
+  const int drop = dropped_load(p.dbg);
+  Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < C::kNA; ++i) {
@@ -532,7 +536,7 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         uint8_t* adst = sA + as * C::kA;
-        if (elect_sync()) {
+        if (s != drop && elect_sync()) {  // drop: test-only injected missing load
           mbar_arrive_tx(&afull[as], C::kA);
           if (KIND == 0) {  // dS sub-tile `half`: 128 query rows x 64 keys
             bulk_load(adst, src + 2 * kWideTile + half * kWideTile, kWideTile, &afull[as]);
@@ -573,10 +577,10 @@ __global__ void __launch_bounds__(384, 1)
       }
       // let the copies in flight land
       for (int v = s > C::kNA ? s - C::kNA : 0; v < s; ++v)
-        mbar_wait_quiet(&afull[v % C::kNA], (v / C::kNA) & 1, kWaitLimitNs);
+        mbar_wait_quiet(&afull[v % C::kNA], (v / C::kNA) & 1, lim);
       const uint32_t first = bcnt > (uint32_t)C::kNB ? bcnt - C::kNB : 0u;
       for (uint32_t c = first; c < bcnt; ++c)
-        mbar_wait_quiet(&bfull[c % C::kNB], (c / C::kNB) & 1u, kWaitLimitNs);
+        mbar_wait_quiet(&bfull[c % C::kNB], (c / C::kNB) & 1u, lim);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -617,7 +621,7 @@ __global__ void __launch_bounds__(384, 1)
       if (elect_sync()) {
         mma_commit(&acc_done);
         mma_commit(&drain_bar);
-        mbar_wait_quiet(&drain_bar, 0, kWaitLimitNs);
+        mbar_wait_quiet(&drain_bar, 0, lim);
       }
       __syncwarp();
     }
@@ -767,6 +771,10 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
       if ((e = launch_pre(pp, a.bf16, a.num_sms, st)) != cudaSuccess) return e;
       ++*n_launches;
     }
+  }
+  // the block plan belongs to the dq stage (it depends on the key side and the
+  // mask), so a D preprocess is valid for every problem with the same query rows
+  if (stages & 2) {
     WidePlanParams pl;
     pl.geo = a.geo;
     pl.plan = a.wide_plan;
@@ -805,6 +813,7 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
       sp.n_qtiles = nqt;
       sp.scale_log2 = a.scale_log2;
       sp.status = a.status;
+      sp.dbg = a.dbg_scores;
       if ((e = a.bf16 ? launch_scores<true>(sp, a.dqk, st) : launch_scores<false>(sp, a.dqk, st)) !=
           cudaSuccess)
         return e;
@@ -831,6 +840,7 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
     qp.n_tiles = nqt;
     qp.scale = a.scale;
     qp.status = a.status;
+    qp.dbg = a.dbg_dq;
     if ((e = launch_acc<0>(qp, a.dqk, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
     ++*n_launches;
   }
@@ -856,6 +866,7 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
     kp.n_tiles = nkt;
     kp.scale = a.scale;
     kp.status = a.status;
+    kp.dbg = a.dbg_dkdv;
     if ((e = launch_acc<1>(kp, a.dqk, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
     ++*n_launches;
   }

@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   const int kt0 = (j1 >= j0) ? (int)(j0 / kBlockN) : 0;
   const int n_kv = (j1 >= j0) ? (int)(j1 / kBlockN) - kt0 + 1 : 0;
 
-  Abort ab{&abort_flag, p.status};
+  const unsigned long long lim = wait_limit(p.dbg);
+  const int drop = dropped_load(p.dbg);
+  Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < C::kKRing; ++i) {
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
           ok = false;
           return;
         }
-        if (elect_sync()) {
+        if (vcnt != drop && elect_sync()) {  // drop: test-only injected missing load
           mbar_arrive_tx(&vfull[st], C::kVCh * kSlotBytes);
 #pragma unroll
           for (int c = 0; c < C::kVCh; ++c)
@@ -171,12 +173,12 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
         if (ok) load_v(jt);
       }
       // let every copy still in flight land before the CTA can exit
-      mbar_wait_quiet(&q_bar, 0, kWaitLimitNs);
+      mbar_wait_quiet(&q_bar, 0, lim);
       const uint32_t first = kcnt > (uint32_t)C::kKRing ? kcnt - C::kKRing : 0u;
       for (uint32_t c = first; c < kcnt; ++c)
-        mbar_wait_quiet(&kfull[c % C::kKRing], (c / C::kKRing) & 1u, kWaitLimitNs);
+        mbar_wait_quiet(&kfull[c % C::kKRing], (c / C::kKRing) & 1u, lim);
       for (int v = vcnt > C::kVStages ? vcnt - C::kVStages : 0; v < vcnt; ++v)
-        mbar_wait_quiet(&vfull[v % C::kVStages], (v / C::kVStages) & 1, kWaitLimitNs);
+        mbar_wait_quiet(&vfull[v % C::kVStages], (v / C::kVStages) & 1, lim);
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       uint64_t* drain = s_role ? &drain_bar : &drain_bar2;
       if (elect_sync()) {
         mma_commit(drain);
-        mbar_wait_quiet(drain, 0, kWaitLimitNs);
+        mbar_wait_quiet(drain, 0, lim);
       }
       __syncwarp();
     }

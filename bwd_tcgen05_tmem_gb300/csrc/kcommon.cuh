@@ -80,6 +80,27 @@ __host__ __device__ inline void query_range(const Seq& s, long long j0, long lon
   if (i1 > s.lq - 1) i1 = s.lq - 1;
 }
 
+// ----------------------------------------------------------------- fault injection
+// Test-only (attn_debug_inject): the first CTA of a launch may run with a
+// shorter wait limit and leave out one of its loads, so that a wait is certain
+// to run out and the unwind path (abort flag, status word, in-flight copies
+// landed, MMAs drained, TMEM freed) runs.  Every other CTA, and every launch
+// without an injection, uses kWaitLimitNs and leaves out nothing.
+struct DebugInject {
+  unsigned long long wait_ns;  // 0: kWaitLimitNs
+  int drop_load;               // index of the load the first CTA leaves out; -1: none
+};
+
+__device__ __forceinline__ bool first_cta() {
+  return (blockIdx.x | blockIdx.y | blockIdx.z) == 0;
+}
+__device__ __forceinline__ unsigned long long wait_limit(const DebugInject& d) {
+  return (d.wait_ns && first_cta()) ? d.wait_ns : kWaitLimitNs;
+}
+__device__ __forceinline__ int dropped_load(const DebugInject& d) {
+  return first_cta() ? d.drop_load : -1;
+}
+
 // ----------------------------------------------------------------- params
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;
@@ -92,6 +113,7 @@ struct FwdParams {
   int batch, hq, hkv, n_qtiles, n_split;
   float scale_log2;
   int* status;
+  DebugInject dbg;
 };
 
 }  // namespace attn

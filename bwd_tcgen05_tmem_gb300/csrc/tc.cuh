@@ -77,8 +77,9 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Abort state shared by all roles of a CTA: once any wait gives up, every
 // role stops waiting and unwinds.  `status` is the caller's device status word.
 struct Abort {
-  volatile int* flag;  // shared memory
-  int* status;         // global memory, may be null
+  volatile int* flag;           // shared memory
+  int* status;                  // global memory, may be null
+  unsigned long long limit_ns;  // wall-clock limit of one wait
 };
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the abort
@@ -91,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (mbar_test(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*ab.flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > ab.limit_ns) {
         *ab.flag = 1;
         if (ab.status) atomicExch(ab.status, DEV_TIMEOUT);
         return false;

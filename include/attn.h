@@ -144,12 +144,16 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
  *                        status word (PR #3699 "backward helper chain");
  *   attn_bwd_dq:         dQ (reads D from the workspace);
  *   attn_bwd_dkdv:       dK and dV, reduced over each GQA group (reads D).
- * The dq and dkdv stages require a preprocess on the same workspace, for the
- * same problem, earlier on the stream.  Where the backward materialises P and
- * dS (head dim 512; head dim 256 up to 16 GiB of blocks) the dq stage also
- * writes them into the workspace and the dkdv stage reads them: it then
- * requires the dq stage earlier on the stream as well.  Arguments a stage
- * does not use may be NULL.
+ * The dq and dkdv stages require a preprocess earlier on the stream, on the
+ * same workspace, for a problem with the same query rows, query heads, dtype
+ * and batch/cu_seqlens_q layout: D depends only on O and dO of each query
+ * row, so one preprocess serves several calls that differ only in their keys,
+ * mask or window (a context-parallel ring does this).  Where the backward
+ * materialises P and dS (head dim 512; head dim 256 up to 16 GiB of blocks)
+ * the dq stage also writes them, with their block plan, into the workspace
+ * and the dkdv stage reads them: it then requires the dq stage of the same
+ * problem earlier on the stream as well.  Arguments a stage does not use may
+ * be NULL.
  */
 attn_status_t attn_bwd_preprocess(const attn_params_t* p, const void* q, const void* k,
                                   const void* v, const void* o, const void* dout,
@@ -247,6 +251,31 @@ const char* attn_last_error(void);
 /* Number of kernels the last successful attn_fwd / attn_bwd / attn_lse_merge
  * call on this thread enqueued. */
 int attn_last_launch_count(void);
+
+/*
+ * TEST ONLY: fault injection for the bounded-wait unwind path.  Every wait of
+ * the attention kernels on an mbarrier phase has a wall-clock limit (2 s by
+ * default); when one runs out the CTA raises ATTN_ERR_TIMEOUT in the status
+ * word, lets its in-flight copies land, drains its MMAs, frees its TMEM and
+ * returns -- no kernel traps or hangs (PR #3699's bot review found a
+ * "missing wait" on a reused barrier phase; this is the guard against that
+ * class of bug).  This call arms the NEXT attn_fwd / attn_bwd* call on the
+ * calling thread, then clears itself: in every kernel selected by
+ * `kernel_mask` (ATTN_DEBUG_* bits), the first CTA of the launch (block
+ * 0,0,0) leaves out its load number `drop_load` (-1: none; the counter is the
+ * kernel's stage/ring load index) and, if `wait_limit_ns` is non-zero, uses
+ * that wait limit instead of 2 s.  No other CTA and no other call is
+ * affected.  A dropped load makes a wait run out, so the call reports
+ * ATTN_ERR_TIMEOUT through attn_query_status and leaves its outputs
+ * undefined; the device stays usable and later calls are unaffected.
+ */
+enum {
+  ATTN_DEBUG_FWD = 1,    /* forward kernel */
+  ATTN_DEBUG_DQ = 2,     /* dQ kernel, or the dQ GEMM of the materialising backward */
+  ATTN_DEBUG_DKDV = 4,   /* dK/dV kernel, or the dK/dV GEMMs of the materialising backward */
+  ATTN_DEBUG_SCORES = 8  /* P/dS scores kernel of the materialising backward */
+};
+void attn_debug_inject(unsigned kernel_mask, int drop_load, uint64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }
