@@ -82,10 +82,10 @@ def file_hash(name):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def load_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    if there is none or the kernel source changed since it was captured."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+def load_profile_value(fname, kernel):
+    """A per-kernel figure from a committed ncu summary (`kernel value hash`
+    lines), or None if there is none or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", fname)
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -96,6 +96,45 @@ def load_traffic(kernel):
                     return None
                 return float(parts[1])
     return None
+
+
+def load_traffic(kernel):
+    """DRAM bytes per full-size launch of `kernel` (ncu, scaled from the 4K case)."""
+    return load_profile_value("dram_traffic.txt", kernel)
+
+
+def load_tensor_pipe(kernel):
+    """Tensor-pipe active % of `kernel` (ncu sm__pipe_tensor_cycles_active, 4K case)."""
+    return load_profile_value("tensor_pipe.txt", kernel)
+
+
+def cpu_model():
+    """Host CPU model string (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def spread(xs):
+    """Median and spread of a list of per-step times."""
+    ys = sorted(xs)
+    n = len(ys)
+    q = lambda f: ys[min(n - 1, max(0, int(round(f * (n - 1)))))]  # noqa: E731
+    return {"median": statistics.median(ys), "min": ys[0], "max": ys[-1],
+            "p25": q(0.25), "p75": q(0.75), "n": n}
 
 
 class ClockSampler:
@@ -195,7 +234,8 @@ def cpu_baseline(w, seconds_target=15.0):
         rows = min(S, max(rows, int(rows * seconds_target / dt)))
         dt, f = run(rows)
     return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads,
-            "kind": "oracle", "seconds": round(dt, 2),
+            "kind": "oracle", "seconds": round(dt, 2), "cpu_model": cpu_model(),
+            "host_cores": ncpu,
             "sample": f"FP64 oracle fwd+bwd of the last {rows} query rows of all "
                       f"{w.heads_q} heads (bottom-right causal against all {S} keys), "
                       f"{nthreads} threads of {ncpu} host cores"}
@@ -277,6 +317,7 @@ def main():
     __graft_entry__.build()
     from bwd_tcgen05_tmem_gb300 import attn
 
+    peaks0, peak_src0 = load_peaks()
     inp = synth.make_inputs(w)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "dout"))
     kw = dict(causal=True, scale=w.scale, window=w.window)
@@ -334,6 +375,9 @@ def main():
     total_ms = t0.elapsed_time(t1)
     per_kernel = {st: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in events)
                   for i, st in enumerate(stages)}
+    step_spread = spread([e[0].elapsed_time(e[4]) for e in events])
+    kernel_spread = {st: spread([e[i].elapsed_time(e[i + 1]) for e in events])
+                     for i, st in enumerate(stages)}
     ms = total_ms / args.steps
     ms = max_over_ranks(ms, dev)
     clocks = clk.summary()
@@ -400,6 +444,35 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dev)
+
+    # the same host copies alone (no kernels): the host link's rate, each
+    # direction on its own and both at once, to read the e2e figure against
+    def copy_run(up, down, n=3):
+        cur = torch.cuda.current_stream()
+        up_st.wait_stream(cur)
+        down_st.wait_stream(cur)
+        for _ in range(n):
+            if up:
+                with torch.cuda.stream(up_st):
+                    for d_, h_ in zip(dev_in[0], host_in):
+                        d_.copy_(h_, non_blocking=True)
+            if down:
+                with torch.cuda.stream(down_st):
+                    for h_, d_ in zip(host_out[0], dev_out[0]):
+                        h_.copy_(d_, non_blocking=True)
+        cur.wait_stream(up_st)
+        cur.wait_stream(down_st)
+
+    copy_gbs = {}
+    for name, up, down in (("h2d", True, False), ("d2h", False, True), ("both", True, True)):
+        copy_run(up, down, 1)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        copy_run(up, down, 3)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        nbytes = 3 * ((h2d if up else 0) + (d2h if down else 0))
+        copy_gbs[name] = nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
     del dev_in, dev_out, e2e_ws
 
     # ---- one-GPU context-parallel ring emulation (dual chunk swap, 8 ranks)
@@ -425,7 +498,29 @@ def main():
             torch.cuda.synchronize()
             fwd_ms += c0.elapsed_time(c1) / n_cp
             bwd_ms += c1.elapsed_time(c2) / n_cp
+        # the LSE-merge kernel alone: every rank's merge, back to back on one
+        # stream; algorithmic bytes = the parts' FP32 O and LSE read once plus
+        # the merged O (bf16) and LSE written once
+        n_m = 5
+        m_bytes = 0
+        for r_, pcs in enumerate(ring.pieces):
+            for pc in pcs:
+                m_bytes += pc.q_rows[1] * w.heads_q * (4 * w.d_v + 4)
+            m_bytes += 2 * ring.chunk * w.heads_q * (2 * w.d_v + 4)
+        ring.merge_all()
+        c0.record(stream)
+        for _ in range(n_m):
+            ring.merge_all()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        merge_ms = c0.elapsed_time(c1) / n_m
         cp_obj = {"cp": 8, "chunks": 16, "chunk_tokens": w.seqlen // 16,
+                  "merge": {"ms": merge_ms, "bytes": m_bytes,
+                            "gbs": m_bytes / (merge_ms * 1e-3) / 1e9,
+                            "hbm_frac": m_bytes / (merge_ms * 1e-3) / 1e9 / peaks0["hbm_gbs"],
+                            "launches": 8,
+                            "note": "attn_lse_merge of all 8 ranks (FP32 partials of every "
+                                    "ring step), timed alone on one stream"},
                   "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "ms": fwd_ms + bwd_ms,
                   "tflops": fl["total"] / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
                   "launches": ring.launches,
@@ -488,8 +583,12 @@ def main():
                     "whole sequence for H/cp heads per rank, outputs and gradients back"}
         del a2a
 
-    peaks, peak_src = load_peaks()
-    peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    peaks, peak_src = peaks0, peak_src0
+    # the kernels run at close to the maximum SM clock (sampled below), so the
+    # burst figure is the denominator; the sustained one (measured under the
+    # power cap at a lower clock) is reported beside it
+    peak_tf = peaks.get("bf16_tflops", peaks.get("bf16_tflops_sustained"))
+    peak_sus = peaks.get("bf16_tflops_sustained", peak_tf)
     dom = max(("fwd", "dq", "dkdv"), key=lambda s: per_kernel[s])
     ach = fl["kernel"][dom] / (per_kernel[dom] * 1e-3) / 1e12
     traffic = load_traffic(dom)
@@ -512,23 +611,37 @@ def main():
                    "causal": True, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (no flush)"},
         "pct_of_peak": 100.0 * (value / world) / peak_tf,
+        "pct_of_peak_sustained": 100.0 * (value / world) / peak_sus,
         "peak_tflops": peak_tf,
-        "peak_source": f"{peak_src} (bf16 sustained)",
+        "peak_tflops_sustained": peak_sus,
+        "peak_source": f"{peak_src} (bf16 burst; sustained beside it)",
+        "step_ms": step_spread,
+        "kernel_ms_spread": kernel_spread,
         "tflops_fwd": fl["fwd"] / (per_kernel["fwd"] * 1e-3) / 1e12,
         "tflops_bwd": fl["bwd"] / ((per_kernel["pre"] + per_kernel["dq"] + per_kernel["dkdv"])
                                    * 1e-3) / 1e12,
         "kernel_ms": {k_: round(v_, 4) for k_, v_ in per_kernel.items()},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": ach / peak_tf, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained",
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "peak_sustained": peak_sus, "frac_sustained": ach / peak_sus,
+                     "sm_mhz": clocks.get("sm_mhz"),
                      "work_per_launch": fl["kernel"][dom]},
+        "kernels": {k_: {"ms": per_kernel[k_],
+                         "tflops": fl["kernel"][k_] / (per_kernel[k_] * 1e-3) / 1e12,
+                         "frac": fl["kernel"][k_] / (per_kernel[k_] * 1e-3) / 1e12 / peak_tf,
+                         "tensor_pipe_pct": load_tensor_pipe(k_)}
+                    for k_ in ("fwd", "dq", "dkdv")},
         "pre_gbs": (q.shape[0] * (1 if w.is_thd else q.shape[1]) * w.heads_q * (2 * w.d_v * 2 + 4)) /
                    (per_kernel["pre"] * 1e-3) / 1e9,
+        "pre_hbm_frac": (q.shape[0] * (1 if w.is_thd else q.shape[1]) * w.heads_q *
+                         (2 * w.d_v * 2 + 4)) / (per_kernel["pre"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "e2e": {"value": job_tflops(fl["total"], e2e_ms, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps,
+                "steps": e2e_steps, "copy_only_gbs": copy_gbs,
                 "note": "public API on inputs uploaded from pinned host memory and all outputs "
-                        "downloaded every step, pipelined over two device buffer sets"},
+                        "downloaded every step, pipelined over two device buffer sets; "
+                        "copy_only_gbs: the same copies alone (h2d, d2h, both at once)"},
         "gpu_launches": launches,
         "clocks": clocks,
         "cp_emulation": cp_obj,
