@@ -38,9 +38,14 @@ def _problem(seed_shift, s=333, hq=4, hkv=2, dqk=192, dv=128):
     return q, k, v, do
 
 
-def test_noalloc_backward_matches_attn_bwd_twice():
+@pytest.mark.parametrize("shape", [dict(s=333, hq=4, hkv=2, dqk=192, dv=128),
+                                   dict(s=200, hq=4, hkv=1, dqk=512, dv=512)],
+                         ids=["fused-192-128", "materialising-d512-gqa"])
+def test_noalloc_backward_matches_attn_bwd_twice(shape):
+    # the d512 case runs the materialising backward, whose P/dS blocks
+    # (768 KiB here) also live in the static scratch area
     for call, shift in enumerate((0, 10)):
-        q, k, v, do = _problem(shift)
+        q, k, v, do = _problem(shift, **shape)
         scale = 1.0 / math.sqrt(q.shape[-1])
         o, lse = attn.fwd(q, k, v, scale=scale)
         ref = attn.bwd(q, k, v, o, do, lse, scale=scale)
