@@ -114,7 +114,11 @@ cudaError_t launch_pre(const PreParams& p, bool bf16, int num_sms, cudaStream_t 
 }
 
 // ----------------------------------------------------------------- LSE merge
-// One warp per (row, head); each lane owns 4 consecutive value columns per step.
+// One warp per (row, head).  Lane q fetches the LSE of parts q and q + 32 at
+// this row (-inf where a part does not cover it), so all of a row's LSE loads
+// are in flight at once; the maximum and the sum of exp(LSE_p - max) are warp
+// reductions.  The O parts are then read as 16-byte loads, lane = 4 value
+// columns, with each part's weight exp(LSE_p - LSE) broadcast by a shuffle.
 __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ MergeParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t total = p.rows * p.heads;
@@ -123,41 +127,50 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
   for (int64_t w = warp_id; w < total; w += nwarps) {
     const int64_t r = w / p.heads;
     const int h = (int)(w % p.heads);
-    // maximum over the parts covering this row
-    float m = -INFINITY;
-    for (int q = 0; q < p.n; ++q) {
-      const int64_t lr = r - p.row0[q];
-      if (lr < 0 || lr >= p.nrows[q]) continue;
-      m = fmaxf(m, p.lse[q][(int64_t)h * p.nrows[q] + lr]);
-    }
-    float sum = 0.0f;
-    if (m != -INFINITY) {
-      for (int q = 0; q < p.n; ++q) {
-        const int64_t lr = r - p.row0[q];
-        if (lr < 0 || lr >= p.nrows[q]) continue;
-        const float l = p.lse[q][(int64_t)h * p.nrows[q] + lr];
-        if (l != -INFINITY) sum += __expf(l - m);
-      }
-    }
-    const float lse = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
-    if (lane == 0) p.lse_out[(int64_t)h * p.rows + r] = lse;
-    for (int c = lane * 4; c < p.dv; c += 128) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (m != -INFINITY) {
-        for (int q = 0; q < p.n; ++q) {
-          const int64_t lr = r - p.row0[q];
-          if (lr < 0 || lr >= p.nrows[q]) continue;
-          const float l = p.lse[q][(int64_t)h * p.nrows[q] + lr];
-          if (l == -INFINITY) continue;
-          const float a = __expf(l - lse);
-          const float4 v =
-              *reinterpret_cast<const float4*>(p.o[q] + (lr * p.heads + h) * (int64_t)p.dv + c);
-          acc.x = fmaf(a, v.x, acc.x);
-          acc.y = fmaf(a, v.y, acc.y);
-          acc.z = fmaf(a, v.z, acc.z);
-          acc.w = fmaf(a, v.w, acc.w);
+    float l[2] = {-INFINITY, -INFINITY};
+    int64_t lr[2] = {0, 0};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int q = lane + 32 * u;
+      if (q < p.n) {
+        const int64_t x = r - p.row0[q];
+        if (x >= 0 && x < p.nrows[q]) {
+          lr[u] = x;
+          l[u] = p.lse[q][(int64_t)h * p.nrows[q] + x];
         }
       }
+    }
+    float m = fmaxf(l[0], l[1]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = (l[0] == -INFINITY ? 0.0f : __expf(l[0] - m)) +
+                (l[1] == -INFINITY ? 0.0f : __expf(l[1] - m));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float lse = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
+    if (lane == 0) p.lse_out[(int64_t)h * p.rows + r] = lse;
+    // weight of each part (0 for -inf parts and parts not covering the row)
+    const float a[2] = {l[0] == -INFINITY ? 0.0f : __expf(l[0] - lse),
+                        l[1] == -INFINITY ? 0.0f : __expf(l[1] - lse)};
+    for (int c0 = 0; c0 < p.dv; c0 += 128) {
+      const int c = c0 + lane * 4;
+      const bool act = c < p.dv;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int q = 0; q < p.n; ++q) {
+        const int u = q >> 5;
+        const float aq = __shfl_sync(0xffffffffu, u ? a[1] : a[0], q & 31);
+        const int64_t xq = __shfl_sync(0xffffffffu, u ? lr[1] : lr[0], q & 31);
+        if (aq != 0.0f && act) {
+          const float4 v =
+              *reinterpret_cast<const float4*>(p.o[q] + (xq * p.heads + h) * (int64_t)p.dv + c);
+          acc.x = fmaf(aq, v.x, acc.x);
+          acc.y = fmaf(aq, v.y, acc.y);
+          acc.z = fmaf(aq, v.z, acc.z);
+          acc.w = fmaf(aq, v.w, acc.w);
+        }
+      }
+      if (!act) continue;
       const int64_t off = (r * p.heads + h) * (int64_t)p.dv + c;
       if (p.out_kind == 2) {
         *reinterpret_cast<float4*>((float*)p.o_out + off) = acc;
