@@ -94,6 +94,9 @@ WORKLOADS = {
         Workload("tiny_b1_h2_s256_d64", 1, 256, 2, 2, 64, 64),
         Workload("b2_h32_s4096_d192_128", 2, 4096, 32, 32, 192, 128),
         Workload("b1_h32_s32768_d192_128", 1, 32768, 32, 32, 192, 128),
+        # the same heads at 8K: a profiling case (64 tiles per head, so the
+        # grid runs in the same tile-major order as 32K; inputs above L2)
+        Workload("b1_h32_s8192_d192_128", 1, 8192, 32, 32, 192, 128),
         Workload("thd_h32_kv8_t65536_d128_fp16", 0, 0, 32, 8, 128, 128, dtype="fp16",
                  thd_total=65536),
         Workload("thd_h32_kv8_t65536_d128_bf16", 0, 0, 32, 8, 128, 128, dtype="bf16",
