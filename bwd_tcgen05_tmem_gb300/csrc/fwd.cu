@@ -35,7 +35,18 @@ struct FwdCfg {
   static constexpr int kVStages = (kQSlots + 2 * kVCh + 2 <= kMaxSlots) ? 2 : 1;
   static constexpr int kKRingRaw = kMaxSlots - kQSlots - kVStages * kVCh;
   static constexpr int kKRing = kKRingRaw > 16 ? 16 : kKRingRaw;
-  static constexpr int kSmem = (kQSlots + kVStages * kVCh + kKRing) * kSlotBytes + 1024;
+  // Where Q leaves too little room for a K ring of two tiles next to the V
+  // stages (head dims 256 and 512: a K tile is 64-128 KB), K and V stream
+  // through one ring of slot pairs instead (32 KB each, two 64-column chunks):
+  // every slot beyond Q serves whichever operand the MMAs need next.  A K pair
+  // feeds 8 S MMAs, a V pair one N = 128 half of the PV product.
+  static constexpr bool kPR = kKRingRaw < 2 * kKCh;
+  static constexpr int kPairs = (kMaxSlots - kQSlots) / 2;
+  static constexpr int kKP = kKCh / 2;  // K pairs per key tile
+  static constexpr int kVP = kVCh / 2;  // V pairs per key tile
+  static constexpr int kSmem =
+      (kPR ? kQSlots + 2 * kPairs : kQSlots + kVStages * kVCh + kKRing) * kSlotBytes + 1024;
+  static_assert(!kPR || (kKCh % 2 == 0 && kVCh % 2 == 0 && kPairs >= 2), "pair ring");
   static constexpr int kSB = DV_CTA <= 128 ? 3 : 2;  // S buffers
   static constexpr int kTmemO = 128 * kSB;
   static_assert(kTmemO + DV_CTA <= 512, "TMEM budget");
@@ -53,6 +64,12 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   uint8_t* sK = sV + C::kVStages * C::kVCh * kSlotBytes;
 
   __shared__ uint64_t kfull[C::kKRing], kempty[C::kKRing], vfull[C::kVStages], vempty[C::kVStages];
+  // pair ring (kPR): one empty barrier per pair, and a full barrier per pair
+  // and consumer -- each issuer waits only on loads meant for it, so its parity
+  // wait can never match an older, still pending load of the other issuer
+  constexpr int kNP = C::kPR ? C::kPairs : 1;
+  __shared__ uint64_t pempty[kNP], pfull_k[kNP], pfull_v[kNP];
+  uint8_t* sRing = smem + C::kQSlots * kSlotBytes;  // kPR: pair s at sRing + s * 2 slots
   // o_done[b]: PV of the key tiles that used S buffer b (one phase per use)
   __shared__ uint64_t q_bar, s_full[C::kSB], p_full[C::kSB], o_done[C::kSB], drain_bar, drain_bar2;
   __shared__ uint32_t tmem_base_sh;
@@ -93,6 +110,11 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
     for (int i = 0; i < C::kVStages; ++i) {
       mbar_init(&vfull[i], 1);
       mbar_init(&vempty[i], 1);
+    }
+    for (int i = 0; i < kNP; ++i) {
+      mbar_init(&pempty[i], 1);
+      mbar_init(&pfull_k[i], 1);
+      mbar_init(&pfull_v[i], 1);
     }
     mbar_init(&q_bar, 1);
     for (int i = 0; i < C::kSB; ++i) {
@@ -167,18 +189,67 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
         __syncwarp();
         ++vcnt;
       };
-      load_k(0);
-      for (int jt = 0; jt < n_kv && ok; ++jt) {
-        if (jt + 1 < n_kv) load_k(jt + 1);
-        if (ok) load_v(jt);
+      if constexpr (!C::kPR) {
+        load_k(0);
+        for (int jt = 0; jt < n_kv && ok; ++jt) {
+          if (jt + 1 < n_kv) load_k(jt + 1);
+          if (ok) load_v(jt);
+        }
+      } else {
+        // pair ring: the same order (K0, K1, V0, K2, V1, ...) at pair granularity.
+        // Per slot: which consumer the last load was for and the parity it
+        // completes, to let copies in flight land before the CTA exits.
+        uint32_t L = 0, kpar = 0, vpar = 0, lastk = 0, lastpar = 0, used = 0;
+        auto load_pair = [&](bool is_k, int jt, int pp) {
+          const uint32_t slot = L % C::kPairs;
+          if (!mbar_wait_warp(&pempty[slot], ((L / C::kPairs) & 1u) ^ 1u, ab)) {
+            ok = false;
+            return;
+          }
+          const uint32_t bit = 1u << slot;
+          const uint32_t par = ((is_k ? kpar : vpar) & bit) ? 1u : 0u;
+          if (is_k) kpar ^= bit; else vpar ^= bit;
+          lastk = is_k ? (lastk | bit) : (lastk & ~bit);
+          lastpar = par ? (lastpar | bit) : (lastpar & ~bit);
+          used |= bit;
+          uint64_t* full = is_k ? &pfull_k[slot] : &pfull_v[slot];
+          int d1, d2, d3;
+          map_coords(is_k ? p.ok : p.ov, 0, g, sq.k_start + (kt0 + jt) * kBlockN, tb, d1, d2, d3);
+          uint8_t* dst = sRing + slot * 2 * kSlotBytes;
+          // drop: test-only injected missing load (the first V pair of tile `drop`)
+          if (!(!is_k && pp == 0 && jt == drop) && elect_sync()) {
+            mbar_arrive_tx(full, 2 * kSlotBytes);
+            for (int c = 0; c < 2; ++c) {
+              if (is_k)
+                tma_load_4d(dst + c * kSlotBytes, &p.tm_k, full, (2 * pp + c) * 64, d1, d2, d3);
+              else
+                tma_load_4d(dst + c * kSlotBytes, &p.tm_v, full,
+                            split * DV_CTA + (2 * pp + c) * 64, d1, d2, d3);
+            }
+          }
+          __syncwarp();
+          ++L;
+        };
+        for (int pp = 0; pp < C::kKP && ok; ++pp) load_pair(true, 0, pp);
+        for (int jt = 0; jt < n_kv && ok; ++jt) {
+          if (jt + 1 < n_kv)
+            for (int pp = 0; pp < C::kKP && ok; ++pp) load_pair(true, jt + 1, pp);
+          for (int pp = 0; pp < C::kVP && ok; ++pp) load_pair(false, jt, pp);
+        }
+        for (int sl = 0; sl < C::kPairs; ++sl)
+          if (used & (1u << sl))
+            mbar_wait_quiet((lastk >> sl) & 1u ? &pfull_k[sl] : &pfull_v[sl],
+                            (lastpar >> sl) & 1u, lim);
       }
       // let every copy still in flight land before the CTA can exit
       mbar_wait_quiet(&q_bar, 0, lim);
-      const uint32_t first = kcnt > (uint32_t)C::kKRing ? kcnt - C::kKRing : 0u;
-      for (uint32_t c = first; c < kcnt; ++c)
-        mbar_wait_quiet(&kfull[c % C::kKRing], (c / C::kKRing) & 1u, lim);
-      for (int v = vcnt > C::kVStages ? vcnt - C::kVStages : 0; v < vcnt; ++v)
-        mbar_wait_quiet(&vfull[v % C::kVStages], (v / C::kVStages) & 1, lim);
+      if constexpr (!C::kPR) {
+        const uint32_t first = kcnt > (uint32_t)C::kKRing ? kcnt - C::kKRing : 0u;
+        for (uint32_t c = first; c < kcnt; ++c)
+          mbar_wait_quiet(&kfull[c % C::kKRing], (c / C::kKRing) & 1u, lim);
+        for (int v = vcnt > C::kVStages ? vcnt - C::kVStages : 0; v < vcnt; ++v)
+          mbar_wait_quiet(&vfull[v % C::kVStages], (v / C::kVStages) & 1, lim);
+      }
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
@@ -242,16 +313,81 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
         }
         __syncwarp();
       };
+      // pair ring: a load's position in the producer's sequence fixes its slot
+      //   K(j) pair p: j == 0 ? p : kKP + (j - 1)(kKP + kVP) + p
+      //   V(j) pair p: kKP + j (kKP + kVP) + (j + 1 < n_kv ? kKP : 0) + p
+      const uint64_t rdesc = make_sdesc(smem_u32(sRing), 16, 1024);              // K-major
+      const uint64_t rdesc_mn = make_sdesc(smem_u32(sRing), kSlotBytes, 1024);   // MN-major
+      constexpr uint32_t idesc_o2 = make_idesc(128, 128, BF16, false, true);
+      uint32_t rpar = 0;  // per slot: parity of this issuer's next wait on it
+      auto issue_s_pr = [&](int jt) {
+        const uint32_t d = tmem + (uint32_t)((jt % C::kSB) * 128);
+        for (int pp = 0; pp < C::kKP; ++pp) {
+          const uint32_t L = jt == 0 ? (uint32_t)pp
+                                     : (uint32_t)(C::kKP + (jt - 1) * (C::kKP + C::kVP) + pp);
+          const uint32_t slot = L % C::kPairs;
+          if (!mbar_wait_warp(&pfull_k[slot], (rpar >> slot) & 1u, ab)) {
+            ok = false;
+            return;
+          }
+          rpar ^= 1u << slot;
+          tc_fence_after();
+          const uint64_t kb = rdesc + (uint64_t)((slot * 2 * kSlotBytes) >> 4);
+          if (elect_sync()) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const uint64_t qa = qdesc + (uint64_t)((2 * pp + c) * (kSlotBytes >> 4));
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_ss(d, qa + 2 * k, kb + (uint64_t)(c * (kSlotBytes >> 4)) + 2 * k, idesc_s,
+                       (pp | c | k) ? 1u : 0u);
+            }
+            mma_commit(&pempty[slot]);
+            if (pp == C::kKP - 1) mma_commit(&s_full[jt % C::kSB]);
+          }
+          __syncwarp();
+        }
+      };
+      auto issue_pv_pr = [&](int jt) {
+        if (!mbar_wait_warp(&p_full[jt % C::kSB], (jt / C::kSB) & 1u, ab)) {
+          ok = false;
+          return;
+        }
+        const uint32_t pa = tmem + (uint32_t)((jt % C::kSB) * 128);
+        for (int pp = 0; pp < C::kVP; ++pp) {
+          const uint32_t L = (uint32_t)(C::kKP + jt * (C::kKP + C::kVP) +
+                                        (jt + 1 < n_kv ? C::kKP : 0) + pp);
+          const uint32_t slot = L % C::kPairs;
+          if (!mbar_wait_warp(&pfull_v[slot], (rpar >> slot) & 1u, ab)) {
+            ok = false;
+            return;
+          }
+          rpar ^= 1u << slot;
+          tc_fence_after();
+          const uint64_t vb = rdesc_mn + (uint64_t)((slot * 2 * kSlotBytes) >> 4);
+          if (elect_sync()) {  // O columns [128 pp, 128 pp + 128) += P V_pair
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tmem + C::kTmemO + pp * 128, pa + k * 8, vb + k * 128, idesc_o2,
+                     (jt > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&pempty[slot]);
+            if (pp == C::kVP - 1) mma_commit(&o_done[jt % C::kSB]);
+          }
+          __syncwarp();
+        }
+      };
       if (s_role) {
         for (int jt = 0; jt < n_kv && ok; ++jt) {
           // S buffer jt%kSB last held P(jt-kSB): wait until PV(jt-kSB) has read it
           if (jt >= C::kSB &&
               !mbar_wait_warp(&o_done[jt % C::kSB], ((jt - C::kSB) / C::kSB) & 1u, ab))
             break;
-          issue_s(jt);
+          if constexpr (C::kPR) issue_s_pr(jt); else issue_s(jt);
         }
       } else {
-        for (int jt = 0; jt < n_kv && ok; ++jt) issue_pv(jt);
+        for (int jt = 0; jt < n_kv && ok; ++jt) {
+          if constexpr (C::kPR) issue_pv_pr(jt); else issue_pv(jt);
+        }
       }
       uint64_t* drain = s_role ? &drain_bar : &drain_bar2;
       if (elect_sync()) {
