@@ -115,10 +115,15 @@ cudaError_t launch_pre(const PreParams& p, bool bf16, int num_sms, cudaStream_t 
 
 // ----------------------------------------------------------------- LSE merge
 // One warp per (row, head).  Lane q fetches the LSE of parts q and q + 32 at
-// this row (-inf where a part does not cover it), so all of a row's LSE loads
-// are in flight at once; the maximum and the sum of exp(LSE_p - max) are warp
-// reductions.  The O parts are then read as 16-byte loads, lane = 4 value
-// columns, with each part's weight exp(LSE_p - LSE) broadcast by a shuffle.
+// this row (-inf where a part does not cover it); the maximum and the sum of
+// exp(LSE_p - max) are warp reductions.  The O rows of the covering parts are
+// loaded (16-byte loads, lane = 4 value columns) together with the LSE, eight
+// parts at a time, so a row costs one round trip to memory rather than two;
+// each part's weight exp(LSE_p - LSE) is broadcast by a shuffle, and a part
+// whose weight is 0 (LSE = -inf, or not covering the row) is left out of the
+// sum, so a NaN in its O never reaches the result.
+constexpr int kMergeGroup = 8;
+
 __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ MergeParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t total = p.rows * p.heads;
@@ -128,48 +133,59 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
     const int64_t r = w / p.heads;
     const int h = (int)(w % p.heads);
     float l[2] = {-INFINITY, -INFINITY};
-    int64_t lr[2] = {0, 0};
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int q = lane + 32 * u;
       if (q < p.n) {
         const int64_t x = r - p.row0[q];
-        if (x >= 0 && x < p.nrows[q]) {
-          lr[u] = x;
-          l[u] = p.lse[q][(int64_t)h * p.nrows[q] + x];
-        }
+        if (x >= 0 && x < p.nrows[q]) l[u] = p.lse[q][(int64_t)h * p.nrows[q] + x];
       }
     }
-    float m = fmaxf(l[0], l[1]);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float sum = (l[0] == -INFINITY ? 0.0f : __expf(l[0] - m)) +
-                (l[1] == -INFINITY ? 0.0f : __expf(l[1] - m));
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float lse = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
-    if (lane == 0) p.lse_out[(int64_t)h * p.rows + r] = lse;
-    // weight of each part (0 for -inf parts and parts not covering the row)
-    const float a[2] = {l[0] == -INFINITY ? 0.0f : __expf(l[0] - lse),
-                        l[1] == -INFINITY ? 0.0f : __expf(l[1] - lse)};
+    float lse = -INFINITY, a0 = 0.0f, a1 = 0.0f;  // a0/a1: weights of parts lane, lane + 32
+    bool have_lse = false;
     for (int c0 = 0; c0 < p.dv; c0 += 128) {
       const int c = c0 + lane * 4;
       const bool act = c < p.dv;
+      // O of every covering part, issued before the LSE values are used
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int q = 0; q < p.n; ++q) {
-        const int u = q >> 5;
-        const float aq = __shfl_sync(0xffffffffu, u ? a[1] : a[0], q & 31);
-        const int64_t xq = __shfl_sync(0xffffffffu, u ? lr[1] : lr[0], q & 31);
-        if (aq != 0.0f && act) {
-          const float4 v =
-              *reinterpret_cast<const float4*>(p.o[q] + (xq * p.heads + h) * (int64_t)p.dv + c);
-          acc.x = fmaf(aq, v.x, acc.x);
-          acc.y = fmaf(aq, v.y, acc.y);
-          acc.z = fmaf(aq, v.z, acc.z);
-          acc.w = fmaf(aq, v.w, acc.w);
+      for (int g0 = 0; g0 < p.n; g0 += kMergeGroup) {
+        float4 v[kMergeGroup];
+#pragma unroll
+        for (int t = 0; t < kMergeGroup; ++t) {
+          const int q = g0 + t;
+          v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (q < p.n && act) {
+            const int64_t x = r - p.row0[q];
+            if (x >= 0 && x < p.nrows[q])
+              v[t] = *reinterpret_cast<const float4*>(p.o[q] + (x * p.heads + h) * (int64_t)p.dv + c);
+          }
+        }
+        if (!have_lse) {  // the weights, once per row (the LSE loads are in flight too)
+          float m = fmaxf(l[0], l[1]);
+#pragma unroll
+          for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          float sum = (l[0] == -INFINITY ? 0.0f : __expf(l[0] - m)) +
+                      (l[1] == -INFINITY ? 0.0f : __expf(l[1] - m));
+#pragma unroll
+          for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          lse = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
+          a0 = l[0] == -INFINITY ? 0.0f : __expf(l[0] - lse);
+          a1 = l[1] == -INFINITY ? 0.0f : __expf(l[1] - lse);
+          have_lse = true;
+        }
+#pragma unroll
+        for (int t = 0; t < kMergeGroup; ++t) {
+          const int q = g0 + t;
+          const float aq = __shfl_sync(0xffffffffu, q < 32 ? a0 : a1, q & 31);
+          if (aq != 0.0f) {  // warp-uniform; -inf parts (and non-covering ones) skipped
+            acc.x = fmaf(aq, v[t].x, acc.x);
+            acc.y = fmaf(aq, v[t].y, acc.y);
+            acc.z = fmaf(aq, v[t].z, acc.z);
+            acc.w = fmaf(aq, v[t].w, acc.w);
+          }
         }
       }
+      if (c0 == 0 && lane == 0) p.lse_out[(int64_t)h * p.rows + r] = lse;
       if (!act) continue;
       const int64_t off = (r * p.heads + h) * (int64_t)p.dv + c;
       if (p.out_kind == 2) {
