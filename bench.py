@@ -383,53 +383,34 @@ def main():
     clocks = clk.summary()
 
     # ---- end to end through host buffers (pinned), copies inside the timed region.
-    # Every step uploads its inputs from pinned host memory and downloads all
-    # of its outputs (O, LSE, dQ, dK, dV); the steps are pipelined over two
-    # device buffer sets, uploads on one copy stream and downloads on another,
-    # so step s+1's upload and step s-1's download overlap step s's compute.
+    # Every step is one attn_fwd_bwd_host call of the C ABI: it uploads the
+    # step's inputs from pinned host memory into a device arena, runs the
+    # forward and backward there and downloads all outputs (O, LSE, dQ, dK,
+    # dV) into host memory.  Consecutive steps alternate between two streams
+    # with an arena each, so one step's copies overlap the other's kernels.
     host_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
     outs0 = (o, lse, dq, dk, dv)
     host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs0]
                 for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
-    dev_in = [[torch.empty_like(t) for t in (q, k, v, do)] for _ in range(2)]
-    dev_out = [[torch.empty_like(t) for t in outs0] for _ in range(2)]
-    e2e_ws = [(torch.empty_like(fws), torch.empty_like(bws)) for _ in range(2)]
-    up_st, down_st = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    hkw = dict(kw)
+    if w.is_thd:  # host metadata for the host-buffer call
+        hkw.update(cu_seqlens_q=inp["cu_seqlens"], cu_seqlens_k=inp["cu_seqlens"])
+    h_o, h_lse, h_dq, h_dk, h_dv = host_out[0]
+    arena_bytes = attn.host_arena_size(*host_in, h_o, h_dq, h_dk, h_dv, **hkw)
+    arenas = [torch.empty(arena_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    e2e_st = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
 
     def e2e_run(n):
         cur = torch.cuda.current_stream()
-        up_st.wait_stream(cur)
-        down_st.wait_stream(cur)
-        done, copied = [None] * n, [None] * n
+        for st_ in e2e_st:
+            st_.wait_stream(cur)
         for s_ in range(n):
-            bset = s_ % 2
-            if s_ >= 2:  # buffer set bset is free once step s_-2 computed and downloaded
-                up_st.wait_event(done[s_ - 2])
-            with torch.cuda.stream(up_st):
-                for d_, h_ in zip(dev_in[bset], host_in):
-                    d_.copy_(h_, non_blocking=True)
-            up = torch.cuda.Event()
-            up.record(up_st)
-            cur.wait_event(up)
-            if s_ >= 2:
-                cur.wait_event(copied[s_ - 2])
-            qi, ki, vi, doi = dev_in[bset]
-            oo, ll, gq, gk, gv = dev_out[bset]
-            fw, bw = e2e_ws[bset]
-            attn.fwd(qi, ki, vi, out=oo, lse=ll, workspace=fw, **kw)
-            attn.bwd(qi, ki, vi, oo, doi, ll, dq=gq, dk=gk, dv=gv, workspace=bw, **kw)
-            done[s_] = torch.cuda.Event()
-            done[s_].record(cur)
-            down_st.wait_event(done[s_])
-            with torch.cuda.stream(down_st):
-                for h_, d_ in zip(host_out[bset], dev_out[bset]):
-                    h_.copy_(d_, non_blocking=True)
-            copied[s_] = torch.cuda.Event()
-            copied[s_].record(down_st)
-        cur.wait_stream(up_st)
-        cur.wait_stream(down_st)
+            attn.fwd_bwd_host(*host_in, *host_out[s_ % 2], arenas[s_ % 2], stream=e2e_st[s_ % 2],
+                              **hkw)
+        for st_ in e2e_st:
+            cur.wait_stream(st_)
 
     # enough steps that the unoverlapped first upload and last download
     # (about 7 ms each at the host link's rate) weigh little per step
@@ -446,9 +427,17 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dev)
+    for a_ in arenas:  # device-detected problems: forward, then backward status word
+        attn.query_status(a_)
+        attn.query_status(a_[256:])
 
     # the same host copies alone (no kernels): the host link's rate, each
     # direction on its own and both at once, to read the e2e figure against
+    del arenas
+    dev_in = [[torch.empty_like(t) for t in (q, k, v, do)]]
+    dev_out = [[torch.empty_like(t) for t in outs0]]
+    up_st, down_st = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
     def copy_run(up, down, n=3):
         cur = torch.cuda.current_stream()
         up_st.wait_stream(cur)
@@ -475,7 +464,7 @@ def main():
         torch.cuda.synchronize()
         nbytes = 3 * ((h2d if up else 0) + (d2h if down else 0))
         copy_gbs[name] = nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
-    del dev_in, dev_out, e2e_ws
+    del dev_in, dev_out
 
     # ---- one-GPU context-parallel ring emulation (dual chunk swap, 8 ranks)
     cp_obj = None
@@ -641,9 +630,10 @@ def main():
         "e2e": {"value": job_tflops(fl["total"], e2e_ms, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "copy_only_gbs": copy_gbs,
-                "note": "public API on inputs uploaded from pinned host memory and all outputs "
-                        "downloaded every step, pipelined over two device buffer sets; "
-                        "copy_only_gbs: the same copies alone (h2d, d2h, both at once)"},
+                "note": "C ABI attn_fwd_bwd_host per step: inputs uploaded from pinned host "
+                        "memory, forward + backward, all outputs downloaded; steps alternate "
+                        "between two streams with a device arena each; copy_only_gbs: the "
+                        "same copies alone (h2d, d2h, both at once)"},
         "gpu_launches": launches,
         "clocks": clocks,
         "cp_emulation": cp_obj,

@@ -31,7 +31,7 @@ EXPORTED = ["attn_fwd_workspace_size", "attn_bwd_workspace_size", "attn_fwd", "a
             "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkdv", "attn_bwd_noalloc",
             "attn_lse_merge", "attn_cp_relayout",
             "attn_query_status", "attn_last_error", "attn_last_launch_count",
-            "attn_debug_inject"]
+            "attn_debug_inject", "attn_host_arena_size", "attn_fwd_bwd_host"]
 # attn_debug_inject kernel bits (test only)
 DEBUG_FWD, DEBUG_DQ, DEBUG_DKDV, DEBUG_SCORES = 1, 2, 4, 8
 
@@ -108,6 +108,10 @@ def load():
         lib.attn_last_launch_count.restype = ctypes.c_int
         lib.attn_debug_inject.argtypes = [ctypes.c_uint, ctypes.c_int, ctypes.c_uint64]
         lib.attn_debug_inject.restype = None
+        lib.attn_host_arena_size.argtypes = [P]
+        lib.attn_host_arena_size.restype = sz
+        lib.attn_fwd_bwd_host.argtypes = [P] + [vp] * 9 + [vp, sz, vp]
+        lib.attn_fwd_bwd_host.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -285,6 +289,38 @@ def bwd_noalloc(q, k, v, o, dout, lse, *, causal=True, scale=None, window=(-1, -
     _check(lib.attn_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
                                 _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
     return dq, dk, dv
+
+
+def _host_params(q, k, v, dout, o, dq, dk, dv, kw):
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout), ("o", o), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+    return make_params(q, k, v, o=o, dout=dout, dq=dq, dk=dk, dv=dv, o_dtype=o.dtype,
+                       grad_dtype=dq.dtype, **kw)
+
+
+def host_arena_size(q, k, v, dout, o, dq, dk, dv, **kw):
+    """Bytes of device arena attn_fwd_bwd_host needs for these host tensors."""
+    p = _host_params(q, k, v, dout, o, dq, dk, dv, kw)
+    return load().attn_host_arena_size(ctypes.byref(p))
+
+
+def fwd_bwd_host(q, k, v, dout, o, lse, dq, dk, dv, arena, *, stream=None, **kw):
+    """attn_fwd_bwd_host: one forward + backward step whose inputs (q, k, v,
+    dout) and outputs (o, lse, dq, dk, dv) are HOST tensors (pinned for the
+    copies to overlap); ``arena`` is a device uint8 tensor of at least
+    host_arena_size() bytes.  THD ``cu_seqlens_q/k`` (and ``seqused_q/k``) in
+    ``kw`` are host int32 tensors too.  Enqueued on ``stream``; the outputs are
+    valid once it has passed the call."""
+    lib = load()
+    if lse.is_cuda or not arena.is_cuda:
+        raise ValueError("lse must be a host tensor and arena a device tensor")
+    p = _host_params(q, k, v, dout, o, dq, dk, dv, kw)
+    _check(lib.attn_fwd_bwd_host(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                 _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(arena),
+                                 arena.numel(), _stream(stream)))
+    return o, lse, dq, dk, dv
 
 
 def workspace_size(kind, q, k, v, **kw):

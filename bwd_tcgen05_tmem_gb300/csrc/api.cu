@@ -591,6 +591,174 @@ attn_status_t attn_bwd_noalloc(const attn_params_t* p, const void* q, const void
                   kStageAll);
 }
 
+}  // extern "C"
+
+// ----------------------------------------------------------------- attn_fwd_bwd_host
+// One step from host buffers: every tensor is copied into the caller's device
+// arena, the forward and backward run there, and the results are copied back,
+// all in order on the caller's stream.  The arena holds each tensor with the
+// layout (strides) the caller gave for its host copy.
+namespace {
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Bytes from a tensor's base to the end of its last element.
+size_t tensor_bytes(const int64_t s[3], const attn_params_t* p, bool is_q, int heads, int d,
+                    size_t es) {
+  return (size_t)span_of(nullptr, s, p, is_q, heads, d, es).hi;
+}
+
+size_t lse_bytes(const attn_params_t* p) {
+  int64_t sb = 0, sh = 0;
+  lse_strides(p, sb, sh);
+  const int64_t rows = thd(p) ? p->total_q : p->seqlen_q;
+  const int64_t nb = thd(p) ? 1 : p->batch;
+  if (rows <= 0 || nb <= 0 || p->heads_q <= 0) return 0;
+  return (size_t)(((nb - 1) * sb + (int64_t)(p->heads_q - 1) * sh + rows) * 4);
+}
+
+struct HostArena {
+  // byte offsets into the arena, and the bytes each tensor spans
+  size_t fws, bws, off[9], bytes[9], cu_q, cu_k, used_q, used_k, total;
+};
+enum { kQ, kK, kV, kDo, kO, kLse, kDq, kDk, kDv };
+
+HostArena host_arena(const attn_params_t* p) {
+  HostArena a;
+  memset(&a, 0, sizeof(a));
+  const size_t g = esize(p->grad_dtype);
+  a.bytes[kQ] = tensor_bytes(p->stride_q, p, true, p->heads_q, p->d_qk, 2);
+  a.bytes[kK] = tensor_bytes(p->stride_k, p, false, p->heads_kv, p->d_qk, 2);
+  a.bytes[kV] = tensor_bytes(p->stride_v, p, false, p->heads_kv, p->d_v, 2);
+  a.bytes[kDo] = tensor_bytes(p->stride_do, p, true, p->heads_q, p->d_v, 2);
+  a.bytes[kO] = tensor_bytes(p->stride_o, p, true, p->heads_q, p->d_v, esize(p->o_dtype));
+  a.bytes[kLse] = lse_bytes(p);
+  a.bytes[kDq] = tensor_bytes(p->stride_dq, p, true, p->heads_q, p->d_qk, g);
+  a.bytes[kDk] = tensor_bytes(p->stride_dk, p, false, p->heads_kv, p->d_qk, g);
+  a.bytes[kDv] = tensor_bytes(p->stride_dv, p, false, p->heads_kv, p->d_v, g);
+  size_t at = 0;
+  a.fws = at;
+  at += up256(attn_fwd_workspace_size(p));
+  a.bws = at;
+  at += up256(attn_bwd_workspace_size(p));
+  for (int i = 0; i < 9; ++i) {
+    a.off[i] = at;
+    at += up256(a.bytes[i]);
+  }
+  if (thd(p)) {
+    const size_t cu = (size_t)(p->batch + 1) * 4, used = (size_t)p->batch * 4;
+    a.cu_q = at;
+    at += up256(cu);
+    a.cu_k = at;
+    at += up256(cu);
+    if (p->seqused_q) {
+      a.used_q = at;
+      at += up256(used);
+      a.used_k = at;
+      at += up256(used);
+    }
+  }
+  a.total = at;
+  return a;
+}
+
+// The caller's buffers must be host memory: a device pointer here is a mix-up.
+attn_status_t check_host(const char* name, const void* ptr) {
+  if (!ptr) return ATTN_OK;
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // older drivers flag unregistered host memory; it is fine here
+    return ATTN_OK;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
+    return fail(ATTN_ERR_INVALID_ARG, "%s is device memory; attn_fwd_bwd_host takes host buffers",
+                name);
+  return ATTN_OK;
+}
+
+attn_status_t copy(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind,
+                   cudaStream_t st, const char* what) {
+  if (!bytes) return ATTN_OK;
+  const cudaError_t e = cudaMemcpyAsync(dst, src, bytes, kind, st);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, what);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_host_arena_size(const attn_params_t* p) {
+  if (!p || check_params(p)) return 0;
+  return host_arena(p).total;
+}
+
+attn_status_t attn_fwd_bwd_host(const attn_params_t* p, const void* q, const void* k,
+                                const void* v, const void* dout, void* o, float* lse, void* dq,
+                                void* dk, void* dv, void* arena, size_t arena_bytes,
+                                attn_stream_t stream) {
+  g_err[0] = 0;
+  g_launches = 0;
+  attn_status_t s = check_params(p);
+  if (s) return s;
+  const HostArena a = host_arena(p);
+  if (!arena) return fail(ATTN_ERR_WORKSPACE, "arena is NULL");
+  if ((uintptr_t)arena % 256) return fail(ATTN_ERR_ALIGNMENT, "arena is not 256-byte aligned");
+  if (arena_bytes < a.total)
+    return fail(ATTN_ERR_WORKSPACE, "arena too small (%zu < %zu)", arena_bytes, a.total);
+  const void* host_in[4] = {q, k, v, dout};
+  void* host_out[5] = {o, lse, dq, dk, dv};
+  static const char* const names[9] = {"q", "k", "v", "dout", "o", "lse", "dq", "dk", "dv"};
+  for (int i = 0; i < 9; ++i) {
+    const void* h = i < 4 ? host_in[i] : host_out[i - 4];
+    if (a.bytes[i] && !h) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", names[i]);
+    if ((s = check_host(names[i], h))) return s;
+  }
+  if ((s = check_host("cu_seqlens_q", p->cu_seqlens_q))) return s;
+  if ((s = check_host("seqused_q", p->seqused_q))) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  char* base = (char*)arena;
+  // the device copy of the parameters: same shape and strides, device metadata
+  attn_params_t pd = *p;
+  if (thd(p)) {
+    const size_t cu = (size_t)(p->batch + 1) * 4, used = (size_t)p->batch * 4;
+    if ((s = copy(base + a.cu_q, p->cu_seqlens_q, cu, cudaMemcpyHostToDevice, st, "cu_seqlens_q")) ||
+        (s = copy(base + a.cu_k, p->cu_seqlens_k, cu, cudaMemcpyHostToDevice, st, "cu_seqlens_k")))
+      return s;
+    pd.cu_seqlens_q = (const int32_t*)(base + a.cu_q);
+    pd.cu_seqlens_k = (const int32_t*)(base + a.cu_k);
+    if (p->seqused_q) {
+      if ((s = copy(base + a.used_q, p->seqused_q, used, cudaMemcpyHostToDevice, st, "seqused_q")) ||
+          (s = copy(base + a.used_k, p->seqused_k, used, cudaMemcpyHostToDevice, st, "seqused_k")))
+        return s;
+      pd.seqused_q = (const int32_t*)(base + a.used_q);
+      pd.seqused_k = (const int32_t*)(base + a.used_k);
+    }
+  }
+  for (int i = 0; i < 4; ++i)
+    if ((s = copy(base + a.off[i], host_in[i], a.bytes[i], cudaMemcpyHostToDevice, st, names[i])))
+      return s;
+  if (p->accumulate)  // the gradients are summed into the caller's values
+    for (int i = kDq; i <= kDv; ++i)
+      if ((s = copy(base + a.off[i], host_out[i - 4], a.bytes[i], cudaMemcpyHostToDevice, st,
+                    names[i])))
+        return s;
+  s = attn_fwd(&pd, base + a.off[kQ], base + a.off[kK], base + a.off[kV], base + a.off[kO],
+               (float*)(base + a.off[kLse]), base + a.fws, a.bws - a.fws, stream);
+  if (s) return s;
+  const int fwd_launches = g_launches;
+  s = attn_bwd(&pd, base + a.off[kQ], base + a.off[kK], base + a.off[kV], base + a.off[kO],
+               base + a.off[kDo], (const float*)(base + a.off[kLse]), base + a.off[kDq],
+               base + a.off[kDk], base + a.off[kDv], base + a.bws, a.off[0] - a.bws, stream);
+  g_launches += fwd_launches;
+  if (s) return s;
+  for (int i = kO; i <= kDv; ++i)
+    if ((s = copy(host_out[i - 4], base + a.off[i], a.bytes[i], cudaMemcpyDeviceToHost, st,
+                  names[i])))
+      return s;
+  return ATTN_OK;
+}
+
 attn_status_t attn_lse_merge(int n_parts, const float* const* o_parts,
                              const float* const* lse_parts, const int64_t* part_row0,
                              const int64_t* part_rows, int64_t rows, int heads, int d_v,

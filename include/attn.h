@@ -200,6 +200,40 @@ attn_status_t attn_bwd_noalloc(const attn_params_t* p, const void* q, const void
                                void* dq, void* dk, void* dv, attn_stream_t stream);
 
 /*
+ * One forward + backward step from HOST buffers (a deployment aid with no
+ * counterpart on the attention pages: the end-to-end path of a caller whose
+ * tensors live in host memory).
+ *
+ * q, k, v, dout (inputs) and o, lse, dq, dk, dv (outputs) are HOST pointers,
+ * laid out with the strides, dtypes and LSE layout that `p` gives, exactly as
+ * attn_fwd / attn_bwd would take them on the device; for THD inputs
+ * p->cu_seqlens_q/k (and seqused_q/k) are HOST arrays here too.  On `stream`,
+ * in order: every input is copied into `arena` (one cudaMemcpyAsync per
+ * tensor, the span from its base to its last element), attn_fwd and attn_bwd
+ * run there, and O, LSE, dQ, dK, dV are copied back.  With p->accumulate the
+ * host dq/dk/dv are uploaded first and the gradients are added to them.
+ *
+ * arena: caller-owned DEVICE memory, 256-byte aligned, at least
+ * attn_host_arena_size(p) bytes: the forward's workspace (its first 256 bytes),
+ * then the backward's, then the device copies of all nine tensors.  So
+ * attn_query_status(arena) reports device-detected problems of the forward and
+ * attn_query_status((char*)arena + 256) those of the backward.  The call
+ * returns once the work is enqueued.  Host buffers should be pinned (cudaHostAlloc / cudaHostRegister)
+ * for the copies to be asynchronous; the inputs must not change and the
+ * outputs must not be read until the stream has passed the call.  Two calls on
+ * two streams with two arenas overlap one step's copies with the other's
+ * kernels.  A device pointer among the buffers is refused with
+ * ATTN_ERR_INVALID_ARG.  Results are identical to attn_fwd + attn_bwd on the
+ * device copies.  attn_host_arena_size returns 0 for parameters that
+ * attn_fwd / attn_bwd would refuse.
+ */
+size_t attn_host_arena_size(const attn_params_t* p);
+attn_status_t attn_fwd_bwd_host(const attn_params_t* p, const void* q, const void* k,
+                                const void* v, const void* dout, void* o, float* lse, void* dq,
+                                void* dk, void* dv, void* arena, size_t arena_bytes,
+                                attn_stream_t stream);
+
+/*
  * LSE-weighted merge of partial attention results over disjoint key sets
  * (PR #3527: the context-parallel ring correction exponentiates LSE
  * differences):  LSE = ln sum_p exp(LSE_p),  O = sum_p exp(LSE_p - LSE) O_p,

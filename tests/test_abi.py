@@ -196,3 +196,42 @@ def test_d256_backward_route_by_block_bytes(lib, s, window, wide):
             blocks = b * hq * sum(min(qt, (1023 + 127) // 128 + 1) if qt > 8 else qt + 1
                                   for qt in range(nq))
         assert need == blk_off + blocks * 65536
+
+
+def host_step_params():
+    q, k, v = fake((2, 256, 4, 128)), fake((2, 256, 2, 128)), fake((2, 256, 2, 128))
+    o, do = fake((2, 256, 4, 128)), fake((2, 256, 4, 128))
+    dq, dk, dv = (fake(t.shape, torch.float32) for t in (q, k, v))
+    return attn.make_params(q, k, v, o=o, dout=do, dq=dq, dk=dk, dv=dv,
+                            grad_dtype=torch.float32), (q, k, v, do, o, dq, dk, dv)
+
+
+def test_host_arena_size_is_workspaces_plus_tensor_copies(lib):
+    """attn_fwd_bwd_host's arena: forward workspace, backward workspace, then
+    the nine tensors, each rounded up to 256 bytes (include/attn.h)."""
+    p, ts = host_step_params()
+    up = lambda x: (x + 255) // 256 * 256
+    nbytes = [t.numel() * t.element_size() for t in ts]  # contiguous: span = numel
+    lse = 2 * 4 * 256 * 4
+    want = (up(lib.attn_fwd_workspace_size(ctypes.byref(p))) +
+            up(lib.attn_bwd_workspace_size(ctypes.byref(p))) + sum(up(b) for b in nbytes) + up(lse))
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) == 256  # status word at arena + 0
+    assert lib.attn_host_arena_size(ctypes.byref(p)) == want
+    bad, _ = host_step_params()
+    bad.d_qk = 96
+    assert lib.attn_host_arena_size(ctypes.byref(bad)) == 0
+
+
+def test_host_step_refuses_bad_arena(lib):
+    p, _ = host_step_params()
+    need = lib.attn_host_arena_size(ctypes.byref(p))
+
+    def call(arena, nbytes):
+        ptrs = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(9)]
+        return lib.attn_fwd_bwd_host(ctypes.byref(p), *ptrs, ctypes.c_void_p(arena), nbytes, None)
+
+    assert call(0, need) == 4
+    assert call(0x7000100, need - 1) == 4
+    assert call(0x7000010, need) == 3
+    p.heads_kv = 3
+    assert call(0x7000100, need) == 1
