@@ -124,7 +124,7 @@ cudaError_t launch_pre(const PreParams& p, bool bf16, int num_sms, cudaStream_t 
 // sum, so a NaN in its O never reaches the result.
 constexpr int kMergeGroup = 8;
 
-__global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ MergeParams p) {
+__global__ void __launch_bounds__(256, 4) attn_merge_kernel(const __grid_constant__ MergeParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t total = p.rows * p.heads;
   const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
