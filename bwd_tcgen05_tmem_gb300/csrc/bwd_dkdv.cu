@@ -382,8 +382,8 @@ __global__ void __launch_bounds__(384, 1)
           dd = p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok];
           if (l2 == -INFINITY) l2 = INFINITY;  // keyless query row: masked anyway
         }
-        s_lse2[st][t] = l2;
-        s_d[st][t] = dd;
+        s_lse2[st][t] = -l2;  // negated: the softmax adds them
+        s_d[st][t] = -dd;
       }
       mbar_arrive(&ld_full[st]);
     }
@@ -439,27 +439,37 @@ __global__ void __launch_bounds__(384, 1)
       const float4* l4 = reinterpret_cast<const float4*>(&s_lse2[st][col0]);
       const float4* d4 = reinterpret_cast<const float4*>(&s_d[st][col0]);
       uint32_t pp[C::kHalf / 2], pd[C::kHalf / 2];
+      // P = exp2(s * scale * log2 e - LSE log2 e), dS = P (dP - D), two columns
+      // per packed FP32 operation (shared memory holds -LSE log2 e and -D; the
+      // softmax warps are bound by instruction issue)
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
       for (int t4 = 0; t4 < C::kHalf / 4; ++t4) {
         const float4 la = l4[t4];
-        const float lz[4] = {la.x, la.y, la.z, la.w};
-        float dz[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t nl[2] = {f2_pack(la.x, la.y), f2_pack(la.z, la.w)};
+        uint64_t nd[2] = {0ull, 0ull};
         if constexpr (C::kDK) {
           const float4 da = d4[t4];
-          dz[0] = da.x; dz[1] = da.y; dz[2] = da.z; dz[3] = da.w;
+          nd[0] = f2_pack(da.x, da.y);
+          nd[1] = f2_pack(da.z, da.w);
         }
 #pragma unroll
         for (int u = 0; u < 4; u += 2) {
           const int t = 4 * t4 + u;
-          float e0 = ex2(fmaf(s[t], sl2, -lz[u]));
-          float e1 = ex2(fmaf(s[t + 1], sl2, -lz[u + 1]));
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[t], s[t + 1]), sl2x2, nl[u / 2]), x0, x1);
+          float e0 = ex2(x0);
+          float e1 = ex2(x1);
           if (!full_tile) {
             if (t < lo || t > hi) e0 = 0.0f;
             if (t + 1 < lo || t + 1 > hi) e1 = 0.0f;
           }
           if constexpr (C::kDV) pp[t / 2] = Pack<BF16>::two(e0, e1);
-          if constexpr (C::kDK)
-            pd[t / 2] = Pack<BF16>::two(e0 * (dp[t] - dz[u]), e1 * (dp[t + 1] - dz[u + 1]));
+          if constexpr (C::kDK) {
+            float g0, g1;
+            f2_unpack(f2_mul(f2_pack(e0, e1), f2_add(f2_pack(dp[t], dp[t + 1]), nd[u / 2])), g0, g1);
+            pd[t / 2] = Pack<BF16>::two(g0, g1);
+          }
         }
       }
       mbar_arrive(&ld_empty[st]);
