@@ -436,47 +436,68 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
         for (int t = 0; t < 128; ++t)
           if (t < lo || t > hi) s[t] = -INFINITY;
       }
-      // row maximum as 8 independent chains (one warp per sub-partition has
-      // no other warp to hide a 128-long dependency chain), two elements per
-      // three-input max: the softmax warps are bound by instruction issue
-      float mxv[8];
+      // exp2(s * scale * log2 e - m) and the row sum in packed pairs (eight
+      // sum chains, element t into chain t % 8, as four pairs); P is stored
+      // into the first half of the S buffer
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      auto exps = [&](float neg_m) -> float {
+        const uint64_t negm2 = f2_pack(neg_m, neg_m);
+        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mxv[u] = s[u];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-      for (int t = 8; t < 120; t += 16)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) mxv[u] = fmax3(mxv[u], s[t + u], s[t + 8 + u]);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mxv[u] = fmaxf(mxv[u], s[120 + u]);
-      const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
-                             fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
-      const float m_tile = mx * sl2;
-      const bool grow = m_tile > m_run + 8.0f;
-      const float m_new = grow ? m_tile : m_run;
-      const float alpha = grow ? ex2(m_run - m_new) : 1.0f;
-      m_run = m_new;
-      const float neg_m = (m_run == -INFINITY) ? 0.0f : -m_run;
-      // exp2(s * scale * log2 e - m) and the row sum in packed pairs: eight
-      // sum chains (element t into chain t % 8), as four pairs
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * t], s[c * 32 + 2 * t + 1]), sl2x2, negm2), x0, x1);
-          const float e0 = ex2(x0), e1 = ex2(x1);
-          acc2[t & 3] = f2_add(acc2[t & 3], f2_pack(e0, e1));
-          pk[t] = Pack<BF16>::two(e0, e1);
+          for (int t = 0; t < 16; ++t) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * t], s[c * 32 + 2 * t + 1]), sl2x2, negm2),
+                      x0, x1);
+            const float e0 = ex2(x0), e1 = ex2(x1);
+            acc2[t & 3] = f2_add(acc2[t & 3], f2_pack(e0, e1));
+            pk[t] = Pack<BF16>::two(e0, e1);
+          }
+          tmem_st16(sb + c * 16, pk);
         }
-        tmem_st16(sb + c * 16, pk);
-      }
-      float rsv[8];
+        float rsv[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) f2_unpack(acc2[u], rsv[2 * u], rsv[2 * u + 1]);
-      const float rs = ((rsv[0] + rsv[1]) + (rsv[2] + rsv[3])) + ((rsv[4] + rsv[5]) + (rsv[6] + rsv[7]));
+        for (int u = 0; u < 4; ++u) f2_unpack(acc2[u], rsv[2 * u], rsv[2 * u + 1]);
+        return ((rsv[0] + rsv[1]) + (rsv[2] + rsv[3])) + ((rsv[4] + rsv[5]) + (rsv[6] + rsv[7]));
+      };
+      // The softmax warps are bound by instruction issue, so the tile's row
+      // maximum is computed only when needed: against the running maximum a
+      // row sum of at most 2^7 bounds every exponential by 2^7, so the maximum
+      // has not grown by the 2^8 that triggers a rescale, and P and the sum
+      // are exactly what the full computation gives.  Otherwise (a row's
+      // first keys, or a larger sum in any row of the warp) the warp computes
+      // the maximum and the exponentials again.
+      float rs = 0.0f, alpha = 1.0f;
+      bool grow = false;
+      bool need_max = __any_sync(0xffffffffu, m_run == -INFINITY);
+      if (!need_max) {
+        rs = exps(-m_run);
+        need_max = __any_sync(0xffffffffu, !(rs <= 128.0f));
+      }
+      if (need_max) {
+        // row maximum as 8 independent chains (one warp per sub-partition has
+        // no other warp to hide a 128-long dependency chain), two elements per
+        // three-input max
+        float mxv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mxv[u] = s[u];
+#pragma unroll
+        for (int t = 8; t < 120; t += 16)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mxv[u] = fmax3(mxv[u], s[t + u], s[t + 8 + u]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mxv[u] = fmaxf(mxv[u], s[120 + u]);
+        const float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
+                               fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
+        const float m_tile = mx * sl2;
+        grow = m_tile > m_run + 8.0f;
+        const float m_new = grow ? m_tile : m_run;
+        alpha = grow ? ex2(m_run - m_new) : 1.0f;
+        m_run = m_new;
+        rs = exps((m_run == -INFINITY) ? 0.0f : -m_run);
+      }
       l_run = l_run * alpha + rs;
       // rescale O rows whose maximum grew (after PV(jt-1) has finished)
       if (__any_sync(0xffffffffu, grow && jt > 0)) {
