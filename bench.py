@@ -383,11 +383,12 @@ def main():
     clocks = clk.summary()
 
     # ---- end to end through host buffers (pinned), copies inside the timed region.
-    # Every step is one attn_fwd_bwd_host call of the C ABI: it uploads the
-    # step's inputs from pinned host memory into a device arena, runs the
-    # forward and backward there and downloads all outputs (O, LSE, dQ, dK,
-    # dV) into host memory.  Consecutive steps alternate between two streams
-    # with an arena each, so one step's copies overlap the other's kernels.
+    # Every step runs attn_fwd_bwd_host_stages of the C ABI in its three stages:
+    # upload the step's inputs from pinned host memory into a device arena,
+    # forward + backward there, download all outputs (O, LSE, dQ, dK, dV) into
+    # host memory.  Uploads, compute and downloads have a stream each, ordered
+    # by events, with two arenas: step s+1 uploads and step s-1 downloads while
+    # step s computes, and the compute of consecutive steps stays in order.
     host_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
     outs0 = (o, lse, dq, dk, dv)
     host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs0]
@@ -400,16 +401,29 @@ def main():
     h_o, h_lse, h_dq, h_dk, h_dv = host_out[0]
     arena_bytes = attn.host_arena_size(*host_in, h_o, h_dq, h_dk, h_dv, **hkw)
     arenas = [torch.empty(arena_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
-    e2e_st = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    up_s, comp_s, down_s = (torch.cuda.Stream(device=dev) for _ in range(3))
 
     def e2e_run(n):
         cur = torch.cuda.current_stream()
-        for st_ in e2e_st:
+        for st_ in (up_s, comp_s, down_s):
             st_.wait_stream(cur)
+        ev = [[torch.cuda.Event() for _ in range(3)] for _ in range(n)]  # up, compute, down
         for s_ in range(n):
-            attn.fwd_bwd_host(*host_in, *host_out[s_ % 2], arenas[s_ % 2], stream=e2e_st[s_ % 2],
-                              **hkw)
-        for st_ in e2e_st:
+            a_ = s_ % 2
+            args = (*host_in, *host_out[a_], arenas[a_])
+            if s_ >= 2:  # arena a_: step s_-2 has read its inputs
+                up_s.wait_event(ev[s_ - 2][1])
+            attn.fwd_bwd_host(*args, stream=up_s, stages=attn.HOST_UPLOAD, **hkw)
+            ev[s_][0].record(up_s)
+            comp_s.wait_event(ev[s_][0])
+            if s_ >= 2:  # and its outputs are downloaded
+                comp_s.wait_event(ev[s_ - 2][2])
+            attn.fwd_bwd_host(*args, stream=comp_s, stages=attn.HOST_COMPUTE, **hkw)
+            ev[s_][1].record(comp_s)
+            down_s.wait_event(ev[s_][1])
+            attn.fwd_bwd_host(*args, stream=down_s, stages=attn.HOST_DOWNLOAD, **hkw)
+            ev[s_][2].record(down_s)
+        for st_ in (up_s, comp_s, down_s):
             cur.wait_stream(st_)
 
     # enough steps that the unoverlapped first upload and last download
@@ -436,7 +450,7 @@ def main():
     del arenas
     dev_in = [[torch.empty_like(t) for t in (q, k, v, do)]]
     dev_out = [[torch.empty_like(t) for t in outs0]]
-    up_st, down_st = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    up_st, down_st = up_s, down_s
 
     def copy_run(up, down, n=3):
         cur = torch.cuda.current_stream()
@@ -643,10 +657,11 @@ def main():
         "e2e": {"value": job_tflops(fl["total"], e2e_ms, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "copy_only_gbs": copy_gbs,
-                "note": "C ABI attn_fwd_bwd_host per step: inputs uploaded from pinned host "
-                        "memory, forward + backward, all outputs downloaded; steps alternate "
-                        "between two streams with a device arena each; copy_only_gbs: the "
-                        "same copies alone (h2d, d2h, both at once)"},
+                "note": "C ABI attn_fwd_bwd_host_stages per step: inputs uploaded from "
+                        "pinned host memory, forward + backward, all outputs downloaded; "
+                        "upload, compute and download streams ordered by events over two "
+                        "device arenas; copy_only_gbs: the same copies alone (h2d, d2h, "
+                        "both at once)"},
         "gpu_launches": launches,
         "clocks": clocks,
         "cp_emulation": cp_obj,

@@ -31,7 +31,10 @@ EXPORTED = ["attn_fwd_workspace_size", "attn_bwd_workspace_size", "attn_fwd", "a
             "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkdv", "attn_bwd_noalloc",
             "attn_lse_merge", "attn_cp_relayout",
             "attn_query_status", "attn_last_error", "attn_last_launch_count",
-            "attn_debug_inject", "attn_host_arena_size", "attn_fwd_bwd_host"]
+            "attn_debug_inject", "attn_host_arena_size", "attn_fwd_bwd_host",
+            "attn_fwd_bwd_host_stages"]
+# attn_fwd_bwd_host_stages stage bits
+HOST_UPLOAD, HOST_COMPUTE, HOST_DOWNLOAD, HOST_ALL = 1, 2, 4, 7
 # attn_debug_inject kernel bits (test only)
 DEBUG_FWD, DEBUG_DQ, DEBUG_DKDV, DEBUG_SCORES = 1, 2, 4, 8
 
@@ -112,6 +115,8 @@ def load():
         lib.attn_host_arena_size.restype = sz
         lib.attn_fwd_bwd_host.argtypes = [P] + [vp] * 9 + [vp, sz, vp]
         lib.attn_fwd_bwd_host.restype = ctypes.c_int
+        lib.attn_fwd_bwd_host_stages.argtypes = [P] + [vp] * 9 + [vp, sz, ctypes.c_uint, vp]
+        lib.attn_fwd_bwd_host_stages.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -306,20 +311,26 @@ def host_arena_size(q, k, v, dout, o, dq, dk, dv, **kw):
     return load().attn_host_arena_size(ctypes.byref(p))
 
 
-def fwd_bwd_host(q, k, v, dout, o, lse, dq, dk, dv, arena, *, stream=None, **kw):
+def fwd_bwd_host(q, k, v, dout, o, lse, dq, dk, dv, arena, *, stream=None, stages=HOST_ALL,
+                 **kw):
     """attn_fwd_bwd_host: one forward + backward step whose inputs (q, k, v,
     dout) and outputs (o, lse, dq, dk, dv) are HOST tensors (pinned for the
     copies to overlap); ``arena`` is a device uint8 tensor of at least
     host_arena_size() bytes.  THD ``cu_seqlens_q/k`` (and ``seqused_q/k``) in
     ``kw`` are host int32 tensors too.  Enqueued on ``stream``; the outputs are
-    valid once it has passed the call."""
+    valid once it has passed the call.  ``stages``: a mask of HOST_UPLOAD,
+    HOST_COMPUTE and HOST_DOWNLOAD (attn_fwd_bwd_host_stages) to run part of
+    the step, e.g. to pipeline consecutive steps over several streams."""
     lib = load()
     if lse.is_cuda or not arena.is_cuda:
         raise ValueError("lse must be a host tensor and arena a device tensor")
     p = _host_params(q, k, v, dout, o, dq, dk, dv, kw)
-    _check(lib.attn_fwd_bwd_host(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
-                                 _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(arena),
-                                 arena.numel(), _stream(stream)))
+    args = (ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(o), _ptr(lse),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(arena), arena.numel())
+    if stages == HOST_ALL:
+        _check(lib.attn_fwd_bwd_host(*args, _stream(stream)))
+    else:
+        _check(lib.attn_fwd_bwd_host_stages(*args, int(stages), _stream(stream)))
     return o, lse, dq, dk, dv
 
 

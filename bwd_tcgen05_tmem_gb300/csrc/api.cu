@@ -693,70 +693,96 @@ size_t attn_host_arena_size(const attn_params_t* p) {
   return host_arena(p).total;
 }
 
-attn_status_t attn_fwd_bwd_host(const attn_params_t* p, const void* q, const void* k,
-                                const void* v, const void* dout, void* o, float* lse, void* dq,
-                                void* dk, void* dv, void* arena, size_t arena_bytes,
-                                attn_stream_t stream) {
+attn_status_t attn_fwd_bwd_host_stages(const attn_params_t* p, const void* q, const void* k,
+                                       const void* v, const void* dout, void* o, float* lse,
+                                       void* dq, void* dk, void* dv, void* arena,
+                                       size_t arena_bytes, unsigned stages, attn_stream_t stream) {
   g_err[0] = 0;
   g_launches = 0;
   attn_status_t s = check_params(p);
   if (s) return s;
+  if (!stages || (stages & ~7u)) return fail(ATTN_ERR_INVALID_ARG, "stages must be a mask of 1, 2, 4");
   const HostArena a = host_arena(p);
   if (!arena) return fail(ATTN_ERR_WORKSPACE, "arena is NULL");
   if ((uintptr_t)arena % 256) return fail(ATTN_ERR_ALIGNMENT, "arena is not 256-byte aligned");
   if (arena_bytes < a.total)
     return fail(ATTN_ERR_WORKSPACE, "arena too small (%zu < %zu)", arena_bytes, a.total);
+  const bool up = stages & ATTN_HOST_UPLOAD, run = stages & ATTN_HOST_COMPUTE,
+             down = stages & ATTN_HOST_DOWNLOAD;
   const void* host_in[4] = {q, k, v, dout};
   void* host_out[5] = {o, lse, dq, dk, dv};
   static const char* const names[9] = {"q", "k", "v", "dout", "o", "lse", "dq", "dk", "dv"};
   for (int i = 0; i < 9; ++i) {
+    // inputs are read by the upload; outputs written by the download (and the
+    // gradients read by the upload when they are accumulated)
+    const bool used = i < 4 ? up : (down || (up && p->accumulate && i >= kDq));
+    if (!used) continue;
     const void* h = i < 4 ? host_in[i] : host_out[i - 4];
     if (a.bytes[i] && !h) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", names[i]);
     if ((s = check_host(names[i], h))) return s;
   }
-  if ((s = check_host("cu_seqlens_q", p->cu_seqlens_q))) return s;
-  if ((s = check_host("seqused_q", p->seqused_q))) return s;
+  if (up) {
+    if ((s = check_host("cu_seqlens_q", p->cu_seqlens_q))) return s;
+    if ((s = check_host("seqused_q", p->seqused_q))) return s;
+  }
   cudaStream_t st = (cudaStream_t)stream;
   char* base = (char*)arena;
-  // the device copy of the parameters: same shape and strides, device metadata
-  attn_params_t pd = *p;
-  if (thd(p)) {
-    const size_t cu = (size_t)(p->batch + 1) * 4, used = (size_t)p->batch * 4;
-    if ((s = copy(base + a.cu_q, p->cu_seqlens_q, cu, cudaMemcpyHostToDevice, st, "cu_seqlens_q")) ||
-        (s = copy(base + a.cu_k, p->cu_seqlens_k, cu, cudaMemcpyHostToDevice, st, "cu_seqlens_k")))
-      return s;
-    pd.cu_seqlens_q = (const int32_t*)(base + a.cu_q);
-    pd.cu_seqlens_k = (const int32_t*)(base + a.cu_k);
-    if (p->seqused_q) {
-      if ((s = copy(base + a.used_q, p->seqused_q, used, cudaMemcpyHostToDevice, st, "seqused_q")) ||
-          (s = copy(base + a.used_k, p->seqused_k, used, cudaMemcpyHostToDevice, st, "seqused_k")))
+  if (up) {
+    if (thd(p)) {
+      const size_t cu = (size_t)(p->batch + 1) * 4, used = (size_t)p->batch * 4;
+      if ((s = copy(base + a.cu_q, p->cu_seqlens_q, cu, cudaMemcpyHostToDevice, st, "cu_seqlens_q")) ||
+          (s = copy(base + a.cu_k, p->cu_seqlens_k, cu, cudaMemcpyHostToDevice, st, "cu_seqlens_k")))
         return s;
-      pd.seqused_q = (const int32_t*)(base + a.used_q);
-      pd.seqused_k = (const int32_t*)(base + a.used_k);
+      if (p->seqused_q &&
+          ((s = copy(base + a.used_q, p->seqused_q, used, cudaMemcpyHostToDevice, st, "seqused_q")) ||
+           (s = copy(base + a.used_k, p->seqused_k, used, cudaMemcpyHostToDevice, st, "seqused_k"))))
+        return s;
     }
+    for (int i = 0; i < 4; ++i)
+      if ((s = copy(base + a.off[i], host_in[i], a.bytes[i], cudaMemcpyHostToDevice, st, names[i])))
+        return s;
+    if (p->accumulate)  // the gradients are summed into the caller's values
+      for (int i = kDq; i <= kDv; ++i)
+        if ((s = copy(base + a.off[i], host_out[i - 4], a.bytes[i], cudaMemcpyHostToDevice, st,
+                      names[i])))
+          return s;
   }
-  for (int i = 0; i < 4; ++i)
-    if ((s = copy(base + a.off[i], host_in[i], a.bytes[i], cudaMemcpyHostToDevice, st, names[i])))
-      return s;
-  if (p->accumulate)  // the gradients are summed into the caller's values
-    for (int i = kDq; i <= kDv; ++i)
-      if ((s = copy(base + a.off[i], host_out[i - 4], a.bytes[i], cudaMemcpyHostToDevice, st,
+  if (run) {
+    // the device copy of the parameters: same shape and strides, the
+    // metadata arrays in the arena
+    attn_params_t pd = *p;
+    if (thd(p)) {
+      pd.cu_seqlens_q = (const int32_t*)(base + a.cu_q);
+      pd.cu_seqlens_k = (const int32_t*)(base + a.cu_k);
+      if (p->seqused_q) {
+        pd.seqused_q = (const int32_t*)(base + a.used_q);
+        pd.seqused_k = (const int32_t*)(base + a.used_k);
+      }
+    }
+    s = attn_fwd(&pd, base + a.off[kQ], base + a.off[kK], base + a.off[kV], base + a.off[kO],
+                 (float*)(base + a.off[kLse]), base + a.fws, a.bws - a.fws, stream);
+    if (s) return s;
+    const int fwd_launches = g_launches;
+    s = attn_bwd(&pd, base + a.off[kQ], base + a.off[kK], base + a.off[kV], base + a.off[kO],
+                 base + a.off[kDo], (const float*)(base + a.off[kLse]), base + a.off[kDq],
+                 base + a.off[kDk], base + a.off[kDv], base + a.bws, a.off[0] - a.bws, stream);
+    g_launches += fwd_launches;
+    if (s) return s;
+  }
+  if (down)
+    for (int i = kO; i <= kDv; ++i)
+      if ((s = copy(host_out[i - 4], base + a.off[i], a.bytes[i], cudaMemcpyDeviceToHost, st,
                     names[i])))
         return s;
-  s = attn_fwd(&pd, base + a.off[kQ], base + a.off[kK], base + a.off[kV], base + a.off[kO],
-               (float*)(base + a.off[kLse]), base + a.fws, a.bws - a.fws, stream);
-  if (s) return s;
-  const int fwd_launches = g_launches;
-  s = attn_bwd(&pd, base + a.off[kQ], base + a.off[kK], base + a.off[kV], base + a.off[kO],
-               base + a.off[kDo], (const float*)(base + a.off[kLse]), base + a.off[kDq],
-               base + a.off[kDk], base + a.off[kDv], base + a.bws, a.off[0] - a.bws, stream);
-  g_launches += fwd_launches;
-  if (s) return s;
-  for (int i = kO; i <= kDv; ++i)
-    if ((s = copy(host_out[i - 4], base + a.off[i], a.bytes[i], cudaMemcpyDeviceToHost, st,
-                  names[i])))
-      return s;
   return ATTN_OK;
+}
+
+attn_status_t attn_fwd_bwd_host(const attn_params_t* p, const void* q, const void* k,
+                                const void* v, const void* dout, void* o, float* lse, void* dq,
+                                void* dk, void* dv, void* arena, size_t arena_bytes,
+                                attn_stream_t stream) {
+  return attn_fwd_bwd_host_stages(p, q, k, v, dout, o, lse, dq, dk, dv, arena, arena_bytes,
+                                  ATTN_HOST_ALL, stream);
 }
 
 attn_status_t attn_lse_merge(int n_parts, const float* const* o_parts,

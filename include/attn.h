@@ -234,6 +234,25 @@ attn_status_t attn_fwd_bwd_host(const attn_params_t* p, const void* q, const voi
                                 attn_stream_t stream);
 
 /*
+ * attn_fwd_bwd_host in stages, for callers that pipeline consecutive steps:
+ * `stages` is a mask of ATTN_HOST_UPLOAD (the host inputs, metadata and, with
+ * accumulate, the host gradients into the arena), ATTN_HOST_COMPUTE (attn_fwd
+ * and attn_bwd on the arena's copies) and ATTN_HOST_DOWNLOAD (O, LSE, dQ, dK,
+ * dV back to host memory); ATTN_HOST_ALL is attn_fwd_bwd_host.  Each stage
+ * enqueues on `stream`, so a caller can upload step s+1 on one stream while
+ * step s computes on another and step s-1 downloads on a third, ordering
+ * them with its own events; one arena must not be uploaded into while its
+ * previous step still computes or downloads.  The same parameters (shape,
+ * strides, flags) must be passed to every stage of one step; the buffers a
+ * stage does not touch may be NULL.
+ */
+enum { ATTN_HOST_UPLOAD = 1, ATTN_HOST_COMPUTE = 2, ATTN_HOST_DOWNLOAD = 4, ATTN_HOST_ALL = 7 };
+attn_status_t attn_fwd_bwd_host_stages(const attn_params_t* p, const void* q, const void* k,
+                                       const void* v, const void* dout, void* o, float* lse,
+                                       void* dq, void* dk, void* dv, void* arena,
+                                       size_t arena_bytes, unsigned stages, attn_stream_t stream);
+
+/*
  * LSE-weighted merge of partial attention results over disjoint key sets
  * (PR #3527: the context-parallel ring correction exponentiates LSE
  * differences):  LSE = ln sum_p exp(LSE_p),  O = sum_p exp(LSE_p - LSE) O_p,

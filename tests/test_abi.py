@@ -235,3 +235,12 @@ def test_host_step_refuses_bad_arena(lib):
     assert call(0x7000010, need) == 3
     p.heads_kv = 3
     assert call(0x7000100, need) == 1
+
+
+def test_host_stages_mask_validated(lib):
+    p, _ = host_step_params()
+    need = lib.attn_host_arena_size(ctypes.byref(p))
+    ptrs = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(9)]
+    for bad in (0, 8, 15):
+        assert lib.attn_fwd_bwd_host_stages(ctypes.byref(p), *ptrs, ctypes.c_void_p(0x7000100),
+                                            need, bad, None) == 1

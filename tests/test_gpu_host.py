@@ -160,3 +160,37 @@ def test_device_pointer_refused():
                                ctypes.c_void_p(arena.data_ptr()), need, None)
     assert rc == 1
     assert b"device memory" in lib.attn_last_error()
+
+
+def test_staged_pipeline_equals_one_call():
+    """attn_fwd_bwd_host_stages: upload, compute and download of consecutive
+    steps on three streams, ordered by events over two arenas (the pipeline
+    the benchmark's end-to-end leg runs), give the one-call results."""
+    b, s, hq, hkv = 1, 300, 4, 2
+    q, k, v, do = inputs((b, s, hq, 192), (b, s, hkv, 192), 128, torch.bfloat16)
+    ref = host_outputs(q, k, v, torch.bfloat16, lse_shape=(b, hq, s))
+    run_host(q, k, v, do, ref, causal=True)
+    outs = [host_outputs(q, k, v, torch.bfloat16, lse_shape=(b, hq, s)) for _ in range(2)]
+    need = attn.host_arena_size(q, k, v, do, ref[0], *ref[2:], causal=True)
+    arenas = [torch.empty(need, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    up, comp, down = (torch.cuda.Stream() for _ in range(3))
+    n = 4
+    ev = [[torch.cuda.Event() for _ in range(3)] for _ in range(n)]
+    for i in range(n):
+        a = i % 2
+        args = (q, k, v, do, *outs[a], arenas[a])
+        if i >= 2:
+            up.wait_event(ev[i - 2][1])
+        attn.fwd_bwd_host(*args, stream=up, stages=attn.HOST_UPLOAD, causal=True)
+        ev[i][0].record(up)
+        comp.wait_event(ev[i][0])
+        if i >= 2:
+            comp.wait_event(ev[i - 2][2])
+        attn.fwd_bwd_host(*args, stream=comp, stages=attn.HOST_COMPUTE, causal=True)
+        ev[i][1].record(comp)
+        down.wait_event(ev[i][1])
+        attn.fwd_bwd_host(*args, stream=down, stages=attn.HOST_DOWNLOAD, causal=True)
+        ev[i][2].record(down)
+    torch.cuda.synchronize()
+    for o_ in outs:
+        assert_same(o_, ref)
