@@ -9,8 +9,8 @@
 // and finally dQ *= scale.  No atomics: every dQ element is written once, so
 // the result is bitwise reproducible.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// S/dP issuer, warp 2 dQ issuer, warps 4..11 two softmax warpgroups; warpgroup w owns key
+// Warp roles (352 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// S/dP issuer, warp 2 dQ issuer, warps 3..10 two softmax warpgroups; warpgroup w owns key
 // columns [w*BKV/2, (w+1)*BKV/2) of every tile (the backward needs no row
 // reduction, so splitting columns is free).  The softmax signals "scores
 // consumed" right after loading S/dP so the next tile's S/dP MMAs overlap the
@@ -52,8 +52,14 @@ struct DqCfg {
   static_assert(DQK <= 256, "one MMA covers the dQ columns");
 };
 
+// Eleven warps: no idle fourth warp, so each thread may hold 184 registers
+// (65536 / 352) instead of 168, which the softmax's 64 scores, 64 dP values and
+// packed dS need to keep several exponentials in flight.
+constexpr int kDqThreads = 352;
+
 template <int DQK, int DV, int BKV, bool BF16, bool G_F32>
-__global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_constant__ DqParams p) {
+__global__ void __launch_bounds__(kDqThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ DqParams p) {
   using C = DqCfg<DQK, DV, BKV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -269,10 +275,11 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dq_kernel(const __grid_consta
       }
       __syncwarp();
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 3) {
     // ------------------------------------------------------------ softmax / dS
-    const int wq = (warp - 4) & 3;
-    const int wg = (warp - 4) >> 2;
+    // warps 3..10; a warp reads and writes the TMEM lanes of its sub-partition
+    const int wq = warp & 3;
+    const int wg = (warp - 3) >> 2;
     const int r = wq * 32 + (threadIdx.x & 31);
     const int i = q0 + r;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -430,7 +437,7 @@ static cudaError_t launch_dq_t(const DqParams& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   dim3 grid = tile_major(p.n_qtiles) ? dim3((unsigned)p.n_qtiles, (unsigned)p.hq, (unsigned)p.batch)
                                       : dim3((unsigned)p.hq, (unsigned)p.n_qtiles, (unsigned)p.batch);
-  k<<<grid, 384, C::kSmem, st>>>(p);
+  k<<<grid, kDqThreads, C::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 
