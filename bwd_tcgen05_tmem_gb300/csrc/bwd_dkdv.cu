@@ -102,9 +102,6 @@ __global__ void __launch_bounds__(384, 1)
   const Seq sq = load_seq(p.geo, b);
   const int k0 = ktile * kBlockM;
   if (k0 >= sq.lk) return;
-  if (threadIdx.x == 0) skip_sh = (p.status && *(volatile int*)p.status) ? 1 : 0;
-  __syncthreads();
-  if (skip_sh) return;
   long long i0, i1;
   query_range(sq, k0, min(k0 + kBlockM, sq.lk) - 1, i0, i1);
   const int qt0 = (i1 >= i0) ? (int)(i0 / BQ) : 0;
@@ -115,6 +112,10 @@ __global__ void __launch_bounds__(384, 1)
   const int drop = dropped_load(p.dbg);
   Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
+    // a failed device check or an earlier abort stops every CTA; the status
+    // word is tested only once the barriers are set up and the resident K and
+    // V copies are under way (tensor-map copies stay in bounds regardless)
+    const int status = p.status ? *(volatile int*)p.status : 0;
     abort_flag = 0;
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&sfull[i], 1);
@@ -136,6 +137,19 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&ld_empty[s], 256);
     }
     fence_barrier_init();
+    if (n_it > 0) {
+      int c1, c2, c3, v1, v2, v3;
+      map_coords(p.ok, 0, g, sq.k_start + k0, tb, c1, c2, c3);
+      map_coords(p.ov, 0, g, sq.k_start + k0, tb, v1, v2, v3);
+      mbar_arrive_tx(&kv_bar, (C::kKSlots + C::kVSlots) * kSlotBytes);
+      for (int c = 0; c < C::kKSlots; ++c)
+        tma_load_4d(sK + c * kSlotBytes, &p.tm_k, &kv_bar, c * 64, c1, c2, c3);
+      if (C::kDK) {
+        for (int c = 0; c < C::kVSlots; ++c)
+          tma_load_4d(sV + c * kSlotBytes, &p.tm_v, &kv_bar, c * 64, v1, v2, v3);
+      }
+    }
+    skip_sh = status != 0;
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, 512);
@@ -144,26 +158,18 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  if (skip_sh) {  // let the resident copies land, free TMEM, leave
+    if (threadIdx.x == 0 && n_it > 0) mbar_wait_quiet(&kv_bar, 0, lim);
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    return;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // per query tile: the ring chunks (score-only operand), then the stage
-    // the whole warp runs the loop (indices stay warp-uniform); one elected
-    // lane issues the copies
+    // (K and V were issued with the barrier set-up); the whole warp runs the
+    // loop (indices stay warp-uniform); one elected lane issues the copies
     if (n_it > 0) {
-      int c1, c2, c3, v1, v2, v3;
-      map_coords(p.ok, 0, g, sq.k_start + k0, tb, c1, c2, c3);
-      map_coords(p.ov, 0, g, sq.k_start + k0, tb, v1, v2, v3);
-      if (elect_sync()) {
-        mbar_arrive_tx(&kv_bar, (C::kKSlots + C::kVSlots) * kSlotBytes);
-        for (int c = 0; c < C::kKSlots; ++c)
-          tma_load_4d(sK + c * kSlotBytes, &p.tm_k, &kv_bar, c * 64, c1, c2, c3);
-        if (C::kDK) {
-          for (int c = 0; c < C::kVSlots; ++c)
-            tma_load_4d(sV + c * kSlotBytes, &p.tm_v, &kv_bar, c * 64, v1, v2, v3);
-        }
-      }
-      __syncwarp();
       uint32_t rcnt = 0;
       int it = 0;
       bool ok = true;

@@ -85,9 +85,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const Seq sq = load_seq(p.geo, b);
   const int q0 = tile * kBlockM;
   if (q0 >= sq.lq) return;
-  if (threadIdx.x == 0) skip_sh = (p.status && *(volatile int*)p.status) ? 1 : 0;
-  __syncthreads();
-  if (skip_sh) return;
   long long j0, j1;
   key_range(sq, q0, min(q0 + kBlockM, sq.lq) - 1, j0, j1);
   const int kt0 = (j1 >= j0) ? (int)(j0 / BKV) : 0;
@@ -97,6 +94,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int drop = dropped_load(p.dbg);
   Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
+    // a failed device check or an earlier abort stops every CTA; the status
+    // word is tested only once the barriers are set up and the resident Q and
+    // dO copies are under way (tensor-map copies stay in bounds regardless)
+    const int status = p.status ? *(volatile int*)p.status : 0;
     abort_flag = 0;
     for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&kfull[i], 1);
@@ -114,6 +115,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&drain_bar, 1);
     mbar_init(&drain_bar2, 1);
     fence_barrier_init();
+    if (n_kv > 0) {
+      int c1, c2, c3, o1, o2, o3;
+      map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
+      map_coords(p.odo, 0, h, sq.q_start + q0, tb, o1, o2, o3);
+      mbar_arrive_tx(&q_bar, (C::kQSlots + C::kDoSlots) * kSlotBytes);
+      for (int c = 0; c < C::kQSlots; ++c)
+        tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
+      for (int c = 0; c < C::kDoSlots; ++c)
+        tma_load_4d(sDo + c * kSlotBytes, &p.tm_do, &q_bar, c * 64, o1, o2, o3);
+    }
+    skip_sh = status != 0;
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, 512);
@@ -122,24 +134,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  if (skip_sh) {  // let the resident copies land, free TMEM, leave
+    if (threadIdx.x == 0 && n_kv > 0) mbar_wait_quiet(&q_bar, 0, lim);
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    return;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // per key tile: V chunks (ring), then the K stage
-    // the whole warp runs the loop (indices stay warp-uniform); one elected
-    // lane issues the copies
+    // per key tile: V chunks (ring), then the K stage (Q and dO were issued
+    // with the barrier set-up); the whole warp runs the loop (indices stay
+    // warp-uniform); one elected lane issues the copies
     if (n_kv > 0) {
-      int c1, c2, c3, o1, o2, o3;
-      map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
-      map_coords(p.odo, 0, h, sq.q_start + q0, tb, o1, o2, o3);
-      if (elect_sync()) {
-        mbar_arrive_tx(&q_bar, (C::kQSlots + C::kDoSlots) * kSlotBytes);
-        for (int c = 0; c < C::kQSlots; ++c)
-          tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
-        for (int c = 0; c < C::kDoSlots; ++c)
-          tma_load_4d(sDo + c * kSlotBytes, &p.tm_do, &q_bar, c * 64, o1, o2, o3);
-      }
-      __syncwarp();
       uint32_t vcnt = 0;
       int jt = 0;
       bool ok = true;

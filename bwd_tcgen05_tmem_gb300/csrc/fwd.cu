@@ -89,10 +89,6 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   const Seq sq = load_seq(p.geo, b);
   const int q0 = tile * kBlockM;
   if (q0 >= sq.lq) return;  // tile past the end of this sequence (uniform)
-  // a failed device check (cu_seqlens) or an earlier abort stops every CTA
-  if (threadIdx.x == 0) skip_sh = (p.status && *(volatile int*)p.status) ? 1 : 0;
-  __syncthreads();
-  if (skip_sh) return;
   long long j0, j1;
   key_range(sq, q0, min(q0 + kBlockM, sq.lq) - 1, j0, j1);
   const int kt0 = (j1 >= j0) ? (int)(j0 / kBlockN) : 0;
@@ -102,6 +98,11 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   const int drop = dropped_load(p.dbg);
   Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
+    // A failed device check (cu_seqlens) or an earlier abort stops every CTA.
+    // The status word is loaded first and tested only after the barriers are
+    // set up and Q's copy is under way: Q heads the critical path, and a
+    // tensor-map copy stays in bounds whatever the sequence metadata says.
+    const int status = p.status ? *(volatile int*)p.status : 0;
     abort_flag = 0;
     for (int i = 0; i < C::kKRing; ++i) {
       mbar_init(&kfull[i], 1);
@@ -125,6 +126,17 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
     mbar_init(&drain_bar, 1);
     mbar_init(&drain_bar2, 1);
     fence_barrier_init();
+    if (n_kv > 0) {
+      int c1, c2, c3;
+      map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_tx(&q_bar, C::kQSlots * kSlotBytes);
+      for (int c = 0; c < C::kQSlots; ++c)
+        tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
+    }
+    skip_sh = status != 0;
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, 512);
@@ -133,24 +145,18 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  if (skip_sh) {  // let Q's copy land, free TMEM, leave
+    if (threadIdx.x == 0 && n_kv > 0) mbar_wait_quiet(&q_bar, 0, lim);
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    return;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // load order = MMA order: K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1)
-    // the whole warp runs the loop (indices stay warp-uniform); one elected
-    // lane issues the copies
+    // (Q was issued with the barrier set-up); the whole warp runs the loop
+    // (indices stay warp-uniform); one elected lane issues the copies
     if (n_kv > 0) {
-      int c1, c2, c3;
-      map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
-      if (elect_sync()) {
-        tma_prefetch_desc(&p.tm_q);
-        tma_prefetch_desc(&p.tm_k);
-        tma_prefetch_desc(&p.tm_v);
-        mbar_arrive_tx(&q_bar, C::kQSlots * kSlotBytes);
-        for (int c = 0; c < C::kQSlots; ++c)
-          tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
-      }
-      __syncwarp();
       uint32_t kcnt = 0;
       int vcnt = 0;
       bool ok = true;
