@@ -70,6 +70,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_lau
     dq.scale_log2 = a.scale_log2;
     dq.status = a.status;
     dq.dbg = a.dbg_dq;
+    dq.n_ctas = a.num_sms;
     if (dq.n_qtiles > 65535 || a.batch > 65535 || a.hq > 65535) return cudaErrorInvalidValue;
     if ((e = launch_dq(dq, a.dqk, a.dv, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
     ++*n_launches;

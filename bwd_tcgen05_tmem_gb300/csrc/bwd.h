@@ -125,6 +125,7 @@ struct DqParams {
   int64_t sdq_b, sdq_t, sdq_h;
   int accum;
   int batch, hq, hkv, n_qtiles;
+  int n_ctas;  // persistent grid: CTAs that share the work items
   float scale, scale_log2;
   int* status;
   DebugInject dbg;

@@ -69,34 +69,60 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint8_t* sV = sK + C::kKStages * C::kKStage;
 
   __shared__ uint64_t kfull[C::kKStages], kempty[C::kKStages], vfull[C::kVRing], vempty[C::kVRing];
-  __shared__ uint64_t q_bar, sdp_full, sc_free, ds_full, dq_done, drain_bar, drain_bar2;
+  __shared__ uint64_t q_bar, q_free, sdp_full, sc_free, ds_full, dq_done, drain_bar, drain_bar2;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, skip_sh;
 
   const int warp = threadIdx.x >> 5;
-  // (query tile, head) in the grid order of tile_major(); heaviest tiles first
+  // Persistent: the work items, in the order the one-CTA-per-item grid had
+  // (heaviest query tiles first: with tile_major(), x walks the query tiles
+  // of a head, y the heads, z the batch; otherwise x walks the heads), are
+  // dealt to the CTAs in rounds, every other round in reverse CTA order, so
+  // each CTA's heavy and light items even out.  Every role decodes the same
+  // items, and the barrier phases run on across items, so the next item's
+  // Q/dO loads and first S/dP MMAs overlap this item's last tiles and
+  // epilogue.
   const bool tmaj = tile_major(p.n_qtiles);
-  const int h = tmaj ? blockIdx.y : blockIdx.x;
-  const int tile = p.n_qtiles - 1 - (tmaj ? blockIdx.x : blockIdx.y);
-  const int b = blockIdx.z;
-  const int tb = p.geo.cu_q ? 0 : b;  // TMA batch coordinate (packed THD tensors have one)
-  const int g = h / (p.hq / p.hkv);
-
-  const Seq sq = load_seq(p.geo, b);
-  const int q0 = tile * kBlockM;
-  if (q0 >= sq.lq) return;
-  long long j0, j1;
-  key_range(sq, q0, min(q0 + kBlockM, sq.lq) - 1, j0, j1);
-  const int kt0 = (j1 >= j0) ? (int)(j0 / BKV) : 0;
-  const int n_kv = (j1 >= j0) ? (int)(j1 / BKV) - kt0 + 1 : 0;
+  const int gx = tmaj ? p.n_qtiles : p.hq, gy = tmaj ? p.hq : p.n_qtiles;
+  const int n_items = gx * gy * p.batch;  // the launch checks that it fits
+  const int n_rounds = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
+  // round k's item for this CTA (may be past the end in the last round)
+  auto item_at = [&](int k) {
+    return k * (int)gridDim.x + ((k & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
+  };
+  struct Item {
+    Seq sq;
+    int h, g, b, tb, q0, kt0, n_kv;
+    bool live;  // the query tile lies inside its sequence
+  };
+  auto item = [&](int L) {
+    Item it;
+    const int x = L % gx;
+    const int rest = L / gx;
+    const int y = rest % gy;
+    it.b = rest / gy;
+    it.h = tmaj ? y : x;
+    it.g = it.h / (p.hq / p.hkv);
+    it.tb = p.geo.cu_q ? 0 : it.b;  // TMA batch coordinate (packed THD tensors have one)
+    it.sq = load_seq(p.geo, it.b);
+    it.q0 = (p.n_qtiles - 1 - (tmaj ? x : y)) * kBlockM;
+    it.live = it.q0 < it.sq.lq;
+    it.kt0 = 0;
+    it.n_kv = 0;
+    if (it.live) {
+      long long j0, j1;
+      key_range(it.sq, it.q0, min(it.q0 + kBlockM, it.sq.lq) - 1, j0, j1);
+      it.kt0 = (j1 >= j0) ? (int)(j0 / BKV) : 0;
+      it.n_kv = (j1 >= j0) ? (int)(j1 / BKV) - it.kt0 + 1 : 0;
+    }
+    return it;
+  };
 
   const unsigned long long lim = wait_limit(p.dbg);
   const int drop = dropped_load(p.dbg);
   Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
-    // a failed device check or an earlier abort stops every CTA; the status
-    // word is tested only once the barriers are set up and the resident Q and
-    // dO copies are under way (tensor-map copies stay in bounds regardless)
+    // a failed device check or an earlier abort stops every CTA
     const int status = p.status ? *(volatile int*)p.status : 0;
     abort_flag = 0;
     for (int i = 0; i < C::kKStages; ++i) {
@@ -108,6 +134,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(&vempty[i], 1);
     }
     mbar_init(&q_bar, 1);
+    mbar_init(&q_free, 1);
     mbar_init(&sdp_full, 1);
     mbar_init(&sc_free, 256);
     mbar_init(&ds_full, 256);
@@ -115,16 +142,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&drain_bar, 1);
     mbar_init(&drain_bar2, 1);
     fence_barrier_init();
-    if (n_kv > 0) {
-      int c1, c2, c3, o1, o2, o3;
-      map_coords(p.oq, 0, h, sq.q_start + q0, tb, c1, c2, c3);
-      map_coords(p.odo, 0, h, sq.q_start + q0, tb, o1, o2, o3);
-      mbar_arrive_tx(&q_bar, (C::kQSlots + C::kDoSlots) * kSlotBytes);
-      for (int c = 0; c < C::kQSlots; ++c)
-        tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
-      for (int c = 0; c < C::kDoSlots; ++c)
-        tma_load_4d(sDo + c * kSlotBytes, &p.tm_do, &q_bar, c * 64, o1, o2, o3);
-    }
     skip_sh = status != 0;
   }
   if (warp == 1) {
@@ -134,25 +151,45 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  if (skip_sh) {  // let the resident copies land, free TMEM, leave
-    if (threadIdx.x == 0 && n_kv > 0) mbar_wait_quiet(&q_bar, 0, lim);
+  if (skip_sh) {
     if (warp == 1) tmem_dealloc(tmem, 512);
     return;
   }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // per key tile: V chunks (ring), then the K stage (Q and dO were issued
-    // with the barrier set-up); the whole warp runs the loop (indices stay
-    // warp-uniform); one elected lane issues the copies
-    if (n_kv > 0) {
-      uint32_t vcnt = 0;
-      int jt = 0;
-      bool ok = true;
-      for (; jt < n_kv && ok; ++jt) {
-        const int krow = sq.k_start + (kt0 + jt) * BKV;
+    // per item: Q and dO once their buffers are free (the previous item's
+    // S/dP MMAs have run), then per key tile the V chunks (ring) and the K
+    // stage.  The whole warp runs the loop (indices stay warp-uniform); one
+    // elected lane issues the copies.
+    uint32_t vcnt = 0;
+    int gk = 0, ni = 0;  // K stages and items issued
+    bool ok = true;
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int L = item_at(k);
+      if (L >= n_items) continue;
+      const Item it = item(L);
+      if (!it.live || it.n_kv == 0) continue;
+      if (ni > 0 && !mbar_wait_warp(&q_free, (ni - 1) & 1u, ab)) {
+        ok = false;
+        break;
+      }
+      int c1, c2, c3, o1, o2, o3;
+      map_coords(p.oq, 0, it.h, it.sq.q_start + it.q0, it.tb, c1, c2, c3);
+      map_coords(p.odo, 0, it.h, it.sq.q_start + it.q0, it.tb, o1, o2, o3);
+      if (elect_sync()) {
+        mbar_arrive_tx(&q_bar, (C::kQSlots + C::kDoSlots) * kSlotBytes);
+        for (int c = 0; c < C::kQSlots; ++c)
+          tma_load_4d(sQ + c * kSlotBytes, &p.tm_q, &q_bar, c * 64, c1, c2, c3);
+        for (int c = 0; c < C::kDoSlots; ++c)
+          tma_load_4d(sDo + c * kSlotBytes, &p.tm_do, &q_bar, c * 64, o1, o2, o3);
+      }
+      __syncwarp();
+      ++ni;
+      for (int jt = 0; jt < it.n_kv && ok; ++jt) {
+        const int krow = it.sq.k_start + (it.kt0 + jt) * BKV;
         int d1, d2, d3;
-        map_coords(p.ov, 0, g, krow, tb, d1, d2, d3);
+        map_coords(p.ov, 0, it.g, krow, it.tb, d1, d2, d3);
 #pragma unroll
         for (int c = 0; c < C::kVCh; ++c, ++vcnt) {
           const uint32_t slot = vcnt % C::kVRing;
@@ -167,13 +204,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           __syncwarp();
         }
         if (!ok) break;
-        const int st = jt % C::kKStages;
-        if (!mbar_wait_warp(&kempty[st], ((jt / C::kKStages) & 1) ^ 1, ab)) {
+        const int st = gk % C::kKStages;
+        if (!mbar_wait_warp(&kempty[st], ((gk / C::kKStages) & 1) ^ 1, ab)) {
           ok = false;
           break;
         }
-        map_coords(p.ok, 0, g, krow, tb, d1, d2, d3);
-        if (jt != drop && elect_sync()) {  // drop: test-only injected missing load
+        map_coords(p.ok, 0, it.g, krow, it.tb, d1, d2, d3);
+        if (gk != drop && elect_sync()) {  // drop: test-only injected missing load
           mbar_arrive_tx(&kfull[st], C::kKStage);
 #pragma unroll
           for (int c = 0; c < C::kKCh; ++c)
@@ -181,208 +218,247 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                         d3);
         }
         __syncwarp();
+        ++gk;
       }
-      mbar_wait_quiet(&q_bar, 0, lim);
-      const uint32_t first = vcnt > (uint32_t)C::kVRing ? vcnt - C::kVRing : 0u;
-      for (uint32_t c = first; c < vcnt; ++c)
-        mbar_wait_quiet(&vfull[c % C::kVRing], (c / C::kVRing) & 1u, lim);
-      const int nk = ok ? n_kv : jt;  // K stages issued
-      for (int v = nk > C::kKStages ? nk - C::kKStages : 0; v < nk; ++v)
-        mbar_wait_quiet(&kfull[v % C::kKStages], (v / C::kKStages) & 1, lim);
     }
+    // let every copy still in flight land before the CTA can exit
+    if (ni > 0) mbar_wait_quiet(&q_bar, (ni - 1) & 1u, lim);
+    const uint32_t first = vcnt > (uint32_t)C::kVRing ? vcnt - C::kVRing : 0u;
+    for (uint32_t c = first; c < vcnt; ++c)
+      mbar_wait_quiet(&vfull[c % C::kVRing], (c / C::kVRing) & 1u, lim);
+    for (int v = gk > C::kKStages ? gk - C::kKStages : 0; v < gk; ++v)
+      mbar_wait_quiet(&kfull[v % C::kKStages], (v / C::kKStages) & 1, lim);
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
     // warp 1 issues S and dP, warp 2 issues dQ += dS K: one thread issues a
     // tcgen05.mma about every 60 cycles, so each product gets its own issuer.
     // Each warp runs its loop on all lanes; the elected lane issues the MMAs
-    // and commits.
-    if (n_kv > 0) {
-      const bool sc_role = warp == 1;
-      constexpr uint32_t idesc_s = make_idesc(128, BKV, BF16, false, false);
-      constexpr uint32_t idesc_q = make_idesc(128, DQK, BF16, false, true);
-      const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
-      const uint64_t ddesc = make_sdesc(smem_u32(sDo), 16, 1024);
-      const uint64_t kdesc = make_sdesc(smem_u32(sK), 16, 1024);
-      const uint64_t kdesc_mn = make_sdesc(smem_u32(sK), C::kChunk, 1024);
-      const uint64_t vdesc = make_sdesc(smem_u32(sV), 16, 1024);
-      uint32_t vcnt = 0;
-      bool ok = sc_role ? mbar_wait_warp(&q_bar, 0, ab) : true;
-      tc_fence_after();
-      auto issue_scores = [&](int jt) {
+    // and commits.  gt counts the key tiles of all items of this CTA.
+    const bool sc_role = warp == 1;
+    constexpr uint32_t idesc_s = make_idesc(128, BKV, BF16, false, false);
+    constexpr uint32_t idesc_q = make_idesc(128, DQK, BF16, false, true);
+    const uint64_t qdesc = make_sdesc(smem_u32(sQ), 16, 1024);
+    const uint64_t ddesc = make_sdesc(smem_u32(sDo), 16, 1024);
+    const uint64_t kdesc = make_sdesc(smem_u32(sK), 16, 1024);
+    const uint64_t kdesc_mn = make_sdesc(smem_u32(sK), C::kChunk, 1024);
+    const uint64_t vdesc = make_sdesc(smem_u32(sV), 16, 1024);
+    uint32_t vcnt = 0;
+    int gt = 0, ni = 0;
+    bool ok = true;
+    auto issue_scores = [&]() {
 #pragma unroll
-        for (int c = 0; c < C::kVCh; ++c, ++vcnt) {  // dP = dO V^T
-          const uint32_t slot = vcnt % C::kVRing;
-          if (!mbar_wait_warp(&vfull[slot], (vcnt / C::kVRing) & 1u, ab)) {
-            ok = false;
-            return;
-          }
-          tc_fence_after();
-          const uint64_t da = ddesc + (uint64_t)(c * (kSlotBytes >> 4));
-          const uint64_t vb = vdesc + (uint64_t)(slot * (C::kChunk >> 4));
-          if (elect_sync()) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(tmem + C::kTdP, da + 2 * k, vb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
-            mma_commit(&vempty[slot]);
-          }
-          __syncwarp();
-        }
-        const int st = jt % C::kKStages;  // S = Q K^T
-        if (!mbar_wait_warp(&kfull[st], (jt / C::kKStages) & 1, ab)) {
+      for (int c = 0; c < C::kVCh; ++c, ++vcnt) {  // dP = dO V^T
+        const uint32_t slot = vcnt % C::kVRing;
+        if (!mbar_wait_warp(&vfull[slot], (vcnt / C::kVRing) & 1u, ab)) {
           ok = false;
           return;
         }
         tc_fence_after();
+        const uint64_t da = ddesc + (uint64_t)(c * (kSlotBytes >> 4));
+        const uint64_t vb = vdesc + (uint64_t)(slot * (C::kChunk >> 4));
         if (elect_sync()) {
 #pragma unroll
-          for (int c = 0; c < C::kKCh; ++c) {
-            const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
-            const uint64_t kb = kdesc + (uint64_t)((st * C::kKStage + c * C::kChunk) >> 4);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(tmem, qa + 2 * k, kb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
-          }
-          mma_commit(&sdp_full);
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + C::kTdP, da + 2 * k, vb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+          mma_commit(&vempty[slot]);
         }
         __syncwarp();
-      };
-      auto issue_dq = [&](int jt) {  // dQ += dS K  (K stage read MN-major, N = DQK)
-        const int st = jt % C::kKStages;
-        const uint64_t kb = kdesc_mn + (uint64_t)((st * C::kKStage) >> 4);
-        if (elect_sync()) {
-          mma_ts(tmem + C::kTdQ, tmem + C::kTdS, kb, idesc_q, jt > 0 ? 1u : 0u);
-#pragma unroll
-          for (int k = 1; k < BKV / 16; ++k)
-            mma_ts(tmem + C::kTdQ, tmem + C::kTdS + k * 8, kb + k * 128, idesc_q, 1u);
-          mma_commit(&kempty[st]);
-          mma_commit(&dq_done);
-        }
-        __syncwarp();
-      };
-      if (sc_role) {
-        for (int jt = 0; jt < n_kv && ok; ++jt) {
-          // S/dP of tile jt overwrite those of jt-1: the softmax must hold them
-          if (jt > 0 && !mbar_wait_warp(&sc_free, (jt - 1) & 1u, ab)) break;
-          issue_scores(jt);
-        }
-      } else {
-        for (int jt = 0; jt < n_kv && ok; ++jt) {
-          if (!mbar_wait_warp(&ds_full, jt & 1u, ab)) break;
-          // the K stage of tile jt: loaded (its S MMAs ran), released below
-          if (!mbar_wait_warp(&kfull[jt % C::kKStages], (jt / C::kKStages) & 1, ab)) break;
-          tc_fence_after();
-          issue_dq(jt);
-        }
       }
-      uint64_t* drain = sc_role ? &drain_bar : &drain_bar2;
+      const int st = gt % C::kKStages;  // S = Q K^T
+      if (!mbar_wait_warp(&kfull[st], (gt / C::kKStages) & 1, ab)) {
+        ok = false;
+        return;
+      }
+      tc_fence_after();
       if (elect_sync()) {
-        mma_commit(drain);
-        mbar_wait_quiet(drain, 0, lim);
+#pragma unroll
+        for (int c = 0; c < C::kKCh; ++c) {
+          const uint64_t qa = qdesc + (uint64_t)(c * (kSlotBytes >> 4));
+          const uint64_t kb = kdesc + (uint64_t)((st * C::kKStage + c * C::kChunk) >> 4);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem, qa + 2 * k, kb + 2 * k, idesc_s, (c | k) ? 1u : 0u);
+        }
+        mma_commit(&sdp_full);
       }
       __syncwarp();
+    };
+    auto issue_dq = [&](bool accumulate) {  // dQ += dS K  (K stage read MN-major, N = DQK)
+      const int st = gt % C::kKStages;
+      const uint64_t kb = kdesc_mn + (uint64_t)((st * C::kKStage) >> 4);
+      if (elect_sync()) {
+        mma_ts(tmem + C::kTdQ, tmem + C::kTdS, kb, idesc_q, accumulate ? 1u : 0u);
+#pragma unroll
+        for (int k = 1; k < BKV / 16; ++k)
+          mma_ts(tmem + C::kTdQ, tmem + C::kTdS + k * 8, kb + k * 128, idesc_q, 1u);
+        mma_commit(&kempty[st]);
+        mma_commit(&dq_done);
+      }
+      __syncwarp();
+    };
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int L = item_at(k);
+      if (L >= n_items) continue;
+      const Item it = item(L);
+      if (!it.live || it.n_kv == 0) continue;
+      if (sc_role) {
+        if (!mbar_wait_warp(&q_bar, ni & 1u, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int jt = 0; jt < it.n_kv && ok; ++jt, ++gt) {
+          // S/dP of this tile overwrite the previous tile's: the softmax must hold them
+          if (gt > 0 && !mbar_wait_warp(&sc_free, (gt - 1) & 1u, ab)) {
+            ok = false;
+            break;
+          }
+          issue_scores();
+        }
+        if (!ok) break;
+        if (elect_sync()) mma_commit(&q_free);  // Q and dO are read once these have run
+        __syncwarp();
+        ++ni;
+      } else {
+        // the first dQ MMA of an item overwrites the accumulator: the softmax
+        // warps have read the previous item's dQ before they hand over its dS
+        for (int jt = 0; jt < it.n_kv && ok; ++jt, ++gt) {
+          if (!mbar_wait_warp(&ds_full, gt & 1u, ab)) {
+            ok = false;
+            break;
+          }
+          // the K stage of this tile: loaded (its S MMAs ran), released below
+          if (!mbar_wait_warp(&kfull[gt % C::kKStages], (gt / C::kKStages) & 1, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_dq(jt > 0);
+        }
+      }
     }
+    uint64_t* drain = sc_role ? &drain_bar : &drain_bar2;
+    if (elect_sync()) {
+      mma_commit(drain);
+      mbar_wait_quiet(drain, 0, lim);
+    }
+    __syncwarp();
   } else if (warp >= 3) {
     // ------------------------------------------------------------ softmax / dS
     // warps 3..10; a warp reads and writes the TMEM lanes of its sub-partition
     const int wq = warp & 3;
     const int wg = (warp - 3) >> 2;
     const int r = wq * 32 + (threadIdx.x & 31);
-    const int i = q0 + r;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const int col0 = wg * C::kHalf;
     const float sl2 = p.scale_log2;
-    const int64_t tok = (int64_t)sq.q_start + i;
-    float lse2 = INFINITY, Dr = 0.0f;
-    if (i < sq.lq) {
-      lse2 = p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + tok] * 1.4426950408889634f;
-      Dr = p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok];
-      if (lse2 == -INFINITY) lse2 = INFINITY;  // keyless row: every key is masked anyway
-    }
-    const long long vis_lo = (long long)i + sq.off - sq.L;
-    long long vis_hi = (long long)i + sq.off + sq.R;
-    if (vis_hi > sq.lk - 1) vis_hi = sq.lk - 1;
-    const long long rows_last = min(q0 + kBlockM, sq.lq) - 1;
+    int gt = 0;
     bool ok = true;
-    for (int jt = 0; jt < n_kv; ++jt) {
-      const int k0 = (kt0 + jt) * BKV;
-      if (!mbar_wait_warp(&sdp_full, jt & 1u, ab)) {
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int L = item_at(k);
+      if (L >= n_items) continue;
+      const Item it = item(L);
+      if (!it.live) continue;
+      const Seq& sq = it.sq;
+      const int q0 = it.q0;
+      const int i = q0 + r;
+      const int64_t tok = (int64_t)sq.q_start + i;
+      float lse2 = INFINITY, Dr = 0.0f;
+      if (i < sq.lq) {
+        lse2 = p.lse[(int64_t)it.b * p.lse_sb + (int64_t)it.h * p.lse_sh + tok] *
+               1.4426950408889634f;
+        Dr = p.d[(int64_t)it.b * p.d_sb + (int64_t)it.h * p.d_sh + tok];
+        if (lse2 == -INFINITY) lse2 = INFINITY;  // keyless row: every key is masked anyway
+      }
+      const long long vis_lo = (long long)i + sq.off - sq.L;
+      long long vis_hi = (long long)i + sq.off + sq.R;
+      if (vis_hi > sq.lk - 1) vis_hi = sq.lk - 1;
+      const long long rows_last = min(q0 + kBlockM, sq.lq) - 1;
+      for (int jt = 0; jt < it.n_kv; ++jt, ++gt) {
+        const int k0 = (it.kt0 + jt) * BKV;
+        if (!mbar_wait_warp(&sdp_full, gt & 1u, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[C::kHalf], dp[C::kHalf];
+#pragma unroll
+        for (int c = 0; c < C::kHalf / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_off + col0 + c * 32, rr);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(rr[t]);
+          tmem_ld32(tmem + lane_off + C::kTdP + col0 + c * 32, rr);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) dp[c * 32 + t] = __uint_as_float(rr[t]);
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sc_free);
+        const int c0 = k0 + col0;  // first key of this warpgroup's columns
+        const bool full_tile = (c0 + C::kHalf - 1 <= sq.lk - 1) &&
+                               ((long long)c0 >= rows_last + sq.off - sq.L) &&
+                               ((long long)(c0 + C::kHalf - 1) <= (long long)q0 + sq.off + sq.R);
+        uint32_t pk[C::kHalf / 2];
+        const long long lo = vis_lo - c0, hi = vis_hi - c0;
+        // P = exp2(s * scale * log2 e - LSE log2 e), dS = P (dP - D), two
+        // columns per packed FP32 operation (the softmax warps are bound by
+        // instruction issue; a - b is a + (-b) exactly, so the results are
+        // unchanged)
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
+        const uint64_t nd2 = f2_pack(-Dr, -Dr);
+#pragma unroll
+        for (int t = 0; t < C::kHalf; t += 2) {
+          float x0, x1;
+          if constexpr (C::kPackArg) {
+            f2_unpack(f2_fma(f2_pack(s[t], s[t + 1]), sl2x2, nl2), x0, x1);
+          } else {
+            x0 = fmaf(s[t], sl2, -lse2);
+            x1 = fmaf(s[t + 1], sl2, -lse2);
+          }
+          float e0 = ex2(x0);
+          float e1 = ex2(x1);
+          if (!full_tile) {
+            if (t < lo || t > hi) e0 = 0.0f;
+            if (t + 1 < lo || t + 1 > hi) e1 = 0.0f;
+          }
+          float g0, g1;
+          f2_unpack(f2_mul(f2_pack(e0, e1), f2_add(f2_pack(dp[t], dp[t + 1]), nd2)), g0, g1);
+          pk[t / 2] = Pack<BF16>::two(g0, g1);
+        }
+        // the dS columns were last read by the previous tile's dQ MMAs
+        if (gt > 0 && !mbar_wait_warp(&dq_done, (gt - 1) & 1u, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < C::kHalf / 32; ++c) {
+          uint32_t w16[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) w16[t] = pk[c * 16 + t];
+          tmem_st16(tmem + lane_off + C::kTdS + col0 / 2 + c * 16, w16);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&ds_full);
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (it.n_kv > 0 && !mbar_wait_warp(&dq_done, (gt - 1) & 1u, ab)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      float s[C::kHalf], dp[C::kHalf];
-#pragma unroll
-      for (int c = 0; c < C::kHalf / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_off + col0 + c * 32, rr);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(rr[t]);
-        tmem_ld32(tmem + lane_off + C::kTdP + col0 + c * 32, rr);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) dp[c * 32 + t] = __uint_as_float(rr[t]);
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&sc_free);
-      const int c0 = k0 + col0;  // first key of this warpgroup's columns
-      const bool full_tile = (c0 + C::kHalf - 1 <= sq.lk - 1) &&
-                             ((long long)c0 >= rows_last + sq.off - sq.L) &&
-                             ((long long)(c0 + C::kHalf - 1) <= (long long)q0 + sq.off + sq.R);
-      uint32_t pk[C::kHalf / 2];
-      const long long lo = vis_lo - c0, hi = vis_hi - c0;
-      // P = exp2(s * scale * log2 e - LSE log2 e), dS = P (dP - D), two columns
-      // per packed FP32 operation (the softmax warps are bound by instruction
-      // issue; a - b is a + (-b) exactly, so the results are unchanged)
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
-      const uint64_t nd2 = f2_pack(-Dr, -Dr);
-#pragma unroll
-      for (int t = 0; t < C::kHalf; t += 2) {
-        float x0, x1;
-        if constexpr (C::kPackArg) {
-          f2_unpack(f2_fma(f2_pack(s[t], s[t + 1]), sl2x2, nl2), x0, x1);
-        } else {
-          x0 = fmaf(s[t], sl2, -lse2);
-          x1 = fmaf(s[t + 1], sl2, -lse2);
-        }
-        float e0 = ex2(x0);
-        float e1 = ex2(x1);
-        if (!full_tile) {
-          if (t < lo || t > hi) e0 = 0.0f;
-          if (t + 1 < lo || t + 1 > hi) e1 = 0.0f;
-        }
-        float g0, g1;
-        f2_unpack(f2_mul(f2_pack(e0, e1), f2_add(f2_pack(dp[t], dp[t + 1]), nd2)), g0, g1);
-        pk[t / 2] = Pack<BF16>::two(g0, g1);
-      }
-      if (jt > 0 && !mbar_wait_warp(&dq_done, (jt - 1) & 1u, ab)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < C::kHalf / 32; ++c) {
-        uint32_t w16[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) w16[t] = pk[c * 16 + t];
-        tmem_st16(tmem + lane_off + C::kTdS + col0 / 2 + c * 16, w16);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&ds_full);
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && n_kv > 0) ok = mbar_wait_warp(&dq_done, (n_kv - 1) & 1u, ab);
-    if (ok) {
       tc_fence_after();
       const bool valid = i < sq.lq;
-      char* row = (char*)p.dq +
-                  ((int64_t)b * p.sdq_b + tok * p.sdq_t + (int64_t)h * p.sdq_h) * (G_F32 ? 4 : 2);
+      char* row = (char*)p.dq + ((int64_t)it.b * p.sdq_b + tok * p.sdq_t + (int64_t)it.h * p.sdq_h) *
+                                    (G_F32 ? 4 : 2);
       constexpr int kCols = DQK / 2;  // dQ columns stored by this warpgroup
 #pragma unroll
       for (int c = 0; c < kCols / 32; ++c) {
         const int col = wg * kCols + c * 32;
         uint32_t rr[32];
-        if (n_kv > 0) {
+        if (it.n_kv > 0) {
           tmem_ld32(tmem + lane_off + C::kTdQ + col, rr);
           tmem_ld_wait();
         } else {
@@ -425,6 +501,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           }
         }
       }
+      // the epilogue's TMEM reads are complete (tcgen05.wait::ld) before this
+      // thread hands over the next item's first dS, which the dQ issuer
+      // waits for before its first MMA of that item overwrites the accumulator
+      tc_fence_before();
     }
     tc_fence_before();
   }
@@ -441,9 +521,12 @@ static cudaError_t launch_dq_t(const DqParams& p, cudaStream_t st) {
   auto k = attn_bwd_dq_kernel<DQK, DV, BKV, BF16, G_F32>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid = tile_major(p.n_qtiles) ? dim3((unsigned)p.n_qtiles, (unsigned)p.hq, (unsigned)p.batch)
-                                      : dim3((unsigned)p.hq, (unsigned)p.n_qtiles, (unsigned)p.batch);
-  k<<<grid, kDqThreads, C::kSmem, st>>>(p);
+  // persistent: at most one CTA per SM, each walking the work items
+  const long long items = (long long)p.n_qtiles * p.hq * p.batch;
+  if (items > 0x7fffffffll) return cudaErrorInvalidValue;  // item indices are 32-bit
+  const long long ctas = items < p.n_ctas ? items : p.n_ctas;
+  if (ctas <= 0) return cudaSuccess;
+  k<<<(unsigned)ctas, kDqThreads, C::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 
