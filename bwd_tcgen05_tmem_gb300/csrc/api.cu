@@ -461,6 +461,7 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
   a.dbg_dkdv = inject_for(inj, ATTN_DEBUG_DKDV);
   a.dbg_scores = inject_for(inj, ATTN_DEBUG_SCORES);
   a.num_sms = num_sms();
+  a.queue_counter = (int*)((char*)ws + attn::kQueueCounterOffset);
   a.seqlen_q = p->seqlen_q;
   a.seqlen_k = p->seqlen_k;
   a.total_q = p->total_q;

@@ -6,7 +6,8 @@
 
 namespace attn {
 
-cudaError_t launch_dq(const DqParams& p, int dqk, int dv, bool bf16, bool gf32, cudaStream_t st);
+cudaError_t launch_dq(const DqParams& p, int dqk, int dv, bool bf16, bool gf32, int num_sms,
+                      cudaStream_t st);
 int dq_block_kv(int dqk, int dv);
 int dkv_plan(int dqk, int dv, int* bq, int* mode);
 cudaError_t launch_dkv(const DkvParams& p, int dqk, int dv, int mode, bool bf16, bool gf32,
@@ -70,9 +71,11 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_lau
     dq.scale_log2 = a.scale_log2;
     dq.status = a.status;
     dq.dbg = a.dbg_dq;
-    dq.n_ctas = a.num_sms;
+    dq.counter = a.queue_counter;
     if (dq.n_qtiles > 65535 || a.batch > 65535 || a.hq > 65535) return cudaErrorInvalidValue;
-    if ((e = launch_dq(dq, a.dqk, a.dv, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
+    // the work-queue counter starts at zero for every launch
+    if ((e = cudaMemsetAsync(dq.counter, 0, sizeof(int), st)) != cudaSuccess) return e;
+    if ((e = launch_dq(dq, a.dqk, a.dv, a.bf16, a.g_f32, a.num_sms, st)) != cudaSuccess) return e;
     ++*n_launches;
   }
   if (has_k && (stages & 4)) {

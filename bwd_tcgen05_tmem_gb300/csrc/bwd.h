@@ -14,6 +14,7 @@ struct BwdArgs {
   float scale, scale_log2;
   int* status;
   int num_sms;
+  int* queue_counter;  // work-queue counter in the workspace (persistent kernels)
   const float* lse;
   int64_t lse_sb, lse_sh;
   float* d;
@@ -125,7 +126,7 @@ struct DqParams {
   int64_t sdq_b, sdq_t, sdq_h;
   int accum;
   int batch, hq, hkv, n_qtiles;
-  int n_ctas;  // persistent grid: CTAs that share the work items
+  int* counter;  // work-queue counter (zeroed before the launch)
   float scale, scale_log2;
   int* status;
   DebugInject dbg;

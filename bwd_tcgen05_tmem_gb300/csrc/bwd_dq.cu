@@ -74,22 +74,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __shared__ int abort_flag, skip_sh;
 
   const int warp = threadIdx.x >> 5;
-  // Persistent: the work items, in the order the one-CTA-per-item grid had
-  // (heaviest query tiles first: with tile_major(), x walks the query tiles
-  // of a head, y the heads, z the batch; otherwise x walks the heads), are
-  // dealt to the CTAs in rounds, every other round in reverse CTA order, so
-  // each CTA's heavy and light items even out.  Every role decodes the same
-  // items, and the barrier phases run on across items, so the next item's
-  // Q/dO loads and first S/dP MMAs overlap this item's last tiles and
+  // Persistent: one CTA per SM takes work items (query tile, head, batch)
+  // from the work queue, in the order the one-CTA-per-item grid had (heaviest
+  // query tiles first: with tile_major(), x walks the query tiles of a head, y
+  // the heads, z the batch; otherwise x walks the heads).  Every role decodes
+  // the same items, and the barrier phases run on across items, so the next
+  // item's Q/dO loads and first S/dP MMAs overlap this item's last tiles and
   // epilogue.
   const bool tmaj = tile_major(p.n_qtiles);
   const int gx = tmaj ? p.n_qtiles : p.hq, gy = tmaj ? p.hq : p.n_qtiles;
   const int n_items = gx * gy * p.batch;  // the launch checks that it fits
-  const int n_rounds = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
-  // round k's item for this CTA (may be past the end in the last round)
-  auto item_at = [&](int k) {
-    return k * (int)gridDim.x + ((k & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x);
-  };
+  __shared__ ItemRing<4> iring;
   struct Item {
     Seq sq;
     int h, g, b, tb, q0, kt0, n_kv;
@@ -118,8 +113,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     return it;
   };
 
-  const unsigned long long lim = wait_limit(p.dbg);
-  const int drop = dropped_load(p.dbg);
+  const unsigned long long lim = wait_limit_all(p.dbg);
   Abort ab{&abort_flag, p.status, lim};
   if (threadIdx.x == 0) {
     // a failed device check or an earlier abort stops every CTA
@@ -135,6 +129,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     mbar_init(&q_bar, 1);
     mbar_init(&q_free, 1);
+    item_ring_init(iring, 10);  // consumers: the two MMA issuers, eight softmax warps
     mbar_init(&sdp_full, 1);
     mbar_init(&sc_free, 256);
     mbar_init(&ds_full, 256);
@@ -165,9 +160,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     uint32_t vcnt = 0;
     int gk = 0, ni = 0;  // K stages and items issued
     bool ok = true;
-    for (int k = 0; k < n_rounds && ok; ++k) {
-      const int L = item_at(k);
-      if (L >= n_items) continue;
+    for (int q = 0; ok; ++q) {
+      const int L = item_ring_push(iring, q, p.counter, n_items, ab, ok);
+      if (L < 0) break;
       const Item it = item(L);
       if (!it.live || it.n_kv == 0) continue;
       if (ni > 0 && !mbar_wait_warp(&q_free, (ni - 1) & 1u, ab)) {
@@ -210,7 +205,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           break;
         }
         map_coords(p.ok, 0, it.g, krow, it.tb, d1, d2, d3);
-        if (gk != drop && elect_sync()) {  // drop: test-only injected missing load
+        // test-only injected missing load: K of tile `drop_load` of work item 0
+        if (!(L == 0 && jt == p.dbg.drop_load) && elect_sync()) {
           mbar_arrive_tx(&kfull[st], C::kKStage);
 #pragma unroll
           for (int c = 0; c < C::kKCh; ++c)
@@ -296,9 +292,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       __syncwarp();
     };
-    for (int k = 0; k < n_rounds && ok; ++k) {
-      const int L = item_at(k);
-      if (L >= n_items) continue;
+    for (int q = 0; ok; ++q) {
+      const int L = item_ring_pop(iring, q, ab, ok);
+      if (L < 0) break;
       const Item it = item(L);
       if (!it.live || it.n_kv == 0) continue;
       if (sc_role) {
@@ -354,9 +350,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const float sl2 = p.scale_log2;
     int gt = 0;
     bool ok = true;
-    for (int k = 0; k < n_rounds && ok; ++k) {
-      const int L = item_at(k);
-      if (L >= n_items) continue;
+    for (int q = 0; ok; ++q) {
+      const int L = item_ring_pop(iring, q, ab, ok);
+      if (L < 0) break;
       const Item it = item(L);
       if (!it.live) continue;
       const Seq& sq = it.sq;
@@ -516,37 +512,39 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 }
 
 template <int DQK, int DV, int BKV, bool BF16, bool G_F32>
-static cudaError_t launch_dq_t(const DqParams& p, cudaStream_t st) {
+static cudaError_t launch_dq_t(const DqParams& p, int num_sms, cudaStream_t st) {
   using C = DqCfg<DQK, DV, BKV>;
   auto k = attn_bwd_dq_kernel<DQK, DV, BKV, BF16, G_F32>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  // persistent: at most one CTA per SM, each walking the work items
+  // persistent: at most one CTA per SM, each taking items from the work queue
   const long long items = (long long)p.n_qtiles * p.hq * p.batch;
-  if (items > 0x7fffffffll) return cudaErrorInvalidValue;  // item indices are 32-bit
-  const long long ctas = items < p.n_ctas ? items : p.n_ctas;
+  if (items > 0x7fffffffll || !p.counter) return cudaErrorInvalidValue;
+  const long long ctas = items < num_sms ? items : num_sms;
   if (ctas <= 0) return cudaSuccess;
   k<<<(unsigned)ctas, kDqThreads, C::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 
 template <int DQK, int DV, int BKV>
-static cudaError_t launch_dq_d(const DqParams& p, bool bf16, bool gf32, cudaStream_t st) {
+static cudaError_t launch_dq_d(const DqParams& p, bool bf16, bool gf32, int num_sms,
+                               cudaStream_t st) {
   if (bf16)
-    return gf32 ? launch_dq_t<DQK, DV, BKV, true, true>(p, st)
-                : launch_dq_t<DQK, DV, BKV, true, false>(p, st);
-  return gf32 ? launch_dq_t<DQK, DV, BKV, false, true>(p, st)
-              : launch_dq_t<DQK, DV, BKV, false, false>(p, st);
+    return gf32 ? launch_dq_t<DQK, DV, BKV, true, true>(p, num_sms, st)
+                : launch_dq_t<DQK, DV, BKV, true, false>(p, num_sms, st);
+  return gf32 ? launch_dq_t<DQK, DV, BKV, false, true>(p, num_sms, st)
+              : launch_dq_t<DQK, DV, BKV, false, false>(p, num_sms, st);
 }
 
 // Rows of the key/value tile streamed by the dQ kernel for a head-dim pair.
 int dq_block_kv(int dqk, int dv) { return (dqk >= 256 || dv >= 256) ? 64 : 128; }
 
-cudaError_t launch_dq(const DqParams& p, int dqk, int dv, bool bf16, bool gf32, cudaStream_t st) {
-  if (dqk == 64 && dv == 64) return launch_dq_d<64, 64, 128>(p, bf16, gf32, st);
-  if (dqk == 128 && dv == 128) return launch_dq_d<128, 128, 128>(p, bf16, gf32, st);
-  if (dqk == 192 && dv == 128) return launch_dq_d<192, 128, 128>(p, bf16, gf32, st);
-  if (dqk == 256 && dv == 256) return launch_dq_d<256, 256, 64>(p, bf16, gf32, st);
+cudaError_t launch_dq(const DqParams& p, int dqk, int dv, bool bf16, bool gf32, int num_sms,
+                      cudaStream_t st) {
+  if (dqk == 64 && dv == 64) return launch_dq_d<64, 64, 128>(p, bf16, gf32, num_sms, st);
+  if (dqk == 128 && dv == 128) return launch_dq_d<128, 128, 128>(p, bf16, gf32, num_sms, st);
+  if (dqk == 192 && dv == 128) return launch_dq_d<192, 128, 128>(p, bf16, gf32, num_sms, st);
+  if (dqk == 256 && dv == 256) return launch_dq_d<256, 256, 64>(p, bf16, gf32, num_sms, st);
   return cudaErrorNotSupported;
 }
 

@@ -100,6 +100,71 @@ __device__ __forceinline__ unsigned long long wait_limit(const DebugInject& d) {
 __device__ __forceinline__ int dropped_load(const DebugInject& d) {
   return first_cta() ? d.drop_load : -1;
 }
+// The persistent kernel (CTAs take work items from a queue): every CTA uses
+// the injected wait limit, and the CTA that runs work item 0 leaves out load
+// `drop_load` of that item (a healthy wait lasts microseconds, so the short
+// limit only runs out where the load is missing).
+__device__ __forceinline__ unsigned long long wait_limit_all(const DebugInject& d) {
+  return d.wait_ns ? d.wait_ns : kWaitLimitNs;
+}
+
+// ----------------------------------------------------------------- work queue
+// A persistent kernel (one CTA per SM) takes its work items from a global
+// counter, in the order a one-CTA-per-item grid would run them, so the SMs
+// stay balanced the way the hardware's block scheduler balances blocks.  One
+// lane of the producer warp takes the next index (atomicAdd) and publishes it
+// in a small shared ring; every other role pops the indices in the same
+// order.  -1 marks the end.  The counter (in the caller's workspace) is zeroed
+// before each launch.
+template <int N>
+struct ItemRing {
+  int idx[N];
+  uint64_t full[N], empty[N];
+};
+
+template <int N>
+__device__ __forceinline__ void item_ring_init(ItemRing<N>& r, uint32_t consumers) {
+  for (int i = 0; i < N; ++i) {
+    mbar_init(&r.full[i], 1);
+    mbar_init(&r.empty[i], consumers);
+  }
+}
+
+// Producer warp (all lanes): the q-th item index, or -1 past the last item.
+template <int N>
+__device__ __forceinline__ int item_ring_push(ItemRing<N>& r, int q, int* counter, int n_items,
+                                              const Abort& ab, bool& ok) {
+  const int slot = q % N;
+  if (q >= N && !mbar_wait_warp(&r.empty[slot], ((q / N) - 1) & 1u, ab)) {
+    ok = false;
+    return -1;
+  }
+  int v = -1;
+  if ((threadIdx.x & 31) == 0) {
+    v = atomicAdd(counter, 1);
+    if (v >= n_items) v = -1;
+    r.idx[slot] = v;
+    mbar_arrive(&r.full[slot]);
+  }
+  return __shfl_sync(0xffffffffu, v, 0);
+}
+
+// Consumer warp (all lanes): the q-th item index, or -1 past the last item.
+template <int N>
+__device__ __forceinline__ int item_ring_pop(ItemRing<N>& r, int q, const Abort& ab, bool& ok) {
+  const int slot = q % N;
+  if (!mbar_wait_warp(&r.full[slot], (q / N) & 1u, ab)) {
+    ok = false;
+    return -1;
+  }
+  const int v = *(volatile int*)&r.idx[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[slot]);
+  return v;
+}
+
+// Byte offset of the work-queue counter in a workspace (after the status word).
+constexpr int kQueueCounterOffset = 128;
 
 // ----------------------------------------------------------------- params
 struct FwdParams {

@@ -314,11 +314,16 @@ int attn_last_launch_count(void);
  * "missing wait" on a reused barrier phase; this is the guard against that
  * class of bug).  This call arms the NEXT attn_fwd / attn_bwd* call on the
  * calling thread, then clears itself: in every kernel selected by
- * `kernel_mask` (ATTN_DEBUG_* bits), the first CTA of the launch (block
- * 0,0,0) leaves out its load number `drop_load` (-1: none; the counter is the
- * kernel's stage/ring load index) and, if `wait_limit_ns` is non-zero, uses
- * that wait limit instead of 2 s.  No other CTA and no other call is
- * affected.  A dropped load makes a wait run out, so the call reports
+ * `kernel_mask` (ATTN_DEBUG_* bits), one CTA leaves out load number
+ * `drop_load` (-1: none) and, if `wait_limit_ns` is non-zero, waits at most
+ * that long instead of 2 s.  In the dQ kernel, which runs work items from a
+ * queue, it is the CTA that runs the first work item (the heaviest query
+ * tile of the first head), the load is the K tile number `drop_load` of that
+ * item, and every CTA of the launch uses the shorter limit (a healthy wait
+ * lasts microseconds); in the other
+ * kernels it is the first CTA (block 0,0,0), the load number counts its
+ * stage/ring loads, and only that CTA uses the shorter limit.  No other call
+ * is affected.  A dropped load makes a wait run out, so the call reports
  * ATTN_ERR_TIMEOUT through attn_query_status and leaves its outputs
  * undefined; the device stays usable and later calls are unaffected.
  */

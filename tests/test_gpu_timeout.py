@@ -27,7 +27,7 @@ from test_gpu_parity import dense_inputs
 
 pytestmark = pytest.mark.gpu
 
-WAIT_NS = 20_000_000  # 20 ms limit for the faulted CTA
+WAIT_NS = 20_000_000  # 20 ms wait limit while a load is left out
 
 CASES = [
     # id, (dqk, dv), hq, hkv, seqlen, kernel bit, dropped load
