@@ -51,6 +51,20 @@ def visible_pairs(w, lengths=None):
     return n * w.heads_q
 
 
+def score_blocks(w, lengths=None):
+    """Visible 128-query x 128-key blocks over sequences and query heads
+    (causal, with the workload's left window): one 32 KiB dS block each on
+    the dS path of the backward."""
+    lens = lengths if lengths is not None else w.lengths()
+    n = 0
+    for L in lens:
+        for qt in range((L + 127) // 128):
+            i0, i1 = 128 * qt, min(128 * qt + 127, L - 1)
+            j0 = max(0, i0 - w.window[0]) if w.window[0] >= 0 else 0
+            n += i1 // 128 - j0 // 128 + 1
+    return n * w.heads_q
+
+
 def flops(w, lengths=None):
     nv = visible_pairs(w, lengths)
     fwd = 2 * nv * (w.d_qk + w.d_v)
@@ -293,6 +307,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cp", action="store_true")
+    ap.add_argument("--bwd-ds", default="auto", choices=["auto", "ds", "recompute"],
+                    help="backward path at head dims 128/192 (attn_params_t.bwd_ds)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -333,9 +349,18 @@ def main():
     o = torch.empty((*q.shape[:-1], w.d_v), dtype=q.dtype, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fws = torch.empty(attn.workspace_size("fwd", q, k, v, **kw), dtype=torch.uint8, device=dev)
-    bws = torch.empty(attn.workspace_size("bwd", q, k, v, **kw), dtype=torch.uint8, device=dev)
+    bkw = dict(kw, bwd_ds={"auto": 0, "ds": 1, "recompute": -1}[args.bwd_ds])
+    bws = torch.empty(attn.workspace_size("bwd", q, k, v, **bkw), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    stages = ("fwd", "pre", "dq", "dkdv")
+    # the stage order of attn_bwd: on the dS path the dK/dV kernel writes the
+    # dS blocks that the dQ GEMM then reads
+    bwd_path = attn.bwd_path(q, k, v, **bkw)
+    if bwd_path == attn.BWD_DS:
+        KERNEL_SOURCES["dq"] = "bwd_dq_ds.cu"
+        stages = ("fwd", "pre", "dkdv", "dq")
+    else:
+        stages = ("fwd", "pre", "dq", "dkdv")
+    api_stages = tuple({"pre": "preprocess"}.get(st, st) for st in stages[1:])
 
     def step(ev=None):
         n = 0
@@ -343,10 +368,10 @@ def main():
             ev[0].record(stream)
         attn.fwd(q, k, v, out=o, lse=lse, workspace=fws, **kw)
         n += attn.last_launch_count()
-        for i, st in enumerate(("preprocess", "dq", "dkdv")):
+        for i, st in enumerate(api_stages):
             if ev:
                 ev[i + 1].record(stream)
-            attn.bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=bws, stage=st, **kw)
+            attn.bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=bws, stage=st, **bkw)
             n += attn.last_launch_count()
         if ev:
             ev[4].record(stream)
@@ -395,7 +420,7 @@ def main():
                 for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
-    hkw = dict(kw)
+    hkw = dict(bkw)
     if w.is_thd:  # host metadata for the host-buffer call
         hkw.update(cu_seqlens_q=inp["cu_seqlens"], cu_seqlens_k=inp["cu_seqlens"])
     h_o, h_lse, h_dq, h_dk, h_dv = host_out[0]
@@ -611,6 +636,11 @@ def main():
     ach = fl["kernel"][dom] / (per_kernel[dom] * 1e-3) / 1e12
     traffic = load_traffic(dom)
     value = job_tflops(fl["total"], ms, world)
+    lens_b = ((inp["cu_seqlens"][1:] - inp["cu_seqlens"][:-1]).tolist() if w.is_thd else None)
+    rows_q = q.shape[0] * (1 if w.is_thd else q.shape[1])
+    rows_k = k.shape[0] * (1 if w.is_thd else k.shape[1])
+    dq_bytes = (score_blocks(w, lens_b) * 32768 + rows_q * w.heads_q * w.d_qk * 2 +
+                rows_k * w.heads_kv * w.d_qk * 2)
     line = {
         "metric": METRIC,
         "value": value,
@@ -645,6 +675,14 @@ def main():
                      "peak_sustained": peak_sus, "frac_sustained": ach / peak_sus,
                      "sm_mhz": clocks.get("sm_mhz"),
                      "work_per_launch": fl["kernel"][dom]},
+        "bwd_path": {attn.BWD_RECOMPUTE: "recompute", attn.BWD_DS: "ds",
+                     attn.BWD_PDS: "pds"}[bwd_path],
+        "dq_gemm_hbm": None if bwd_path != attn.BWD_DS else {
+            "bound": "hbm", "unit": "GB/s", "peak": peaks["hbm_gbs"],
+            "bytes": dq_bytes, "achieved": dq_bytes / (per_kernel["dq"] * 1e-3) / 1e9,
+            "frac": dq_bytes / (per_kernel["dq"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "note": "dQ GEMM of the dS path: dS blocks (32 KiB per visible 128 x 128 "
+                    "tile and query head) read once, K read once, dQ written once"},
         "kernels": {k_: {"ms": per_kernel[k_],
                          "tflops": fl["kernel"][k_] / (per_kernel[k_] * 1e-3) / 1e12,
                          "frac": fl["kernel"][k_] / (per_kernel[k_] * 1e-3) / 1e12 / peak_tf,

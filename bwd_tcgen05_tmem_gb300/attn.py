@@ -32,9 +32,11 @@ EXPORTED = ["attn_fwd_workspace_size", "attn_bwd_workspace_size", "attn_fwd", "a
             "attn_lse_merge", "attn_cp_relayout",
             "attn_query_status", "attn_last_error", "attn_last_launch_count",
             "attn_debug_inject", "attn_host_arena_size", "attn_fwd_bwd_host",
-            "attn_fwd_bwd_host_stages"]
+            "attn_fwd_bwd_host_stages", "attn_bwd_path"]
 # attn_fwd_bwd_host_stages stage bits
 HOST_UPLOAD, HOST_COMPUTE, HOST_DOWNLOAD, HOST_ALL = 1, 2, 4, 7
+# attn_bwd_path results: which backward kernels run (and the stage order)
+BWD_RECOMPUTE, BWD_DS, BWD_PDS = 0, 1, 2
 # attn_debug_inject kernel bits (test only)
 DEBUG_FWD, DEBUG_DQ, DEBUG_DKDV, DEBUG_SCORES = 1, 2, 4, 8
 
@@ -64,6 +66,7 @@ class Params(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("accumulate", ctypes.c_int),
         ("seqused_q", ctypes.c_void_p), ("seqused_k", ctypes.c_void_p),
+        ("bwd_ds", ctypes.c_int),
     ]
 
 
@@ -87,6 +90,8 @@ def load():
         lib.attn_fwd_workspace_size.restype = sz
         lib.attn_bwd_workspace_size.argtypes = [P]
         lib.attn_bwd_workspace_size.restype = sz
+        lib.attn_bwd_path.argtypes = [P]
+        lib.attn_bwd_path.restype = ctypes.c_int
         lib.attn_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.attn_fwd.restype = ctypes.c_int
         for name in ("attn_bwd", "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkdv"):
@@ -163,7 +168,10 @@ def _stream(stream):
 def make_params(q, k, v, *, causal=True, scale=None, window=(-1, -1), bottom_right=False,
                 cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
                 o=None, dout=None, dq=None, dk=None, dv=None, o_dtype=None, grad_dtype=None,
-                lse_strides=(0, 0), accumulate=False, seqused_q=None, seqused_k=None):
+                lse_strides=(0, 0), accumulate=False, seqused_q=None, seqused_k=None,
+                bwd_ds=0):
+    """attn_params_t for these tensors.  ``bwd_ds``: 0 auto, 1 always, -1
+    never keep dS in the backward's workspace (attn_bwd_path)."""
     thd = cu_seqlens_q is not None
     p = Params()
     p.dtype = _code(q.dtype)
@@ -194,6 +202,7 @@ def make_params(q, k, v, *, causal=True, scale=None, window=(-1, -1), bottom_rig
     p.window_left, p.window_right = int(window[0]), int(window[1])
     p.softmax_scale = float(scale if scale is not None else 1.0 / math.sqrt(dqk))
     p.accumulate = int(bool(accumulate))
+    p.bwd_ds = int(bwd_ds)
     if seqused_q is not None:  # padded THD: device int32 [batch] visible lengths
         p.seqused_q = seqused_q.data_ptr()
         p.seqused_k = (seqused_k if seqused_k is not None else seqused_q).data_ptr()
@@ -237,11 +246,13 @@ def bwd(q, k, v, o, dout, lse, *, causal=True, scale=None, window=(-1, -1),
         bottom_right=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None,
         max_seqlen_k=None, seqused_q=None, seqused_k=None, dq=None, dk=None, dv=None,
         grad_dtype=None, lse_strides=(0, 0), accumulate=False, workspace=None, stream=None,
-        stage="all"):
+        stage="all", bwd_ds=0):
     """Fused attention backward. Returns (dq, dk, dv).
 
     ``stage``: "all" (attn_bwd), or one of "preprocess", "dq", "dkdv" to run a
-    single stage of it (the C ABI's attn_bwd_* entry points)."""
+    single stage of it (the C ABI's attn_bwd_* entry points; on the BWD_DS
+    path the dkdv stage comes before the dq stage).  ``bwd_ds``: see
+    make_params."""
     lib = load()
     gdt = grad_dtype if grad_dtype is not None else q.dtype
     if dq is None:
@@ -255,7 +266,8 @@ def bwd(q, k, v, o, dout, lse, *, causal=True, scale=None, window=(-1, -1),
                     cu_seqlens_k=cu_seqlens_k, max_seqlen_q=max_seqlen_q,
                     max_seqlen_k=max_seqlen_k, o=o, dout=dout, dq=dq, dk=dk, dv=dv,
                     o_dtype=o.dtype, grad_dtype=gdt, lse_strides=lse_strides,
-                    accumulate=accumulate, seqused_q=seqused_q, seqused_k=seqused_k)
+                    accumulate=accumulate, seqused_q=seqused_q, seqused_k=seqused_k,
+                    bwd_ds=bwd_ds)
     need = lib.attn_bwd_workspace_size(ctypes.byref(p))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -332,6 +344,15 @@ def fwd_bwd_host(q, k, v, dout, o, lse, dq, dk, dv, arena, *, stream=None, stage
     else:
         _check(lib.attn_fwd_bwd_host_stages(*args, int(stages), _stream(stream)))
     return o, lse, dq, dk, dv
+
+
+def bwd_path(q, k, v, **kw):
+    """attn_bwd_path: BWD_RECOMPUTE, BWD_DS or BWD_PDS for these tensors."""
+    p = make_params(q, k, v, **kw)
+    r = load().attn_bwd_path(ctypes.byref(p))
+    if r < 0:
+        raise AttnError(1, load().attn_last_error().decode(errors="replace"))
+    return r
 
 
 def workspace_size(kind, q, k, v, **kw):

@@ -27,6 +27,13 @@ import torch
 
 from . import attn
 
+# The ring and all-gather schedules run the backward's stages themselves, dq
+# before dkdv (several calls' dq stages overlap on their streams; the dkdv
+# stages that add into shared dK/dV run one after another), and keep one
+# workspace per query-row set across ring steps: the recompute backward, whose
+# dq stage needs no blocks from the dkdv stage and whose workspace is small.
+RECOMPUTE = -1
+
 
 @dataclasses.dataclass
 class Piece:
@@ -141,7 +148,7 @@ class CPRing:
         c = self.chunk
         need = max(256, *(attn.workspace_size("bwd", self.q[0][:, q0:q0 + nq],
                                               self.k[0][:, k0:k0 + nk], self.v[0][:, k0:k0 + nk],
-                                              causal=cz)
+                                              causal=cz, bwd_ds=RECOMPUTE)
                           for (q0, nq), (k0, nk), cz in (((0, 2 * c), (0, 2 * c), True),
                                                          ((0, 2 * c), (0, c), False),
                                                          ((c, c), (0, 2 * c), False))))
@@ -212,7 +219,8 @@ class CPRing:
                      dq=self.dq[r][:, q0:q0 + nq], dk=self.dk[pc.src][:, k0:k0 + nk],
                      dv=self.dv[pc.src][:, k0:k0 + nk], grad_dtype=torch.float32,
                      accumulate=accumulate, lse_strides=(0, rows),
-                     workspace=self.bwd_ws[r][pc.q_rows], stream=self.streams.s[r], stage=stage)
+                     workspace=self.bwd_ws[r][pc.q_rows], stream=self.streams.s[r], stage=stage,
+                     bwd_ds=RECOMPUTE)
             return attn.last_launch_count()
 
         for r in range(cp):  # D of every query-row set the rank's steps use, once
@@ -292,7 +300,7 @@ class CPAllGather:
         self.fwd_ws = [torch.empty(256, dtype=torch.uint8, device=dev) for _ in range(cp)]
         need = max(attn.workspace_size("bwd", self.q[0][:, :self.chunk], k[:, k0:k1],
                                        v[:, k0:k1], causal=True, bottom_right=True,
-                                       window=self.window)
+                                       window=self.window, bwd_ds=RECOMPUTE)
                    for pcs in self.pieces for _, _, (k0, k1) in pcs)
         # one workspace per call: the calls' preprocess and dq stages overlap
         self.bwd_ws = [[torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
@@ -341,7 +349,7 @@ class CPAllGather:
                          window=self.window, scale=self.scale, dq=self.dq[r][:, q0:q0 + nq],
                          dk=self.dk[:, k0:k1], dv=self.dv[:, k0:k1], grad_dtype=torch.float32,
                          accumulate=True, lse_strides=(0, rows), workspace=self.bwd_ws[r][i],
-                         stream=st, stage=stage)
+                         stream=st, stage=stage, bwd_ds=RECOMPUTE)
                 return attn.last_launch_count()
 
             for i in range(len(pcs)):  # independent: every call has its own rows

@@ -162,6 +162,7 @@ attn_status_t check_params(const attn_params_t* p) {
     return fail(ATTN_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
   if (p->stride_lse[0] < 0 || p->stride_lse[1] < 0)
     return fail(ATTN_ERR_INVALID_ARG, "stride_lse must be >= 0");
+  if (p->bwd_ds < -1 || p->bwd_ds > 1) return fail(ATTN_ERR_INVALID_ARG, "bwd_ds must be -1, 0 or 1");
   return ATTN_OK;
 }
 
@@ -235,17 +236,22 @@ attn_status_t launch_check_if_thd(const attn_params_t* p, int* status, cudaStrea
   return ATTN_OK;
 }
 
-// Backward workspace: [status][D: rows x heads_q fp32] and, for head dims
-// above 256, [per-sequence block prefix][64 KiB score blocks].
+// Backward workspace: [status][D: rows x heads_q fp32] and, on the PDS and
+// DS paths, [per-sequence block prefix][64 KiB P/dS or 32 KiB dS blocks].
 struct BwdLayout {
   size_t d_off, plan_off, blk_off, total;
-  long long cap;  // score blocks
+  long long cap;  // blocks
 };
 
 long long wide_block_count(const attn_params_t* p);
 bool wide(const attn_params_t* p) {
   if (p->d_qk < 256 || p->d_v < 256) return false;
   return attn::wide_backward(p->d_qk, p->d_v, wide_block_count(p) * (long long)attn::kWideBlock);
+}
+bool ds_path(const attn_params_t* p) {
+  if (p->d_qk > 192) return false;
+  const long long n = wide_block_count(p);  // the kernels index blocks in 32 bits
+  return n <= INT_MAX && attn::ds_backward(p->d_qk, p->d_v, n * (long long)attn::kDsBlock, p->bwd_ds);
 }
 
 // Score blocks of the wide backward over all query heads: exact for dense
@@ -280,12 +286,13 @@ BwdLayout bwd_layout(const attn_params_t* p) {
   const size_t d_bytes = (size_t)(rq > 0 ? rq : 0) * (size_t)(p->heads_q > 0 ? p->heads_q : 0) * 4;
   l.d_off = kStatusBytes;
   l.total = l.d_off + ((d_bytes + 255) / 256) * 256;
-  if (wide(p)) {
+  const bool w = wide(p);
+  if (w || ds_path(p)) {
     l.plan_off = l.total;
     const size_t plan_bytes = (size_t)(p->batch > 0 ? p->batch + 1 : 1) * 8;
     l.blk_off = ((l.plan_off + plan_bytes + 1023) / 1024) * 1024;
     l.cap = wide_block_count(p);
-    l.total = l.blk_off + (size_t)l.cap * attn::kWideBlock;
+    l.total = l.blk_off + (size_t)l.cap * (w ? attn::kWideBlock : attn::kDsBlock);
   }
   return l;
 }
@@ -302,6 +309,12 @@ size_t attn_fwd_workspace_size(const attn_params_t* p) {
 size_t attn_bwd_workspace_size(const attn_params_t* p) {
   if (!p) return kStatusBytes;
   return bwd_layout(p).total;
+}
+
+int attn_bwd_path(const attn_params_t* p) {
+  if (check_params(p)) return -1;
+  if (wide(p)) return ATTN_BWD_PDS;
+  return ds_path(p) ? ATTN_BWD_DS : ATTN_BWD_RECOMPUTE;
 }
 
 attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, const void* v,
@@ -476,6 +489,11 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
     a.wide_plan = (long long*)((char*)ws + lay.plan_off);
     a.wide_blocks = (uint8_t*)ws + lay.blk_off;
     a.wide_cap = lay.cap;
+  } else if (ds_path(p)) {
+    a.ds = 1;
+    a.ds_plan = (long long*)((char*)ws + lay.plan_off);
+    a.ds_blocks = (uint8_t*)ws + lay.blk_off;
+    a.ds_cap = lay.cap;
   }
   a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout;
   a.dq = dq; a.dk = dk; a.dvp = dv;
@@ -579,6 +597,9 @@ attn_status_t attn_bwd_noalloc(const attn_params_t* p, const void* q, const void
   g_err[0] = 0;
   g_launches = 0;
   if (attn_status_t s0 = check_params(p)) return s0;
+  attn_params_t pr = *p;  // auto: the recompute path, whose workspace is small
+  if (pr.bwd_ds == 0) pr.bwd_ds = -1;
+  p = &pr;
   const size_t need = attn_bwd_workspace_size(p);
   if (need > kNoAllocScratchBytes)
     return fail(ATTN_ERR_WORKSPACE,

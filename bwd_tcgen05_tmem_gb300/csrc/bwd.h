@@ -1,5 +1,6 @@
 // bwd.h -- argument block of the backward pass and its kernel parameter
-// blocks (definitions in bwd_dq.cu, bwd_dkdv.cu, bwd.cu).
+// blocks (definitions in bwd_dq.cu, bwd_dkdv.cu, bwd_dq_ds.cu, bwd_wide.cu,
+// bwd.cu).
 #pragma once
 #include "kcommon.cuh"
 
@@ -30,6 +31,12 @@ struct BwdArgs {
   long long* wide_plan;
   uint8_t* wide_blocks;
   long long wide_cap;
+  // the dS backward (see ds_backward): the dK/dV kernel also writes dS, the
+  // dQ GEMM reads it; per-sequence block prefix and the dS blocks
+  int ds;
+  long long* ds_plan;
+  uint8_t* ds_blocks;
+  long long ds_cap;
   // test-only fault injection (attn_debug_inject), per kernel: dQ / dK-dV
   // kernels, or the scores kernel and the dQ / dK-dV GEMMs of the wide path
   DebugInject dbg_dq, dbg_dkdv, dbg_scores;
@@ -64,6 +71,55 @@ __host__ __device__ inline int wide_blocks_of_qtile(const Seq& s, int qt, int& k
   if (j1 < j0) return 0;
   kb0 = (int)(j0 / 128);
   return (int)(j1 / 128) - kb0 + 1;
+}
+
+// Blocks of query tiles [0, qt) of one sequence; called by a whole warp.
+__device__ inline long long blocks_row_prefix(const Seq& s, int qt) {
+  long long acc = 0;
+  int kb0;
+  for (int t = (int)(threadIdx.x & 31); t < qt; t += 32) acc += wide_blocks_of_qtile(s, t, kb0);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  return acc;
+}
+
+__device__ __forceinline__ bool status_set(const int* status) {
+  return status && *(volatile const int*)status;
+}
+
+__device__ __forceinline__ void raise_status(int* status, int code) {
+  if (status) atomicCAS(status, DEV_OK, code);
+}
+
+// ---------------------------------------------------------------- dS path
+// At head dims up to 192 the backward can keep dS instead of recomputing the
+// scores for dQ: the key-stationary dK/dV kernel, which computes every dS
+// element anyway, writes it once to the workspace, and dQ = scale dS K is a
+// GEMM over those blocks (S and dP are then computed once per query-key pair
+// instead of twice).  One 32 KiB block per (sequence, query head, 128-row
+// query tile, visible 128-key block), indexed like the wide path's blocks
+// (hq*plan[b] + h*T_b + rowprefix_b(qt) + kb - kb0(qt)), holding dS as the
+// MN-major A operand of the dQ MMA in the unswizzled layout: the 16 bytes of
+// queries 8c .. 8c+7 of key row r sit at c*2048 + r*16.  Then the 32 key rows
+// a warp of the dK/dV kernel holds land in 512 contiguous bytes per store.
+constexpr int kDsChunk = 128 * 16;  // one 8-query column of all 128 key rows
+constexpr int kDsBlock = 16 * kDsChunk;
+
+// The dS path serves head dims 128/128 and 192/128 (single-launch dK/dV
+// kernels).  ds_mode (the params' bwd_ds field) forces it off (-1) or on (1);
+// by default (0) it runs at 192/128 while its blocks take at most kDsCap
+// bytes.  The trade, measured on GB300 at causal 192/128: the dK/dV kernel
+// slows by about a quarter with 32 KiB of dS stores per tile, the dQ GEMM
+// streams them at 0.85 of the copy bandwidth, and dQ no longer recomputes
+// S (192) and dP (128) per pair: 33.0 -> 31.6 ms for B1 H32 S32K fwd+bwd,
+// even at 4K.  At 128/128 the recomputing dQ kernel does 384 instead of 512
+// per pair, and the two are even (THD 65K tokens: 9.8 vs 9.9 ms); at 64/64
+// recomputing is cheaper than streaming 32 KiB per 128 x 128 tile.
+constexpr long long kDsCap = 64ll << 30;
+inline bool ds_backward(int dqk, int dv, long long block_bytes, int ds_mode) {
+  const bool shape = (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128);
+  if (!shape || ds_mode < 0) return false;
+  return ds_mode > 0 || (dqk == 192 && block_bytes <= kDsCap);
 }
 
 struct WidePlanParams {
@@ -148,7 +204,31 @@ struct DkvParams {
   float scale, scale_log2;
   int* status;
   DebugInject dbg;
+  // dS path: write dS of every visited tile into its block (null: do not)
+  uint8_t* ds;
+  const long long* plan;
+  long long cap;
 };
+
+// dQ GEMM of the dS path: dQ = scale * sum_kb dS_kb K_kb per query tile
+struct DqDsParams {
+  CUtensorMap tm_k;  // 128-row boxes
+  MapOrder ok;
+  Geometry geo;
+  const long long* plan;
+  const uint8_t* blocks;
+  long long cap;
+  void* dq;
+  int64_t sdq_b, sdq_t, sdq_h;
+  int accum;
+  int batch, hq, hkv, n_qtiles;
+  float scale;
+  int* status;
+  DebugInject dbg;
+};
+
+cudaError_t launch_wide_plan(const WidePlanParams& p, cudaStream_t st);
+cudaError_t launch_dq_ds(const DqDsParams& p, int dqk, bool bf16, bool gf32, cudaStream_t st);
 
 cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* n_launches);
 

@@ -13,6 +13,10 @@
 // then dK *= scale.  The group reduction happens in TMEM, in a fixed order:
 // no atomics, bitwise reproducible.
 //
+// With a dS workspace (the dS path of the backward) the softmax warps also
+// store each dS^T tile, as the MN-major A operand image of the dQ GEMM's
+// 32 KiB blocks (bwd.h), so that dQ needs no second pass over the scores.
+//
 // MODE selects the accumulators: 3 = dK and dV, 1 = dV only, 2 = dK only
 // (head dim 256 runs one launch of each: both accumulators do not fit in the
 // 512 TMEM columns next to the score tiles).
@@ -49,8 +53,11 @@ struct DkvCfg {
   static constexpr int kStages = (kBudget - kResident - 3 * kStageBytes >= 2 * kRingTile * kChunk) ? 3 : 2;
   static constexpr int kRingRaw = kRingTile ? (kBudget - kResident - kStages * kStageBytes) / kChunk : 1;
   static constexpr int kRing = kRingRaw > 12 ? 12 : kRingRaw;
-  static constexpr int kSmem = kResident + kStages * kStageBytes + kRing * kChunk + 1024;
+  static constexpr int kRingAlloc = kRingTile ? kRing : 0;  // ring slots in shared memory
+  static constexpr int kSmem = kResident + kStages * kStageBytes + kRingAlloc * kChunk + 1024;
   static constexpr int kHalf = BQ / 2;
+  // the dS path runs at these shapes (ds_backward)
+  static constexpr bool kCanDs = kDK && kDV && (DQK == 128 || DQK == 192);
   // TMEM columns
   static constexpr int kTS = 0;
   static constexpr int kTdP = BQ;
@@ -67,10 +74,11 @@ struct DkvCfg {
   static_assert(DQK <= 256 && DV <= 256, "one MMA covers the accumulator columns");
 };
 
-template <int DQK, int DV, int BQ, int MODE, bool BF16, bool G_F32>
+template <int DQK, int DV, int BQ, int MODE, bool BF16, bool G_F32, bool WDS>
 __global__ void __launch_bounds__(384, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ DkvParams p) {
   using C = DkvCfg<DQK, DV, BQ, MODE>;
+  static_assert(!WDS || (C::kCanDs && BQ == 64), "dS stores");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sK = smem;
@@ -85,6 +93,7 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ uint64_t ld_full[2], ld_empty[2];
   __shared__ __align__(16) float s_lse2[2][BQ];
   __shared__ __align__(16) float s_d[2][C::kDK ? BQ : 4];
+  __shared__ int s_dsblk[2];  // dS path: block of the tile whose LSE / D are staged
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, skip_sh;
 
@@ -373,12 +382,71 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ LSE / D loader
+    // On the dS path this warp also walks the block table (block indexes fit
+    // in 32 bits, the host checks): ds_row is the first block of the current
+    // 128-row query tile ds_q128 of the current head, ds_kb0 / ds_nkb its
+    // first visible key block and their count, ds_head0 the first block of
+    // head g * grp, ds_tb the blocks of one head of this sequence.  With each
+    // tile's LSE and D it stages the index of the tile's dS block.
+    const bool wds = WDS && n_it > 0;
+    int ds_head0 = 0, ds_tb = 0, ds_row = 0, ds_q128 = 0, ds_kb0 = 0, ds_nkb = 0;
+    if (wds) {
+      ds_tb = (int)(p.plan[b + 1] - p.plan[b]);
+      ds_head0 = (int)((long long)p.hq * p.plan[b] + (long long)g * grp * ds_tb) +
+                 (int)blocks_row_prefix(sq, (qt0 * BQ) >> 7);  // whole warp
+      if constexpr (BQ == 64) {
+        // A visible block whose other 64-row half this CTA never visits (no
+        // query of that half sees a key of this tile) gets zeros there: the
+        // first tile's lower half, the last tile's upper half if it holds rows.
+        const int ql = qt0 + n_qt - 1;
+        const bool lo_gap = (qt0 & 1) != 0;
+        const bool hi_gap = (ql & 1) == 0 && (long long)(ql + 1) * 64 < sq.lq;
+        const int hi_off = hi_gap ? (int)(blocks_row_prefix(sq, ql >> 1) -
+                                          blocks_row_prefix(sq, qt0 >> 1))
+                                  : 0;  // whole warp
+        const uint64_t pol = l2_evict_first();
+        for (int half = 0; half < 2; ++half) {
+          if (!(half == 0 ? lo_gap : hi_gap)) continue;
+          int kb0;
+          const int nkb = wide_blocks_of_qtile(sq, half == 0 ? qt0 >> 1 : ql >> 1, kb0);
+          for (int hh = 0; hh < grp; ++hh) {
+            const int blk = ds_head0 + hh * ds_tb + (half ? hi_off : 0) + (ktile - kb0);
+            if (!(blk >= 0 && blk < p.cap && ktile >= kb0 && ktile < kb0 + nkb)) {
+              if (lane == 0) raise_status(p.status, DEV_WORKSPACE);  // inconsistent plan
+              continue;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.ds + (size_t)blk * kDsBlock + half * (kDsBlock / 2));
+            for (int t = lane; t < kDsBlock / 32; t += 32) st_global_hint(dst + t, make_uint4(0u, 0u, 0u, 0u), pol);
+          }
+        }
+      }
+    }
     bool ok = true;
     for (int it = 0; it < n_it && ok; ++it) {
       const int st = it & 1;
       if (!mbar_wait_warp(&ld_empty[st], ((it >> 1) & 1u) ^ 1u, ab)) break;
       const int h = g * grp + it / n_qt;
       const int q0 = (qt0 + it % n_qt) * BQ;
+      if constexpr (WDS) {
+        int blk = -1;
+        if (wds) {
+          if (it % n_qt == 0) {  // first tile of a head
+            ds_row = ds_head0 + (it / n_qt) * ds_tb;
+            ds_q128 = q0 >> 7;
+            ds_nkb = wide_blocks_of_qtile(sq, ds_q128, ds_kb0);
+          } else if ((q0 >> 7) != ds_q128) {
+            ds_row += ds_nkb;
+            ds_q128 = q0 >> 7;
+            ds_nkb = wide_blocks_of_qtile(sq, ds_q128, ds_kb0);
+          }
+          blk = ds_row + (ktile - ds_kb0);
+          if (!(blk >= 0 && blk < p.cap && ktile >= ds_kb0 && ktile < ds_kb0 + ds_nkb)) {
+            if (lane == 0) raise_status(p.status, DEV_WORKSPACE);  // inconsistent plan: no store
+            blk = -1;
+          }
+        }
+        if (lane == 0) s_dsblk[st] = blk;
+      }
       for (int t = lane; t < BQ; t += 32) {
         const int i = q0 + t;
         float l2 = INFINITY, dd = 0.0f;
@@ -406,6 +474,12 @@ __global__ void __launch_bounds__(384, 1)
     const long long vis_lo = (long long)j - sq.off - sq.R;
     long long vis_hi = (long long)j - sq.off + sq.L;
     if (vis_hi > sq.lq - 1) vis_hi = sq.lq - 1;
+    // dS path: a key row past the sequence sees no query, so its dS row is
+    // zero in the block (the dQ GEMM reads whole blocks, and the K rows it
+    // multiplies there may belong to the next packed sequence); such a tile
+    // takes the masked path
+    if (WDS && j >= sq.lk) vis_hi = -1;
+    const bool part_tile = WDS && k0 + kBlockM > sq.lk;
     const long long krow_last = min(k0 + kBlockM, sq.lk) - 1;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
@@ -437,7 +511,7 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       const int c0 = q0 + col0;  // first query row of this warpgroup's columns
-      const bool full_tile = ((long long)(c0 + C::kHalf - 1) <= sq.lq - 1) &&
+      const bool full_tile = !part_tile && ((long long)(c0 + C::kHalf - 1) <= sq.lq - 1) &&
                              ((long long)c0 >= krow_last - sq.off - sq.R) &&
                              ((long long)(c0 + C::kHalf - 1) <= (long long)k0 - sq.off + sq.L);
       const long long lo = vis_lo - c0, hi = vis_hi - c0;
@@ -449,6 +523,21 @@ __global__ void __launch_bounds__(384, 1)
       // per packed FP32 operation (shared memory holds -LSE log2 e and -D; the
       // softmax warps are bound by instruction issue)
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      // dS path: this thread's key row of dS^T goes into the block as 16-byte
+      // chunks of 8 queries, each stored as soon as it is computed so that the
+      // stores drain while the warp computes; a warp's 32 rows of one chunk
+      // are 512 contiguous bytes.  Written once and read once by the dQ GEMM:
+      // L2 evict-first, so the reused Q / dO tiles stay.
+      bool ds_on = false;
+      uint4* ds_dst = nullptr;
+      uint64_t ds_pol = 0;
+      if constexpr (WDS) {
+        const int dsb = s_dsblk[st];
+        ds_on = dsb >= 0;
+        ds_pol = l2_evict_first();
+        ds_dst = reinterpret_cast<uint4*>(p.ds + (size_t)(ds_on ? dsb : 0) * kDsBlock) + r +
+                 (((q0 + col0) & 127) >> 3) * (kDsChunk / 16);
+      }
 #pragma unroll
       for (int t4 = 0; t4 < C::kHalf / 4; ++t4) {
         const float4 la = l4[t4];
@@ -475,6 +564,13 @@ __global__ void __launch_bounds__(384, 1)
             float g0, g1;
             f2_unpack(f2_mul(f2_pack(e0, e1), f2_add(f2_pack(dp[t], dp[t + 1]), nd[u / 2])), g0, g1);
             pd[t / 2] = Pack<BF16>::two(g0, g1);
+          }
+        }
+        if constexpr (WDS) {
+          if ((t4 & 1) && ds_on) {
+            const int k = t4 >> 1;
+            st_global_hint(ds_dst + k * (kDsChunk / 16),
+                           make_uint4(pd[4 * k], pd[4 * k + 1], pd[4 * k + 2], pd[4 * k + 3]), ds_pol);
           }
         }
       }
@@ -570,16 +666,27 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int DQK, int DV, int BQ, int MODE, bool BF16, bool G_F32>
-static cudaError_t launch_dkv_t(const DkvParams& p, cudaStream_t st) {
+template <int DQK, int DV, int BQ, int MODE, bool BF16, bool G_F32, bool WDS>
+static cudaError_t launch_dkv_w(const DkvParams& p, cudaStream_t st) {
   using C = DkvCfg<DQK, DV, BQ, MODE>;
-  auto k = attn_bwd_dkdv_kernel<DQK, DV, BQ, MODE, BF16, G_F32>;
+  auto k = attn_bwd_dkdv_kernel<DQK, DV, BQ, MODE, BF16, G_F32, WDS>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid = tile_major(p.n_ktiles) ? dim3((unsigned)p.n_ktiles, (unsigned)p.hkv, (unsigned)p.batch)
                                       : dim3((unsigned)p.hkv, (unsigned)p.n_ktiles, (unsigned)p.batch);
   k<<<grid, 384, C::kSmem, st>>>(p);
   return cudaGetLastError();
+}
+
+// the dS-writing variant where the dS path runs (p.ds set), else without it
+template <int DQK, int DV, int BQ, int MODE, bool BF16, bool G_F32>
+static cudaError_t launch_dkv_t(const DkvParams& p, cudaStream_t st) {
+  if constexpr (DkvCfg<DQK, DV, BQ, MODE>::kCanDs) {
+    if (p.ds) return launch_dkv_w<DQK, DV, BQ, MODE, BF16, G_F32, true>(p, st);
+  } else {
+    if (p.ds) return cudaErrorInvalidValue;
+  }
+  return launch_dkv_w<DQK, DV, BQ, MODE, BF16, G_F32, false>(p, st);
 }
 
 template <int DQK, int DV, int BQ, int MODE>

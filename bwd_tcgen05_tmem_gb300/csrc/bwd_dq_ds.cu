@@ -1,0 +1,282 @@
+// bwd_dq_ds.cu -- dQ GEMM of the dS backward path (tcgen05 / TMEM / TMA).
+//
+// dQ_i = scale * sum_kb dS_{i,kb} K_kb  for one 128-row query tile i of one
+// (sequence, query head), over its visible 128-key blocks kb, with the dS
+// blocks the key-stationary dK/dV kernel wrote (layout in bwd.h) and K from
+// the caller's tensor (TransformerEngine PR #3510 backward chain: dQ = dS K;
+// PR #3699: the helper chain around it).  Every dQ element is produced by one
+// CTA, accumulated in TMEM in key-block order, so the result is bitwise
+// reproducible.
+//
+// The kernel streams 32 KiB of dS per 128-key block from HBM and multiplies
+// it by a K tile that the CTAs working on the same head share through L2:
+// per block, 128 x DQK x 128 MACs against 32 KiB, so it is bound by HBM
+// bandwidth (at DQK = 192, about 1.3 PFLOP/s at the measured copy bandwidth).
+// Four dS stages keep 128 KiB in flight per SM.
+//
+// Warp roles (192 threads): warp 0 producer (dS by bulk copy, K by TMA),
+// warp 1 TMEM owner and MMA issuer, warps 2..5 epilogue (TMEM lane quarter
+// warp & 3).  MMA per K-step of 16 keys: M = 128 queries, N = DQK, A = dS
+// (MN-major, unswizzled: 8-query groups SBO = 2 KiB apart, 8-key groups LBO =
+// 128 bytes apart), B = K (MN-major: head-dim contiguous, 128-byte swizzle,
+// 64-column chunks LBO apart).
+#include "bwd.h"
+
+namespace attn {
+
+template <int DQK>
+struct DqDsCfg {
+  static constexpr int kKCh = DQK / 64;
+  static constexpr int kKTile = kKCh * kSlotBytes;  // 128 keys x DQK
+  static constexpr int kDsStages = 4;
+  static constexpr int kBudget = 232448 - 1024 - 512;
+  static constexpr int kKStagesRaw = (kBudget - kDsStages * kDsBlock) / kKTile;
+  static constexpr int kKStages = kKStagesRaw > 4 ? 4 : kKStagesRaw;
+  static constexpr int kSmem = kDsStages * kDsBlock + kKStages * kKTile + 1024;
+  static constexpr int kTmemCols = DQK <= 64 ? 64 : (DQK <= 128 ? 128 : 256);
+  static_assert(DQK % 64 == 0 && DQK <= 256, "head dim");
+  static_assert(kKStages >= 2, "K stages");
+};
+
+template <int DQK, bool BF16, bool G_F32>
+__global__ void __launch_bounds__(192, 1) attn_bwd_dq_ds_kernel(const __grid_constant__ DqDsParams p) {
+  using C = DqDsCfg<DQK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sDs = smem;
+  uint8_t* sK = smem + C::kDsStages * kDsBlock;
+
+  __shared__ uint64_t ds_full[C::kDsStages], ds_empty[C::kDsStages];
+  __shared__ uint64_t k_full[C::kKStages], k_empty[C::kKStages];
+  __shared__ uint64_t acc_done, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag, skip_sh;
+
+  const int warp = threadIdx.x >> 5;
+  // (query tile, query head) in the grid order of tile_major(); under a
+  // causal mask the last query tiles are the heaviest and start first
+  const bool tmaj = tile_major(p.n_qtiles);
+  const int h = tmaj ? blockIdx.y : blockIdx.x;
+  const int qt = p.n_qtiles - 1 - (int)(tmaj ? blockIdx.x : blockIdx.y);
+  const int b = blockIdx.z;
+  const int g = h / (p.hq / p.hkv);
+  const int tb = p.geo.cu_q ? 0 : b;
+  const Seq sq = load_seq(p.geo, b);
+  const int q0 = qt * kBlockM;
+  if (q0 >= sq.lq) return;
+  int kb0;
+  const int n_kb = wide_blocks_of_qtile(sq, qt, kb0);
+
+  const unsigned long long lim = wait_limit(p.dbg);
+  const int drop = dropped_load(p.dbg);
+  Abort ab{&abort_flag, p.status, lim};
+  if (threadIdx.x == 0) {
+    const int status = p.status ? *(volatile int*)p.status : 0;
+    abort_flag = 0;
+    for (int i = 0; i < C::kDsStages; ++i) {
+      mbar_init(&ds_full[i], 1);
+      mbar_init(&ds_empty[i], 1);
+    }
+    for (int i = 0; i < C::kKStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    mbar_init(&acc_done, 1);
+    mbar_init(&drain_bar, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&p.tm_k);
+    skip_sh = status != 0;
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  if (skip_sh) {
+    if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+    return;
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // per key block: its dS block (one 32 KiB bulk copy, read once: L2
+    // evict-first), then the K tile; the whole warp runs the loop, one
+    // elected lane issues the copies
+    const long long T_b = p.plan[b + 1] - p.plan[b];
+    const long long first =
+        (long long)p.hq * p.plan[b] + (long long)h * T_b + blocks_row_prefix(sq, qt);  // whole warp
+    const uint64_t pol = l2_evict_first();
+    bool ok = true;
+    int n = 0;
+    if (n_kb > 0 && !(first >= 0 && first + n_kb <= p.cap)) {  // inconsistent plan
+      if (elect_sync()) {
+        raise_status(p.status, DEV_WORKSPACE);
+        *(volatile int*)&abort_flag = 1;
+      }
+      __syncwarp();
+      ok = false;
+    }
+    for (; n < n_kb && ok; ++n) {
+      const int s = n % C::kDsStages;
+      if (!mbar_wait_warp(&ds_empty[s], ((n / C::kDsStages) & 1) ^ 1, ab)) {
+        ok = false;
+        break;
+      }
+      if (n != drop && elect_sync()) {  // drop: test-only injected missing load
+        mbar_arrive_tx(&ds_full[s], kDsBlock);
+        bulk_load_hint(sDs + s * kDsBlock, p.blocks + (size_t)(first + n) * kDsBlock, kDsBlock,
+                       &ds_full[s], pol);
+      }
+      __syncwarp();
+      const int ks = n % C::kKStages;
+      if (!mbar_wait_warp(&k_empty[ks], ((n / C::kKStages) & 1) ^ 1, ab)) {
+        ok = false;
+        ++n;  // its dS copy is in flight
+        break;
+      }
+      int c1, c2, c3;
+      map_coords(p.ok, 0, g, sq.k_start + (kb0 + n) * kBlockN, tb, c1, c2, c3);
+      if (elect_sync()) {
+        mbar_arrive_tx(&k_full[ks], C::kKTile);
+#pragma unroll
+        for (int c = 0; c < C::kKCh; ++c)
+          tma_load_4d(sK + ks * C::kKTile + c * kSlotBytes, &p.tm_k, &k_full[ks], c * 64, c1, c2, c3);
+      }
+      __syncwarp();
+    }
+    // let the copies in flight land before the CTA can exit (a K copy was
+    // issued for every dS copy but the one a failed K wait broke off)
+    const int nk = ok ? n : n - 1;
+    for (int v = n > C::kDsStages ? n - C::kDsStages : 0; v < n; ++v)
+      mbar_wait_quiet(&ds_full[v % C::kDsStages], (v / C::kDsStages) & 1, lim);
+    for (int v = nk > C::kKStages ? nk - C::kKStages : 0; v < nk; ++v)
+      mbar_wait_quiet(&k_full[v % C::kKStages], (v / C::kKStages) & 1, lim);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = make_idesc(128, DQK, BF16, true, true);
+    const uint64_t adesc = make_sdesc_noswz(smem_u32(sDs), 128, kDsChunk);
+    const uint64_t bdesc = make_sdesc(smem_u32(sK), kSlotBytes, 1024);
+    bool ok = true;
+    for (int n = 0; n < n_kb && ok; ++n) {
+      const int s = n % C::kDsStages, ks = n % C::kKStages;
+      if (!mbar_wait_warp(&ds_full[s], (n / C::kDsStages) & 1, ab) ||
+          !mbar_wait_warp(&k_full[ks], (n / C::kKStages) & 1, ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t ad = adesc + (uint64_t)((s * kDsBlock) >> 4);
+      const uint64_t bd = bdesc + (uint64_t)((ks * C::kKTile) >> 4);
+      if (elect_sync()) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // 16 keys: dS advances 256 bytes, K two 1024-byte groups
+          mma_ss(tmem, ad + 16 * k, bd + 128 * k, idesc, (n | k) ? 1u : 0u);
+        mma_commit(&ds_empty[s]);
+        mma_commit(&k_empty[ks]);
+      }
+      __syncwarp();
+    }
+    if (elect_sync()) {
+      mma_commit(&acc_done);
+      mma_commit(&drain_bar);
+      mbar_wait_quiet(&drain_bar, 0, lim);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = wq * 32 + (threadIdx.x & 31);
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    bool ok = n_kb == 0 || mbar_wait_warp(&acc_done, 0, ab);
+    if (ok && *(volatile int*)&abort_flag) ok = false;  // partial sums: leave the output
+    if (ok) {
+      tc_fence_after();
+      const int i = q0 + r;
+      const bool valid = i < sq.lq;
+      const int64_t tok = (int64_t)sq.q_start + i;
+      char* orow = (char*)p.dq + ((int64_t)tb * p.sdq_b + tok * p.sdq_t + (int64_t)h * p.sdq_h) *
+                                     (G_F32 ? 4 : 2);
+      const float mul = p.scale;
+#pragma unroll 1
+      for (int c = 0; c < DQK / 32; ++c) {
+        uint32_t rr[32];
+        if (n_kb > 0) {
+          tmem_ld32(tmem + lane_off + c * 32, rr);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) rr[t] = 0u;
+        }
+        if (!valid) continue;
+        if (G_F32) {
+          float4* dst = reinterpret_cast<float4*>(orow + c * 32 * 4);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            float4 w = make_float4(__uint_as_float(rr[4 * t]) * mul, __uint_as_float(rr[4 * t + 1]) * mul,
+                                   __uint_as_float(rr[4 * t + 2]) * mul,
+                                   __uint_as_float(rr[4 * t + 3]) * mul);
+            if (p.accum) {  // sum into the caller's FP32 gradient
+              const float4 old = dst[t];
+              w.x += old.x;
+              w.y += old.y;
+              w.z += old.z;
+              w.w += old.w;
+            }
+            dst[t] = w;
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32 * 2);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            uint4 v;
+            v.x = Pack<BF16>::two(__uint_as_float(rr[8 * t + 0]) * mul, __uint_as_float(rr[8 * t + 1]) * mul);
+            v.y = Pack<BF16>::two(__uint_as_float(rr[8 * t + 2]) * mul, __uint_as_float(rr[8 * t + 3]) * mul);
+            v.z = Pack<BF16>::two(__uint_as_float(rr[8 * t + 4]) * mul, __uint_as_float(rr[8 * t + 5]) * mul);
+            v.w = Pack<BF16>::two(__uint_as_float(rr[8 * t + 6]) * mul, __uint_as_float(rr[8 * t + 7]) * mul);
+            dst[t] = v;
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+namespace {
+
+template <int DQK, bool BF16, bool G_F32>
+cudaError_t launch_dq_ds_t(const DqDsParams& p, cudaStream_t st) {
+  using C = DqDsCfg<DQK>;
+  auto k = attn_bwd_dq_ds_kernel<DQK, BF16, G_F32>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid = tile_major(p.n_qtiles) ? dim3((unsigned)p.n_qtiles, (unsigned)p.hq, (unsigned)p.batch)
+                                            : dim3((unsigned)p.hq, (unsigned)p.n_qtiles, (unsigned)p.batch);
+  k<<<grid, 192, C::kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DQK>
+cudaError_t launch_dq_ds_d(const DqDsParams& p, bool bf16, bool gf32, cudaStream_t st) {
+  if (bf16) return gf32 ? launch_dq_ds_t<DQK, true, true>(p, st) : launch_dq_ds_t<DQK, true, false>(p, st);
+  return gf32 ? launch_dq_ds_t<DQK, false, true>(p, st) : launch_dq_ds_t<DQK, false, false>(p, st);
+}
+
+}  // namespace
+
+cudaError_t launch_dq_ds(const DqDsParams& p, int dqk, bool bf16, bool gf32, cudaStream_t st) {
+  if (p.n_qtiles > 65535 || p.batch > 65535 || p.hq > 65535) return cudaErrorInvalidValue;
+  if (dqk == 64) return launch_dq_ds_d<64>(p, bf16, gf32, st);
+  if (dqk == 128) return launch_dq_ds_d<128>(p, bf16, gf32, st);
+  if (dqk == 192) return launch_dq_ds_d<192>(p, bf16, gf32, st);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace attn

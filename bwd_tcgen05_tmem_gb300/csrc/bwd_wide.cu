@@ -33,28 +33,6 @@
 
 namespace attn {
 
-namespace {
-
-// Blocks of query tiles [0, qt) of one sequence; called by a whole warp.
-__device__ long long wide_row_prefix(const Seq& s, int qt) {
-  long long acc = 0;
-  int kb0;
-  for (int t = (int)(threadIdx.x & 31); t < qt; t += 32) acc += wide_blocks_of_qtile(s, t, kb0);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  return acc;
-}
-
-__device__ __forceinline__ bool status_set(const int* status) {
-  return status && *(volatile const int*)status;
-}
-
-__device__ __forceinline__ void raise_status(int* status, int code) {
-  if (status) atomicCAS(status, DEV_OK, code);
-}
-
-}  // namespace
-
 // ------------------------------------------------------------------ planning
 // One CTA: per-sequence block counts, their exclusive prefix, capacity check.
 __global__ void __launch_bounds__(256) attn_wide_plan_kernel(const WidePlanParams p) {
@@ -89,6 +67,11 @@ __global__ void __launch_bounds__(256) attn_wide_plan_kernel(const WidePlanParam
     p.plan[p.batch] = carry;
     if (carry * (long long)p.hq > p.cap) raise_status(p.status, DEV_WORKSPACE);
   }
+}
+
+cudaError_t launch_wide_plan(const WidePlanParams& p, cudaStream_t st) {
+  attn_wide_plan_kernel<<<1, 256, 0, st>>>(p);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ scores
@@ -318,7 +301,7 @@ __global__ void __launch_bounds__(384, 1)
     long long vhi = (long long)i + sq.off + sq.R;
     if (vhi > sq.lk - 1) vhi = sq.lk - 1;
     const long long T_b = p.plan[b + 1] - p.plan[b];
-    const long long first = (long long)p.hq * p.plan[b] + (long long)h * T_b + wide_row_prefix(sq, qt);
+    const long long first = (long long)p.hq * p.plan[b] + (long long)h * T_b + blocks_row_prefix(sq, qt);
     bool ok = first >= 0 && first + n_kb <= p.cap;
     if (!ok) {  // inconsistent plan: stop every role of the CTA
       if (r == 0 && wg == 0) raise_status(p.status, DEV_WORKSPACE);
@@ -492,7 +475,7 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const long long T_b = p.plan[b + 1] - p.plan[b];
-    const long long pre0 = wide_row_prefix(sq, KIND == 0 ? tile : qt0);  // whole warp
+    const long long pre0 = blocks_row_prefix(sq, KIND == 0 ? tile : qt0);  // whole warp
     // the whole warp runs the loop (its values stay warp-uniform); one elected
     // lane issues the copies
     if (n_steps > 0) {
@@ -782,8 +765,7 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
     pl.batch = a.batch;
     pl.hq = a.hq;
     pl.status = a.status;
-    attn_wide_plan_kernel<<<1, 256, 0, st>>>(pl);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_wide_plan(pl, st)) != cudaSuccess) return e;
     ++*n_launches;
   }
   if ((stages & 2) && has_q) {

@@ -94,18 +94,44 @@ typedef struct {
                                seqused_q[b]); the rows up to cu_seqlens_q[b+1] are a gap
                                that no kernel reads or writes. */
   const int32_t* seqused_k; /* the same for keys/values; set both or neither */
+  int bwd_ds;              /* backward at head dims (128,128) and (192,128): 0 = auto
+                              (keep dS in the workspace at (192,128) when its blocks
+                              take at most 64 GiB), 1 = keep dS, -1 = never (recompute
+                              the scores for dQ: the smallest workspace).  See
+                              attn_bwd_path. */
 } attn_params_t;
 
 /* Bytes of workspace attn_fwd / attn_bwd need for `p` (always >= 256: the
  * status word lives at offset 0).  The workspace must be 256-byte aligned.
- * For head dims above 256 (and head dim 256 when that takes at most 16 GiB)
- * the backward also keeps P and dS of every visible
- * 128-query x 128-key tile (64 KiB each, all query heads) in the workspace:
- * the count is exact for dense inputs, and for THD it is a bound that takes
- * every document's keys as max_seqlen_k long (about 8.7 GB for batch 1,
- * 16 query heads, 16384 causal tokens). */
+ * On the ATTN_BWD_PDS path the backward also keeps P and dS of every visible
+ * 128-query x 128-key tile (64 KiB each, all query heads) in the workspace,
+ * on the ATTN_BWD_DS path dS alone (32 KiB each): the count is exact for
+ * dense inputs, and for THD it is a bound that takes every document's keys
+ * as max_seqlen_k long (P and dS: about 8.7 GB for batch 1, 16 query heads,
+ * 16384 causal tokens; dS: about 34.5 GB for batch 1, 32 query heads, 32768
+ * causal tokens). */
 size_t attn_fwd_workspace_size(const attn_params_t* p);
 size_t attn_bwd_workspace_size(const attn_params_t* p);
+
+/* The backward that attn_bwd runs for `p` (a pure function of `p`):
+ *   ATTN_BWD_RECOMPUTE  a query-stationary dQ kernel and a key-stationary
+ *                       dK/dV kernel that both compute S and dP;
+ *   ATTN_BWD_DS         head dims (192,128), and (128,128) with bwd_ds = 1
+ *                       (see bwd_ds): the dK/dV kernel also writes dS (16-bit)
+ *                       into the workspace and dQ = scale dS K is a GEMM over
+ *                       it, so S and dP are computed once per query-key pair;
+ *   ATTN_BWD_PDS        head dim 512, and 256 while its blocks take at most
+ *                       16 GiB: P and dS are written to the workspace and the
+ *                       five contractions run once each.
+ * All three give results within the same bound of the exact gradients, each
+ * bitwise reproducible; they differ in rounding order.  Returns -1 for
+ * invalid params. */
+typedef enum {
+  ATTN_BWD_RECOMPUTE = 0,
+  ATTN_BWD_DS = 1,
+  ATTN_BWD_PDS = 2
+} attn_bwd_path_t;
+int attn_bwd_path(const attn_params_t* p);
 
 /*
  * Forward (PR #3527): O = softmax(scale * Q K^T + mask) V per (sequence, query
@@ -127,11 +153,13 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
  * dQ = scale dS K; dK/dV are summed over the query heads of a GQA group
  * inside the kernel.  dq/dk/dv are fully overwritten (grad_dtype).  The
  * reduction order is fixed, so the backward is bitwise reproducible.
- * Head dim 512 (PR #3527: the d512 backward), and head dim 256 when its P/dS
- * blocks take at most 16 GiB: P and dS are written once to the
- * workspace (16-bit, as the fused kernels round them too) and the five
- * contractions run in three kernels; a workspace whose block table does not
- * fit sets ATTN_ERR_WORKSPACE in the status word.
+ * attn_bwd_path tells which kernels run.  On the ATTN_BWD_PDS path (head dim
+ * 512, PR #3527: the d512 backward; head dim 256 up to 16 GiB of blocks) P and
+ * dS are written once to the workspace (16-bit, as the fused kernels round
+ * them too) and the five contractions run in three kernels; on the
+ * ATTN_BWD_DS path the dK/dV kernel writes dS and a GEMM forms dQ from it.  A
+ * workspace whose block table does not fit sets ATTN_ERR_WORKSPACE in the
+ * status word.
  */
 attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, const void* v,
                        const void* o, const void* dout, const float* lse, void* dq, void* dk,
@@ -139,7 +167,8 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
 
 /*
  * The three stages of attn_bwd, callable one by one with the same arguments
- * (attn_bwd == preprocess, then dq, then dkdv, on one stream):
+ * (attn_bwd == preprocess, then dq, then dkdv, on one stream; on the
+ * ATTN_BWD_DS path preprocess, then dkdv, then dq):
  *   attn_bwd_preprocess: D = rowsum(dO * O) into the workspace; resets the
  *                        status word (PR #3699 "backward helper chain");
  *   attn_bwd_dq:         dQ (reads D from the workspace);
@@ -152,8 +181,10 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
  * materialises P and dS (head dim 512; head dim 256 up to 16 GiB of blocks)
  * the dq stage also writes them, with their block plan, into the workspace
  * and the dkdv stage reads them: it then requires the dq stage of the same
- * problem earlier on the stream as well.  Arguments a stage does not use may
- * be NULL.
+ * problem earlier on the stream as well.  On the ATTN_BWD_DS path it is the
+ * other way round: the dkdv stage writes dS and its block plan, and the dq
+ * stage requires the dkdv stage of the same problem earlier on the stream.
+ * Arguments a stage does not use may be NULL.
  */
 attn_status_t attn_bwd_preprocess(const attn_params_t* p, const void* q, const void* k,
                                   const void* v, const void* o, const void* dout,
@@ -183,7 +214,9 @@ attn_status_t attn_bwd_dkdv(const attn_params_t* p, const void* q, const void* k
  * loads the library, held until the process exits.  That covers problems
  * whose attn_bwd_workspace_size() is at most 8 MiB (about two million
  * query rows x query heads); larger ones return ATTN_ERR_WORKSPACE and
- * nothing is launched.  It calls no allocating routine.
+ * nothing is launched.  With bwd_ds = 0 it takes the ATTN_BWD_RECOMPUTE
+ * path (the ATTN_BWD_DS path's blocks rarely fit).  It calls no allocating
+ * routine.
  *
  * The first call on each device looks up the scratch area's device address
  * (with that device current) and caches it; make that first call before any

@@ -244,3 +244,55 @@ def test_host_stages_mask_validated(lib):
     for bad in (0, 8, 15):
         assert lib.attn_fwd_bwd_host_stages(ctypes.byref(p), *ptrs, ctypes.c_void_p(0x7000100),
                                             need, bad, None) == 1
+
+
+@pytest.mark.parametrize("dims,sq,sk,causal,wl,wr,br", [
+    ((192, 128), 300, 300, True, -1, -1, False), ((128, 128), 200, 333, True, -1, -1, True),
+    ((192, 128), 333, 200, True, -1, -1, True), ((128, 128), 300, 300, False, 100, 30, False),
+    ((192, 128), 700, 700, True, 129, 0, False), ((128, 128), 260, 260, False, -1, -1, False)])
+def test_ds_backward_workspace_counts_visible_blocks(lib, dims, sq, sk, causal, wl, wr, br):
+    """Head dims 128/128 and 192/128 keep dS: one 32 KiB block per visible
+    (query tile, key block) and query head, after the status word, D and the
+    per-sequence block prefix; bwd_ds = -1 leaves the status word and D."""
+    b, hq, hkv = 2, 4, 2
+    q, k, v = fake((b, sq, hq, dims[0])), fake((b, sk, hkv, dims[0])), fake((b, sk, hkv, dims[1]))
+    o = fake((b, sq, hq, dims[1]))
+    kw = dict(o=o, causal=causal, window=(wl, wr), bottom_right=br)
+    base = 256 + -(-(b * sq * hq * 4) // 256) * 256
+    blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
+    blocks = b * hq * _visible_blocks(sq, sk, causal, wl, wr, br)
+    p = attn.make_params(q, k, v, bwd_ds=1, **kw)
+    assert lib.attn_bwd_path(ctypes.byref(p)) == attn.BWD_DS
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == blk_off + blocks * 32768
+    p = attn.make_params(q, k, v, **kw)  # auto: 192/128 keeps dS, 128/128 recomputes
+    assert lib.attn_bwd_path(ctypes.byref(p)) == (attn.BWD_DS if dims[0] == 192 else
+                                                  attn.BWD_RECOMPUTE)
+    p = attn.make_params(q, k, v, bwd_ds=-1, **kw)
+    assert lib.attn_bwd_path(ctypes.byref(p)) == attn.BWD_RECOMPUTE
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == base
+
+
+@pytest.mark.parametrize("b,s,dims,mode,path", [
+    (1, 32768, (192, 128), 0, 1),    # 32 heads: 1,052,672 blocks, 34.5 GB: kept
+    (8, 32768, (192, 128), 0, 0),    # 276 GB of blocks: above the 64 GiB cap, recompute
+    (8, 32768, (192, 128), 1, 1),    # ... unless forced
+    (1, 32768, (128, 128), 0, 0),    # 128/128 recomputes by default
+    (1, 32768, (128, 128), 1, 1),
+    (1, 300, (64, 64), 0, 0),        # 64/64 always recomputes (cheaper than streaming dS)
+    (1, 300, (64, 64), 1, 0),
+    (1, 300, (256, 256), 0, 2),      # P and dS (the wide path)
+    (1, 300, (512, 512), -1, 2),
+    (1, 300, (192, 128), 2, -1),     # invalid bwd_ds
+])
+def test_bwd_path_selection(lib, b, s, dims, mode, path):
+    hq = 32
+    q, k = fake((b, s, hq, dims[0])), fake((b, s, hq, dims[0]))
+    v, o = fake((b, s, hq, dims[1])), fake((b, s, hq, dims[1]))
+    p = attn.make_params(q, k, v, o=o, causal=True, bwd_ds=mode)
+    assert lib.attn_bwd_path(ctypes.byref(p)) == path
+    if path == attn.BWD_DS:
+        nq = (s + 127) // 128
+        blocks = b * hq * nq * (nq + 1) // 2
+        base = 256 + -(-(b * s * hq * 4) // 256) * 256
+        blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
+        assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == blk_off + blocks * 32768

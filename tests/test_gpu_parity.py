@@ -36,7 +36,7 @@ def dense_inputs(b, sq, sk, hq, hkv, dqk, dv, dtype):
 
 
 def run_and_check(q, k, v, do, *, dtype, causal=True, window=(-1, -1), bottom_right=False,
-                  cu=None, max_len=None, backward=True):
+                  cu=None, max_len=None, backward=True, bwd_ds=0, grads=False):
     scale = 1.0 / math.sqrt(q.shape[-1])
     dev = "cuda"
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
@@ -52,11 +52,13 @@ def run_and_check(q, k, v, do, *, dtype, causal=True, window=(-1, -1), bottom_ri
     gate("o", o, ref.o, ref.floor["o"], report)
     check_lse(lse, ref.lse)
     if backward:
-        dq, dk, dv = attn.bwd(qd, kd, vd, o, dod, lse, **kw)
+        dq, dk, dv = attn.bwd(qd, kd, vd, o, dod, lse, bwd_ds=bwd_ds, **kw)
         torch.cuda.synchronize()
         for name, got, ex in (("dq", dq, ref.dq), ("dk", dk, ref.dk), ("dv", dv, ref.dv)):
             gate(name, got, ex, ref.floor[name], report)
             rel_l2(name, got, ex)
+        if grads:
+            report["grads"] = (dq, dk, dv)
     return report
 
 

@@ -30,15 +30,18 @@ pytestmark = pytest.mark.gpu
 WAIT_NS = 20_000_000  # 20 ms wait limit while a load is left out
 
 CASES = [
-    # id, (dqk, dv), hq, hkv, seqlen, kernel bit, dropped load
-    ("fwd-192", (192, 128), 2, 2, 300, attn.DEBUG_FWD, 1),
-    ("dq-192", (192, 128), 2, 2, 300, attn.DEBUG_DQ, 1),
-    ("dkdv-192", (192, 128), 2, 2, 300, attn.DEBUG_DKDV, 1),
-    ("dkdv-128-gqa", (128, 128), 4, 2, 300, attn.DEBUG_DKDV, 3),
-    ("fwd-512", (512, 512), 4, 1, 300, attn.DEBUG_FWD, 1),
-    ("scores-512", (512, 512), 4, 1, 300, attn.DEBUG_SCORES, 5),
-    ("wide-dq-512", (512, 512), 4, 1, 300, attn.DEBUG_DQ, 1),
-    ("wide-dkdv-512", (512, 512), 4, 1, 300, attn.DEBUG_DKDV, 1),
+    # id, (dqk, dv), hq, hkv, seqlen, kernel bit, dropped load, bwd_ds
+    ("fwd-192", (192, 128), 2, 2, 300, attn.DEBUG_FWD, 1, 0),
+    ("ds-dq-gemm-192", (192, 128), 2, 2, 300, attn.DEBUG_DQ, 1, 0),
+    ("ds-dkdv-192", (192, 128), 2, 2, 300, attn.DEBUG_DKDV, 1, 0),
+    ("dq-192", (192, 128), 2, 2, 300, attn.DEBUG_DQ, 1, -1),
+    ("dkdv-192", (192, 128), 2, 2, 300, attn.DEBUG_DKDV, 1, -1),
+    ("ds-dkdv-128-gqa", (128, 128), 4, 2, 300, attn.DEBUG_DKDV, 3, 1),
+    ("dkdv-128-gqa", (128, 128), 4, 2, 300, attn.DEBUG_DKDV, 3, 0),
+    ("fwd-512", (512, 512), 4, 1, 300, attn.DEBUG_FWD, 1, 0),
+    ("scores-512", (512, 512), 4, 1, 300, attn.DEBUG_SCORES, 5, 0),
+    ("wide-dq-512", (512, 512), 4, 1, 300, attn.DEBUG_DQ, 1, 0),
+    ("wide-dkdv-512", (512, 512), 4, 1, 300, attn.DEBUG_DKDV, 1, 0),
 ]
 
 
@@ -59,14 +62,15 @@ def _expect_timeout(ws):
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_expired_wait_reports_timeout_and_device_recovers(case):
-    _, dims, hq, hkv, s, bit, drop = case
+    _, dims, hq, hkv, s, bit, drop, mode = case
     q, k, v, do = dense_inputs(1, s, s, hq, hkv, dims[0], dims[1], "bf16")
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
     fws = torch.empty(attn.workspace_size("fwd", qd, kd, vd), dtype=torch.uint8, device="cuda")
-    bws = torch.empty(attn.workspace_size("bwd", qd, kd, vd), dtype=torch.uint8, device="cuda")
+    bws = torch.empty(attn.workspace_size("bwd", qd, kd, vd, bwd_ds=mode), dtype=torch.uint8,
+                      device="cuda")
     # results before the fault
     o, lse = attn.fwd(qd, kd, vd, workspace=fws)
-    g = attn.bwd(qd, kd, vd, o, dod, lse, workspace=bws)
+    g = attn.bwd(qd, kd, vd, o, dod, lse, workspace=bws, bwd_ds=mode)
     attn.query_status(bws)
     o, lse, g = o.clone(), lse.clone(), [t.clone() for t in g]
 
@@ -82,10 +86,12 @@ def test_expired_wait_reports_timeout_and_device_recovers(case):
         attn.query_status(fws)
     else:
         attn.debug_inject(bit, drop, WAIT_NS)
-        attn.bwd(qd, kd, vd, o, dod, lse, dq=g2[0], dk=g2[1], dv=g2[2], workspace=bws)
+        attn.bwd(qd, kd, vd, o, dod, lse, dq=g2[0], dk=g2[1], dv=g2[2], workspace=bws,
+                 bwd_ds=mode)
         _expect_timeout(bws)
         attn.fwd(qd, kd, vd, out=o2, lse=lse2, workspace=fws)
-        attn.bwd(qd, kd, vd, o, dod, lse, dq=g2[0], dk=g2[1], dv=g2[2], workspace=bws)
+        attn.bwd(qd, kd, vd, o, dod, lse, dq=g2[0], dk=g2[1], dv=g2[2], workspace=bws,
+                 bwd_ds=mode)
         attn.query_status(bws)
     torch.cuda.synchronize()
     assert torch.equal(o2, o) and torch.equal(lse2, lse)
