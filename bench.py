@@ -421,14 +421,18 @@ def main():
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     hkw = dict(bkw)
-    if w.is_thd:  # host metadata for the host-buffer call
-        hkw.update(cu_seqlens_q=inp["cu_seqlens"], cu_seqlens_k=inp["cu_seqlens"])
+    if w.is_thd:  # host metadata for the host-buffer call, pinned like the tensors (a
+        # copy from pageable memory would hold the host until its stream drains)
+        cu_h = inp["cu_seqlens"].pin_memory()
+        hkw.update(cu_seqlens_q=cu_h, cu_seqlens_k=cu_h)
     h_o, h_lse, h_dq, h_dk, h_dv = host_out[0]
     arena_bytes = attn.host_arena_size(*host_in, h_o, h_dq, h_dk, h_dv, **hkw)
     arenas = [torch.empty(arena_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
     up_s, comp_s, down_s = (torch.cuda.Stream(device=dev) for _ in range(3))
 
-    def e2e_run(n):
+    def e2e_run(n, spans=None):
+        # spans: per step and stage (upload, compute, download) a pair of
+        # timing events around the stage, to see where a step waits
         cur = torch.cuda.current_stream()
         for st_ in (up_s, comp_s, down_s):
             st_.wait_stream(cur)
@@ -436,18 +440,22 @@ def main():
         for s_ in range(n):
             a_ = s_ % 2
             args = (*host_in, *host_out[a_], arenas[a_])
-            if s_ >= 2:  # arena a_: step s_-2 has read its inputs
-                up_s.wait_event(ev[s_ - 2][1])
-            attn.fwd_bwd_host(*args, stream=up_s, stages=attn.HOST_UPLOAD, **hkw)
-            ev[s_][0].record(up_s)
-            comp_s.wait_event(ev[s_][0])
-            if s_ >= 2:  # and its outputs are downloaded
-                comp_s.wait_event(ev[s_ - 2][2])
-            attn.fwd_bwd_host(*args, stream=comp_s, stages=attn.HOST_COMPUTE, **hkw)
-            ev[s_][1].record(comp_s)
-            down_s.wait_event(ev[s_][1])
-            attn.fwd_bwd_host(*args, stream=down_s, stages=attn.HOST_DOWNLOAD, **hkw)
-            ev[s_][2].record(down_s)
+            for i_, (st_, stage) in enumerate(((up_s, attn.HOST_UPLOAD), (comp_s, attn.HOST_COMPUTE),
+                                               (down_s, attn.HOST_DOWNLOAD))):
+                if i_ == 0 and s_ >= 2:  # arena a_: step s_-2 has read its inputs
+                    up_s.wait_event(ev[s_ - 2][1])
+                if i_ == 1:
+                    comp_s.wait_event(ev[s_][0])
+                    if s_ >= 2:  # and its outputs are downloaded
+                        comp_s.wait_event(ev[s_ - 2][2])
+                if i_ == 2:
+                    down_s.wait_event(ev[s_][1])
+                if spans:
+                    spans[s_][i_][0].record(st_)
+                attn.fwd_bwd_host(*args, stream=st_, stages=stage, **hkw)
+                if spans:
+                    spans[s_][i_][1].record(st_)
+                ev[s_][i_].record(st_)
         for st_ in (up_s, comp_s, down_s):
             cur.wait_stream(st_)
 
@@ -460,11 +468,18 @@ def main():
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    spans = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(3)]
+             for _ in range(e2e_steps)]
     e0.record(stream)
-    e2e_run(e2e_steps)
+    e2e_run(e2e_steps, spans)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # mean stage durations, and the mean gap between consecutive compute stages
+    stage_ms = {name: statistics.mean(sp[i_][0].elapsed_time(sp[i_][1]) for sp in spans)
+                for i_, name in enumerate(("upload", "compute", "download"))}
+    stage_ms["compute_gap"] = (statistics.mean(spans[s_ - 1][1][1].elapsed_time(spans[s_][1][0])
+                                               for s_ in range(1, e2e_steps)))
     e2e_ms = max_over_ranks(e2e_ms, dev)
     for a_ in arenas:  # device-detected problems: forward, then backward status word
         attn.query_status(a_)
@@ -694,6 +709,7 @@ def main():
                          (2 * w.d_v * 2 + 4)) / (per_kernel["pre"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "e2e": {"value": job_tflops(fl["total"], e2e_ms, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "stage_ms": {k_: round(v_, 3) for k_, v_ in stage_ms.items()},
                 "steps": e2e_steps, "copy_only_gbs": copy_gbs,
                 "note": "C ABI attn_fwd_bwd_host_stages per step: inputs uploaded from "
                         "pinned host memory, forward + backward, all outputs downloaded; "

@@ -65,7 +65,11 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_lau
       qp.scale = a.scale;
       qp.status = a.status;
       qp.dbg = a.dbg_dq;
-      if ((e = launch_dq_ds(qp, a.dqk, a.bf16, a.g_f32, st)) != cudaSuccess) return e;
+      qp.counter = a.queue_counter;
+      if (qp.n_qtiles > 65535 || a.batch > 65535 || a.hq > 65535) return cudaErrorInvalidValue;
+      // the work-queue counter starts at zero for every launch
+      if ((e = cudaMemsetAsync(qp.counter, 0, sizeof(int), st)) != cudaSuccess) return e;
+      if ((e = launch_dq_ds(qp, a.dqk, a.bf16, a.g_f32, a.num_sms, st)) != cudaSuccess) return e;
       ++*n_launches;
     } else if (has_q && (stages & 2)) {
       DqParams dq;

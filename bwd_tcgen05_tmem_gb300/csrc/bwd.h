@@ -222,13 +222,15 @@ struct DqDsParams {
   int64_t sdq_b, sdq_t, sdq_h;
   int accum;
   int batch, hq, hkv, n_qtiles;
+  int* counter;  // work-queue counter (zeroed before the launch)
   float scale;
   int* status;
   DebugInject dbg;
 };
 
 cudaError_t launch_wide_plan(const WidePlanParams& p, cudaStream_t st);
-cudaError_t launch_dq_ds(const DqDsParams& p, int dqk, bool bf16, bool gf32, cudaStream_t st);
+cudaError_t launch_dq_ds(const DqDsParams& p, int dqk, bool bf16, bool gf32, int num_sms,
+                         cudaStream_t st);
 
 cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* n_launches);
 

@@ -251,8 +251,11 @@ attn_status_t attn_bwd_noalloc(const attn_params_t* p, const void* q, const void
  * then the backward's, then the device copies of all nine tensors.  So
  * attn_query_status(arena) reports device-detected problems of the forward and
  * attn_query_status((char*)arena + 256) those of the backward.  The call
- * returns once the work is enqueued.  Host buffers should be pinned (cudaHostAlloc / cudaHostRegister)
- * for the copies to be asynchronous; the inputs must not change and the
+ * returns once the work is enqueued.  Host buffers, and for THD the host
+ * cu_seqlens / seqused arrays, should be pinned (cudaHostAlloc /
+ * cudaHostRegister) for the copies to be asynchronous: a copy from pageable
+ * memory holds the calling thread until the stream has drained, which
+ * serialises a pipeline of steps on several streams.  The inputs must not change and the
  * outputs must not be read until the stream has passed the call.  Two calls on
  * two streams with two arenas overlap one step's copies with the other's
  * kernels.  A device pointer among the buffers is refused with
