@@ -98,16 +98,17 @@ def file_hash(name):
 
 def load_profile_value(fname, kernel):
     """A per-kernel figure from a committed ncu summary (`kernel value hash`
-    lines), or None if there is none or the kernel source changed since."""
+    lines; a stage may have one line per source file, e.g. the dq stage of each
+    backward path), or None if there is none for the kernel's current source."""
     path = os.path.join(ROOT, "profiles", fname)
     if not os.path.exists(path):
         return None
+    want = file_hash(KERNEL_SOURCES[kernel.split("+")[0]])
     with open(path) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 3 and parts[0] == kernel and not line.startswith("#"):
-                if parts[2] != file_hash(KERNEL_SOURCES[kernel]):
-                    return None
+            if (len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel and
+                    parts[2] == want):
                 return float(parts[1])
     return None
 
@@ -649,7 +650,11 @@ def main():
     peak_sus = peaks.get("bf16_tflops_sustained", peak_tf)
     dom = max(("fwd", "dq", "dkdv"), key=lambda s: per_kernel[s])
     ach = fl["kernel"][dom] / (per_kernel[dom] * 1e-3) / 1e12
-    traffic = load_traffic(dom)
+
+    def pkey(k_):  # the profile entry of a kernel: the dK/dV kernel that writes dS has its own
+        return k_ + "+ds" if (k_ == "dkdv" and bwd_path == attn.BWD_DS) else k_
+
+    traffic = load_traffic(pkey(dom))
     value = job_tflops(fl["total"], ms, world)
     lens_b = ((inp["cu_seqlens"][1:] - inp["cu_seqlens"][:-1]).tolist() if w.is_thd else None)
     rows_q = q.shape[0] * (1 if w.is_thd else q.shape[1])
@@ -689,7 +694,10 @@ def main():
                      "peak_source": f"{peak_src} bf16_tflops (burst)",
                      "peak_sustained": peak_sus, "frac_sustained": ach / peak_sus,
                      "sm_mhz": clocks.get("sm_mhz"),
-                     "work_per_launch": fl["kernel"][dom]},
+                     "work_per_launch": fl["kernel"][dom],
+                     # on the dS path the dK/dV kernel also streams the dS blocks out
+                     "ds_write_bytes": (score_blocks(w, lens_b) * 32768
+                                        if bwd_path == attn.BWD_DS and dom == "dkdv" else None)},
         "bwd_path": {attn.BWD_RECOMPUTE: "recompute", attn.BWD_DS: "ds",
                      attn.BWD_PDS: "pds"}[bwd_path],
         "dq_gemm_hbm": None if bwd_path != attn.BWD_DS else {
@@ -701,7 +709,7 @@ def main():
         "kernels": {k_: {"ms": per_kernel[k_],
                          "tflops": fl["kernel"][k_] / (per_kernel[k_] * 1e-3) / 1e12,
                          "frac": fl["kernel"][k_] / (per_kernel[k_] * 1e-3) / 1e12 / peak_tf,
-                         "tensor_pipe_pct": load_tensor_pipe(k_)}
+                         "tensor_pipe_pct": load_tensor_pipe(pkey(k_))}
                     for k_ in ("fwd", "dq", "dkdv")},
         "pre_gbs": (q.shape[0] * (1 if w.is_thd else q.shape[1]) * w.heads_q * (2 * w.d_v * 2 + 4)) /
                    (per_kernel["pre"] * 1e-3) / 1e9,
