@@ -44,17 +44,22 @@ __global__ void __launch_bounds__(256) attn_pre_kernel(const PreParams p) {
         const uint32_t r32 = (uint32_t)r;
         const int h = (int)(r32 % (uint32_t)p.hq);
         const uint32_t t = r32 / (uint32_t)p.hq;  // token (dense: b*S + i)
-        int b;
+        int b = 0;
         int64_t tok;
-        if (p.cu_q) {  // the sequence that owns token t
-          int lo = 0, hi = p.batch;
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if ((uint32_t)p.cu_q[mid] <= t) lo = mid; else hi = mid;
-          }
-          b = lo;
+        if (p.cu_q) {
+          // packed rows are addressed by token alone (D has no batch stride);
+          // only a padded layout needs the sequence that owns token t, to
+          // leave its gap rows alone
           tok = t;
-          if (p.used_q && (int64_t)t - p.cu_q[b] >= p.used_q[b]) continue;  // a gap row: no D
+          if (p.used_q) {
+            int lo = 0, hi = p.batch;
+            while (hi - lo > 1) {
+              const int mid = (lo + hi) >> 1;
+              if ((uint32_t)p.cu_q[mid] <= t) lo = mid; else hi = mid;
+            }
+            b = lo;
+            if ((int64_t)t - p.cu_q[b] >= p.used_q[b]) continue;  // a gap row: no D
+          }
         } else {
           b = (int)(t / (uint32_t)p.seqlen_q);
           tok = t - (uint32_t)b * (uint32_t)p.seqlen_q;
