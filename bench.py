@@ -711,10 +711,11 @@ def main():
                          "frac": fl["kernel"][k_] / (per_kernel[k_] * 1e-3) / 1e12 / peak_tf,
                          "tensor_pipe_pct": load_tensor_pipe(pkey(k_))}
                     for k_ in ("fwd", "dq", "dkdv")},
-        "pre_gbs": (q.shape[0] * (1 if w.is_thd else q.shape[1]) * w.heads_q * (2 * w.d_v * 2 + 4)) /
+        # D preprocess: O and dO read, LSE read, {LSE log2 e, D} written, per row
+        "pre_gbs": (q.shape[0] * (1 if w.is_thd else q.shape[1]) * w.heads_q * (2 * w.d_v * 2 + 12)) /
                    (per_kernel["pre"] * 1e-3) / 1e9,
         "pre_hbm_frac": (q.shape[0] * (1 if w.is_thd else q.shape[1]) * w.heads_q *
-                         (2 * w.d_v * 2 + 4)) / (per_kernel["pre"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                         (2 * w.d_v * 2 + 12)) / (per_kernel["pre"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "e2e": {"value": job_tflops(fl["total"], e2e_ms, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "stage_ms": {k_: round(v_, 3) for k_, v_ in stage_ms.items()},

@@ -236,7 +236,8 @@ attn_status_t launch_check_if_thd(const attn_params_t* p, int* status, cudaStrea
   return ATTN_OK;
 }
 
-// Backward workspace: [status][D: rows x heads_q fp32] and, on the PDS and
+// Backward workspace: [status][row statistics: rows x heads_q x {LSE * log2 e,
+// D} fp32] and, on the PDS and
 // DS paths, [per-sequence block prefix][64 KiB P/dS or 32 KiB dS blocks].
 struct BwdLayout {
   size_t d_off, plan_off, blk_off, total;
@@ -283,7 +284,8 @@ BwdLayout bwd_layout(const attn_params_t* p) {
   BwdLayout l;
   memset(&l, 0, sizeof(l));
   const int64_t rq = rows_q(p);
-  const size_t d_bytes = (size_t)(rq > 0 ? rq : 0) * (size_t)(p->heads_q > 0 ? p->heads_q : 0) * 4;
+  // per row (token, query head) {LSE * log2 e, D}: two floats
+  const size_t d_bytes = (size_t)(rq > 0 ? rq : 0) * (size_t)(p->heads_q > 0 ? p->heads_q : 0) * 8;
   l.d_off = kStatusBytes;
   l.total = l.d_off + ((d_bytes + 255) / 256) * 256;
   const bool w = wide(p);
@@ -414,8 +416,9 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
     if ((s = check_tensor("q", q, p->stride_q, p, 2, has_q))) return s;
     if ((s = check_tensor("k", k, p->stride_k, p, 2, has_k))) return s;
     if ((s = check_tensor("v", v, p->stride_v, p, 2, has_k))) return s;
-    if (has_q && !lse) return fail(ATTN_ERR_INVALID_ARG, "lse is NULL");
   }
+  // the preprocess stores each row's LSE beside D; the later stages read them there
+  if (pre && has_q && !lse) return fail(ATTN_ERR_INVALID_ARG, "lse is NULL");
   if (pre && (s = check_tensor("o", o, p->stride_o, p, 2, has_q))) return s;
   if ((s = check_tensor("dout", dout, p->stride_do, p, 2, has_q))) return s;
   if (sdq && (s = check_tensor("dq", dq, p->stride_dq, p, ge, has_q))) return s;
@@ -447,7 +450,7 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
   }
   int* status = (int*)ws;
   const BwdLayout lay = bwd_layout(p);
-  float* dbuf = (float*)((char*)ws + lay.d_off);
+  float2* dbuf = (float2*)((char*)ws + lay.d_off);
   cudaError_t e;
   if (pre) {
     e = cudaMemsetAsync(status, 0, sizeof(int), st);

@@ -29,6 +29,9 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_lau
     pp.o = a.o;
     pp.dout = a.dout;
     pp.d = a.d;
+    pp.lse = a.lse;
+    pp.lse_sb = a.lse_sb;
+    pp.lse_sh = a.lse_sh;
     pp.cu_q = a.thd ? a.geo.cu_q : nullptr;
     pp.used_q = a.thd ? a.geo.used_q : nullptr;
     pp.so_b = a.so[0]; pp.so_t = a.so[1]; pp.so_h = a.so[2];
@@ -83,9 +86,6 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_lau
       dq.ok = has_k ? a.ok : a.oq;
       dq.ov = has_k ? a.ov : a.oq;
       dq.geo = a.geo;
-      dq.lse = a.lse;
-      dq.lse_sb = a.lse_sb;
-      dq.lse_sh = a.lse_sh;
       dq.d = a.d;
       dq.d_sb = a.d_sb;
       dq.d_sh = a.d_sh;
@@ -135,9 +135,6 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st, int stages, int* n_lau
         kp.oq = has_q ? a.oq : a.ok;
         kp.odo = has_q ? a.odo : a.ok;
         kp.geo = a.geo;
-        kp.lse = a.lse;
-        kp.lse_sb = a.lse_sb;
-        kp.lse_sh = a.lse_sh;
         kp.d = a.d;
         kp.d_sb = a.d_sb;
         kp.d_sh = a.d_sh;

@@ -18,7 +18,10 @@ struct BwdArgs {
   int* queue_counter;  // work-queue counter in the workspace (persistent kernels)
   const float* lse;
   int64_t lse_sb, lse_sh;
-  float* d;
+  // per row {LSE * log2 e (+inf for a row without keys), D}: written by the
+  // preprocess, the only row statistics the backward kernels read (one array
+  // read in lockstep, wherever the caller's LSE lives)
+  float2* d;
   int64_t d_sb, d_sh;
   const void *q, *k, *v, *o, *dout;
   void *dq, *dk, *dvp;
@@ -134,9 +137,7 @@ struct WideScoresParams {
   CUtensorMap tm_q, tm_k, tm_v;  // 128-row boxes
   MapOrder oq, ok, ov;
   Geometry geo;
-  const float* lse;
-  int64_t lse_sb, lse_sh;
-  const float* d;
+  const float2* d;  // per row {LSE * log2 e, D} (the preprocess writes it)
   int64_t d_sb, d_sh;
   const void* dout;
   int64_t sdo_b, sdo_t, sdo_h;
@@ -174,9 +175,7 @@ struct DqParams {
   CUtensorMap tm_q, tm_do, tm_k, tm_v;  // q/do: 128-row boxes, k/v: BKV-row boxes
   MapOrder oq, odo, ok, ov;
   Geometry geo;
-  const float* lse;
-  int64_t lse_sb, lse_sh;
-  const float* d;
+  const float2* d;  // per row {LSE * log2 e, D} (the preprocess writes it)
   int64_t d_sb, d_sh;
   void* dq;
   int64_t sdq_b, sdq_t, sdq_h;
@@ -193,9 +192,7 @@ struct DkvParams {
   CUtensorMap tm_k, tm_v, tm_q, tm_do;  // k/v: 128-row boxes, q/do: BQ-row boxes
   MapOrder ok, ov, oq, odo;
   Geometry geo;
-  const float* lse;
-  int64_t lse_sb, lse_sh;
-  const float* d;
+  const float2* d;  // per row {LSE * log2 e, D} (the preprocess writes it)
   int64_t d_sb, d_sh;
   void *dk, *dv;
   int64_t sdk_b, sdk_t, sdk_h, sdv_b, sdv_t, sdv_h;

@@ -450,11 +450,11 @@ __global__ void __launch_bounds__(384, 1)
       for (int t = lane; t < BQ; t += 32) {
         const int i = q0 + t;
         float l2 = INFINITY, dd = 0.0f;
-        if (i < sq.lq) {
+        if (i < sq.lq) {  // LSE * log2 e (+inf for a keyless row: masked anyway) and D
           const int64_t tok = (int64_t)sq.q_start + i;
-          l2 = p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + tok] * 1.4426950408889634f;
-          dd = p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok];
-          if (l2 == -INFINITY) l2 = INFINITY;  // keyless query row: masked anyway
+          const float2 st = p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok];
+          l2 = st.x;
+          dd = st.y;
         }
         s_lse2[st][t] = -l2;  // negated: the softmax adds them
         s_d[st][t] = -dd;

@@ -360,11 +360,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int i = q0 + r;
       const int64_t tok = (int64_t)sq.q_start + i;
       float lse2 = INFINITY, Dr = 0.0f;
-      if (i < sq.lq) {
-        lse2 = p.lse[(int64_t)it.b * p.lse_sb + (int64_t)it.h * p.lse_sh + tok] *
-               1.4426950408889634f;
-        Dr = p.d[(int64_t)it.b * p.d_sb + (int64_t)it.h * p.d_sh + tok];
-        if (lse2 == -INFINITY) lse2 = INFINITY;  // keyless row: every key is masked anyway
+      if (i < sq.lq) {  // LSE * log2 e (+inf for a keyless row: every key is masked) and D
+        const float2 st = p.d[(int64_t)it.b * p.d_sb + (int64_t)it.h * p.d_sh + tok];
+        lse2 = st.x;
+        Dr = st.y;
       }
       const long long vis_lo = (long long)i + sq.off - sq.L;
       long long vis_hi = (long long)i + sq.off + sq.R;

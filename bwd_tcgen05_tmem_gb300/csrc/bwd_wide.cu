@@ -268,10 +268,10 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const int64_t tok = (int64_t)sq.q_start + i;
     float l2 = INFINITY, dd = 0.0f;  // rows past the end: P = dS = 0
-    if (valid) {
-      l2 = p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + tok] * 1.4426950408889634f;
-      if (l2 == -INFINITY) l2 = INFINITY;  // keyless row
-      dd = p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok];
+    if (valid) {  // LSE * log2 e (+inf for a keyless row) and D
+      const float2 st = p.d[(int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok];
+      l2 = st.x;
+      dd = st.y;
     }
     // dO row (this warpgroup's half of the columns) into TMEM
     {
@@ -739,6 +739,9 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
       pp.o = a.o;
       pp.dout = a.dout;
       pp.d = a.d;
+      pp.lse = a.lse;
+      pp.lse_sb = a.lse_sb;
+      pp.lse_sh = a.lse_sh;
       pp.cu_q = a.thd ? a.geo.cu_q : nullptr;
       pp.used_q = a.thd ? a.geo.used_q : nullptr;
       pp.so_b = a.so[0]; pp.so_t = a.so[1]; pp.so_h = a.so[2];
@@ -778,9 +781,6 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, cudaStream_t st, int stages, int* 
       sp.ok = a.ok;
       sp.ov = a.ov;
       sp.geo = a.geo;
-      sp.lse = a.lse;
-      sp.lse_sb = a.lse_sb;
-      sp.lse_sh = a.lse_sh;
       sp.d = a.d;
       sp.d_sb = a.d_sb;
       sp.d_sh = a.d_sh;

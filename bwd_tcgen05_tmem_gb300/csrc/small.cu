@@ -1,6 +1,8 @@
 // small.cu -- the memory-bound kernels of the attention path:
-//   * attn_pre_kernel:   D[b,h,i] = sum_c dO[i,h,c] * O[i,h,c] in FP32
-//                        (TransformerEngine PR #3699: the backward helper chain);
+//   * attn_pre_kernel:   D[b,h,i] = sum_c dO[i,h,c] * O[i,h,c] in FP32, stored
+//                        with the row's LSE in base 2 as the pair the backward
+//                        kernels read (TransformerEngine PR #3699: the backward
+//                        helper chain);
 //   * attn_merge_kernel: LSE-weighted merge of partial results
 //                        (PR #3527: the context-parallel ring correction);
 //   * attn_check_kernel: device validation of cu_seqlens (PR #3699: every
@@ -33,10 +35,12 @@ __global__ void __launch_bounds__(256) attn_pre_kernel(const PreParams p) {
        base += nwarps * (kRowsPerPass * kU)) {
     uint4 ov[kU][NCH], dv[kU][NCH];
     int64_t didx[kU];
+    float lsev[kU];  // the row's LSE, loaded with its O / dO vectors
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int64_t r = base + u * kRowsPerPass + sub;
       didx[u] = -1;
+      lsev[u] = 0.0f;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) ov[u][c] = dv[u][c] = make_uint4(0u, 0u, 0u, 0u);
       if (r < rows) {
@@ -75,6 +79,7 @@ __global__ void __launch_bounds__(256) attn_pre_kernel(const PreParams p) {
           dv[u][c] = drow[c * LPR + l];
         }
         didx[u] = (int64_t)b * p.d_sb + (int64_t)h * p.d_sh + tok;
+        if (l == 0) lsev[u] = p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + tok];
       }
     }
 #pragma unroll
@@ -89,7 +94,11 @@ __global__ void __launch_bounds__(256) attn_pre_kernel(const PreParams p) {
       }
 #pragma unroll
       for (int s = LPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-      if (l == 0 && didx[u] >= 0) p.d[didx[u]] = acc;
+      if (l == 0 && didx[u] >= 0) {
+        float l2 = lsev[u] * 1.4426950408889634f;
+        if (l2 == -INFINITY) l2 = INFINITY;  // keyless row: every key is masked anyway
+        p.d[didx[u]] = make_float2(l2, acc);
+      }
     }
   }
 }

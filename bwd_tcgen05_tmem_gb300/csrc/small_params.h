@@ -9,11 +9,15 @@ namespace attn {
 struct PreParams {
   const void* o;
   const void* dout;
-  float* d;             // D in the LSE layout
+  // per row (token, query head), in the LSE layout: {LSE * log2 e (+inf
+  // for a row without keys), D}, what the backward kernels read together
+  float2* d;
+  const float* lse;
+  int64_t lse_sb, lse_sh;  // LSE index = b*lse_sb + h*lse_sh + token
   const int32_t* cu_q;  // null: dense
   const int32_t* used_q;  // padded THD: rows past used_q[b] are a gap (skipped)
   int64_t so_b, so_t, so_h, sdo_b, sdo_t, sdo_h;
-  int64_t d_sb, d_sh;   // D index = b*d_sb + h*d_sh + token
+  int64_t d_sb, d_sh;   // row statistics index = b*d_sb + h*d_sh + token
   int batch, seqlen_q, total_q, hq, dv;
   int* status;
 };

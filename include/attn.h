@@ -148,7 +148,8 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
 /*
  * Backward (PR #3510 head-parallel backward, PR #3699 helper chain): from Q,
  * K, V, O, dO and the forward's LSE computes D = rowsum(dO * O) (FP32, kept in
- * the workspace), then per visible tile P = exp(scale QK^T - LSE),
+ * the workspace beside each row's LSE in base 2, the pair the later kernels
+ * read), then per visible tile P = exp(scale QK^T - LSE),
  * dP = dO V^T, dS = P (dP - D), dV = P^T dO, dK = scale dS^T Q,
  * dQ = scale dS K; dK/dV are summed over the query heads of a GQA group
  * inside the kernel.  dq/dk/dv are fully overwritten (grad_dtype).  The
@@ -169,15 +170,18 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
  * The three stages of attn_bwd, callable one by one with the same arguments
  * (attn_bwd == preprocess, then dq, then dkdv, on one stream; on the
  * ATTN_BWD_DS path preprocess, then dkdv, then dq):
- *   attn_bwd_preprocess: D = rowsum(dO * O) into the workspace; resets the
- *                        status word (PR #3699 "backward helper chain");
- *   attn_bwd_dq:         dQ (reads D from the workspace);
- *   attn_bwd_dkdv:       dK and dV, reduced over each GQA group (reads D).
+ *   attn_bwd_preprocess: D = rowsum(dO * O) and LSE * log2 e per query row
+ *                        into the workspace; resets the status word (PR #3699
+ *                        "backward helper chain");
+ *   attn_bwd_dq:         dQ (reads D and LSE from the workspace);
+ *   attn_bwd_dkdv:       dK and dV, reduced over each GQA group (reads D and
+ *                        LSE from the workspace).
  * The dq and dkdv stages require a preprocess earlier on the stream, on the
- * same workspace, for a problem with the same query rows, query heads, dtype
- * and batch/cu_seqlens_q layout: D depends only on O and dO of each query
- * row, so one preprocess serves several calls that differ only in their keys,
- * mask or window (a context-parallel ring does this).  Where the backward
+ * same workspace, for a problem with the same query rows, query heads, dtype,
+ * batch/cu_seqlens_q layout and LSE: D and LSE depend only on each query row,
+ * so one preprocess serves several calls that differ only in their keys, mask
+ * or window (a context-parallel ring does this; its LSE is the merged one).
+ * The dq and dkdv stages ignore their `lse` argument.  Where the backward
  * materialises P and dS (head dim 512; head dim 256 up to 16 GiB of blocks)
  * the dq stage also writes them, with their block plan, into the workspace
  * and the dkdv stage reads them: it then requires the dq stage of the same
@@ -212,7 +216,7 @@ attn_status_t attn_bwd_dkdv(const attn_params_t* p, const void* q, const void* k
  * arguments as attn_bwd minus the workspace and uses instead a scratch area
  * that the library reserves statically: 8 MiB of device memory per GPU that
  * loads the library, held until the process exits.  That covers problems
- * whose attn_bwd_workspace_size() is at most 8 MiB (about two million
+ * whose attn_bwd_workspace_size() is at most 8 MiB (about one million
  * query rows x query heads); larger ones return ATTN_ERR_WORKSPACE and
  * nothing is launched.  With bwd_ds = 0 it takes the ATTN_BWD_RECOMPUTE
  * path (the ATTN_BWD_DS path's blocks rarely fit).  It calls no allocating

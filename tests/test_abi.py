@@ -91,7 +91,7 @@ def test_workspace_sizes(lib):
     p = base_params()
     assert lib.attn_fwd_workspace_size(ctypes.byref(p)) >= 256
     need = lib.attn_bwd_workspace_size(ctypes.byref(p))
-    assert need >= 256 + 2 * 4 * 256 * 4  # status word + D for every query row
+    assert need >= 256 + 2 * 4 * 256 * 8  # status word + {LSE log2 e, D} for every query row
 
 
 def test_merge_validation(lib):
@@ -136,7 +136,7 @@ def test_wide_backward_workspace_counts_visible_blocks(lib, sq, sk, causal, wl, 
     b, hq, hkv = 2, 4, 2
     q, k = fake((b, sq, hq, 512)), fake((b, sk, hkv, 512))
     p = attn.make_params(q, k, k, o=q, causal=causal, window=(wl, wr), bottom_right=br)
-    base = 256 + -(-(b * sq * hq * 4) // 256) * 256
+    base = 256 + -(-(b * sq * hq * 8) // 256) * 256
     blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
     blocks = b * hq * _visible_blocks(sq, sk, causal, wl, wr, br)
     assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == blk_off + blocks * 65536
@@ -183,7 +183,7 @@ def test_d256_backward_route_by_block_bytes(lib, s, window, wide):
     b, hq, hkv = 1, 4, 1
     q, k = fake((b, s, hq, 256)), fake((b, s, hkv, 256))
     p = attn.make_params(q, k, k, o=q, causal=True, window=window)
-    base = 256 + -(-(b * s * hq * 4) // 256) * 256
+    base = 256 + -(-(b * s * hq * 8) // 256) * 256
     need = lib.attn_bwd_workspace_size(ctypes.byref(p))
     if not wide:
         assert need == base
@@ -258,7 +258,7 @@ def test_ds_backward_workspace_counts_visible_blocks(lib, dims, sq, sk, causal, 
     q, k, v = fake((b, sq, hq, dims[0])), fake((b, sk, hkv, dims[0])), fake((b, sk, hkv, dims[1]))
     o = fake((b, sq, hq, dims[1]))
     kw = dict(o=o, causal=causal, window=(wl, wr), bottom_right=br)
-    base = 256 + -(-(b * sq * hq * 4) // 256) * 256
+    base = 256 + -(-(b * sq * hq * 8) // 256) * 256
     blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
     blocks = b * hq * _visible_blocks(sq, sk, causal, wl, wr, br)
     p = attn.make_params(q, k, v, bwd_ds=1, **kw)
@@ -293,6 +293,6 @@ def test_bwd_path_selection(lib, b, s, dims, mode, path):
     if path == attn.BWD_DS:
         nq = (s + 127) // 128
         blocks = b * hq * nq * (nq + 1) // 2
-        base = 256 + -(-(b * s * hq * 4) // 256) * 256
+        base = 256 + -(-(b * s * hq * 8) // 256) * 256
         blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
         assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == blk_off + blocks * 32768

@@ -57,7 +57,7 @@ def test_noalloc_backward_matches_attn_bwd_twice(shape):
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
-    # 2 x 4096 x 300 (rows x query heads) x 4 bytes of D exceeds the 8 MiB area
+    # 2 x 4096 x 300 (rows x query heads) x 8 bytes of row statistics exceed the 8 MiB area
     q = torch.empty((2, 4096, 300, 64), dtype=torch.bfloat16, device="meta")
     p = attn.make_params(q, q, q)
     lib = attn.load()
