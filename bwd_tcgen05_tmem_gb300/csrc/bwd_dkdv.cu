@@ -180,11 +180,11 @@ __global__ void __launch_bounds__(384, 1)
     // loop (indices stay warp-uniform); one elected lane issues the copies
     if (n_it > 0) {
       uint32_t rcnt = 0;
-      int it = 0;
+      int it = 0, hh = 0, tq = 0;  // iteration it = head hh of the group, query tile tq
       bool ok = true;
-      for (; it < n_it && ok; ++it) {
-        const int h = g * grp + it / n_qt;
-        const int qrow = sq.q_start + (qt0 + it % n_qt) * BQ;
+      for (; it < n_it && ok; ++it, (++tq == n_qt) ? (tq = 0, ++hh) : 0) {
+        const int h = g * grp + hh;
+        const int qrow = sq.q_start + (qt0 + tq) * BQ;
         int qc1, qc2, qc3, dc1, dc2, dc3;
         map_coords(p.oq, 0, h, qrow, tb, qc1, qc2, qc3);
         map_coords(p.odo, 0, h, qrow, tb, dc1, dc2, dc3);
@@ -422,16 +422,17 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
     bool ok = true;
-    for (int it = 0; it < n_it && ok; ++it) {
+    int hh = 0, tq = 0;  // iteration it = head hh of the group, query tile tq
+    for (int it = 0; it < n_it && ok; ++it, (++tq == n_qt) ? (tq = 0, ++hh) : 0) {
       const int st = it & 1;
       if (!mbar_wait_warp(&ld_empty[st], ((it >> 1) & 1u) ^ 1u, ab)) break;
-      const int h = g * grp + it / n_qt;
-      const int q0 = (qt0 + it % n_qt) * BQ;
+      const int h = g * grp + hh;
+      const int q0 = (qt0 + tq) * BQ;
       if constexpr (WDS) {
         int blk = -1;
         if (wds) {
-          if (it % n_qt == 0) {  // first tile of a head
-            ds_row = ds_head0 + (it / n_qt) * ds_tb;
+          if (tq == 0) {  // first tile of a head
+            ds_row = ds_head0 + hh * ds_tb;
             ds_q128 = q0 >> 7;
             ds_nkb = wide_blocks_of_qtile(sq, ds_q128, ds_kb0);
           } else if ((q0 >> 7) != ds_q128) {
@@ -482,9 +483,10 @@ __global__ void __launch_bounds__(384, 1)
     const bool part_tile = WDS && k0 + kBlockM > sq.lk;
     const long long krow_last = min(k0 + kBlockM, sq.lk) - 1;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    int tq = 0;  // query tile of iteration it
+    for (int it = 0; it < n_it; ++it, tq = (tq + 1 == n_qt) ? 0 : tq + 1) {
       const int st = it & 1;
-      const int q0 = (qt0 + it % n_qt) * BQ;
+      const int q0 = (qt0 + tq) * BQ;
       if (!mbar_wait_warp(&sdp_full, it & 1u, ab)) {
         ok = false;
         break;
