@@ -109,20 +109,18 @@ constexpr int kDsChunk = 128 * 16;  // one 8-query column of all 128 key rows
 constexpr int kDsBlock = 16 * kDsChunk;
 
 // The dS path serves head dims 128/128 and 192/128 (single-launch dK/dV
-// kernels).  ds_mode (the params' bwd_ds field) forces it off (-1) or on (1);
-// by default (0) it runs at 192/128 while its blocks take at most kDsCap
-// bytes.  The trade, measured on GB300 at causal 192/128: the dK/dV kernel
-// slows by about a quarter with 32 KiB of dS stores per tile, the dQ GEMM
-// streams them at 0.85 of the copy bandwidth, and dQ no longer recomputes
-// S (192) and dP (128) per pair: 33.0 -> 31.6 ms for B1 H32 S32K fwd+bwd,
-// even at 4K.  At 128/128 the recomputing dQ kernel does 384 instead of 512
-// per pair, and the two are even (THD 65K tokens: 9.8 vs 9.9 ms); at 64/64
-// recomputing is cheaper than streaming 32 KiB per 128 x 128 tile.
+// kernels) while its blocks take at most kDsCap bytes; ds_mode (the params'
+// bwd_ds field) forces it off (-1) or on (1).  The trade, measured on GB300:
+// the dK/dV kernel slows by about a fifth with 32 KiB of dS stores per tile,
+// the dQ GEMM streams them at 0.86 of the copy bandwidth, and dQ no longer
+// recomputes S and dP per pair: B1 H32 S32K 192/128 fwd+bwd 33.0 -> 29.9 ms,
+// THD 65K tokens 128/128 9.39 -> 9.04 ms.  At 64/64 recomputing is cheaper
+// than streaming 32 KiB per 128 x 128 tile.
 constexpr long long kDsCap = 64ll << 30;
 inline bool ds_backward(int dqk, int dv, long long block_bytes, int ds_mode) {
   const bool shape = (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128);
   if (!shape || ds_mode < 0) return false;
-  return ds_mode > 0 || (dqk == 192 && block_bytes <= kDsCap);
+  return ds_mode > 0 || block_bytes <= kDsCap;
 }
 
 struct WidePlanParams {

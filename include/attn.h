@@ -95,10 +95,9 @@ typedef struct {
                                that no kernel reads or writes. */
   const int32_t* seqused_k; /* the same for keys/values; set both or neither */
   int bwd_ds;              /* backward at head dims (128,128) and (192,128): 0 = auto
-                              (keep dS in the workspace at (192,128) when its blocks
-                              take at most 64 GiB), 1 = keep dS, -1 = never (recompute
-                              the scores for dQ: the smallest workspace).  See
-                              attn_bwd_path. */
+                              (keep dS in the workspace when its blocks take at most
+                              64 GiB), 1 = keep dS, -1 = never (recompute the scores
+                              for dQ: the smallest workspace).  See attn_bwd_path. */
 } attn_params_t;
 
 /* Bytes of workspace attn_fwd / attn_bwd need for `p` (always >= 256: the
@@ -116,8 +115,8 @@ size_t attn_bwd_workspace_size(const attn_params_t* p);
 /* The backward that attn_bwd runs for `p` (a pure function of `p`):
  *   ATTN_BWD_RECOMPUTE  a query-stationary dQ kernel and a key-stationary
  *                       dK/dV kernel that both compute S and dP;
- *   ATTN_BWD_DS         head dims (192,128), and (128,128) with bwd_ds = 1
- *                       (see bwd_ds): the dK/dV kernel also writes dS (16-bit)
+ *   ATTN_BWD_DS         head dims (128,128) and (192,128) as bwd_ds allows:
+ *                       the dK/dV kernel also writes dS (16-bit)
  *                       into the workspace and dQ = scale dS K is a GEMM over
  *                       it, so S and dP are computed once per query-key pair;
  *   ATTN_BWD_PDS        head dim 512, and 256 while its blocks take at most

@@ -264,9 +264,8 @@ def test_ds_backward_workspace_counts_visible_blocks(lib, dims, sq, sk, causal, 
     p = attn.make_params(q, k, v, bwd_ds=1, **kw)
     assert lib.attn_bwd_path(ctypes.byref(p)) == attn.BWD_DS
     assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == blk_off + blocks * 32768
-    p = attn.make_params(q, k, v, **kw)  # auto: 192/128 keeps dS, 128/128 recomputes
-    assert lib.attn_bwd_path(ctypes.byref(p)) == (attn.BWD_DS if dims[0] == 192 else
-                                                  attn.BWD_RECOMPUTE)
+    p = attn.make_params(q, k, v, **kw)  # auto keeps dS at both head dims
+    assert lib.attn_bwd_path(ctypes.byref(p)) == attn.BWD_DS
     p = attn.make_params(q, k, v, bwd_ds=-1, **kw)
     assert lib.attn_bwd_path(ctypes.byref(p)) == attn.BWD_RECOMPUTE
     assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == base
@@ -276,8 +275,8 @@ def test_ds_backward_workspace_counts_visible_blocks(lib, dims, sq, sk, causal, 
     (1, 32768, (192, 128), 0, 1),    # 32 heads: 1,052,672 blocks, 34.5 GB: kept
     (8, 32768, (192, 128), 0, 0),    # 276 GB of blocks: above the 64 GiB cap, recompute
     (8, 32768, (192, 128), 1, 1),    # ... unless forced
-    (1, 32768, (128, 128), 0, 0),    # 128/128 recomputes by default
-    (1, 32768, (128, 128), 1, 1),
+    (1, 32768, (128, 128), 0, 1),    # 128/128 keeps dS as well
+    (1, 32768, (128, 128), -1, 0),
     (1, 300, (64, 64), 0, 0),        # 64/64 always recomputes (cheaper than streaming dS)
     (1, 300, (64, 64), 1, 0),
     (1, 300, (256, 256), 0, 2),      # P and dS (the wide path)

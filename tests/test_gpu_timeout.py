@@ -37,7 +37,7 @@ CASES = [
     ("dq-192", (192, 128), 2, 2, 300, attn.DEBUG_DQ, 1, -1),
     ("dkdv-192", (192, 128), 2, 2, 300, attn.DEBUG_DKDV, 1, -1),
     ("ds-dkdv-128-gqa", (128, 128), 4, 2, 300, attn.DEBUG_DKDV, 3, 1),
-    ("dkdv-128-gqa", (128, 128), 4, 2, 300, attn.DEBUG_DKDV, 3, 0),
+    ("dkdv-128-gqa", (128, 128), 4, 2, 300, attn.DEBUG_DKDV, 3, -1),
     ("fwd-512", (512, 512), 4, 1, 300, attn.DEBUG_FWD, 1, 0),
     ("scores-512", (512, 512), 4, 1, 300, attn.DEBUG_SCORES, 5, 0),
     ("wide-dq-512", (512, 512), 4, 1, 300, attn.DEBUG_DQ, 1, 0),
