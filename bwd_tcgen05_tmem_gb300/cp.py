@@ -27,12 +27,17 @@ import torch
 
 from . import attn
 
-# The ring and all-gather schedules run the backward's stages themselves, dq
-# before dkdv (several calls' dq stages overlap on their streams; the dkdv
-# stages that add into shared dK/dV run one after another), and keep one
-# workspace per query-row set across ring steps: the recompute backward, whose
-# dq stage needs no blocks from the dkdv stage and whose workspace is small.
-RECOMPUTE = -1
+# The ring and all-gather schedules run the backward's stages themselves (the
+# dkdv stages that add into shared dK/dV run one after another, the dq stages
+# of different calls overlap on their streams) and keep one workspace per
+# query-row set across ring steps.  Each call takes the path the library picks
+# for its shape (attn_bwd_path): on the dS path the dkdv stage writes the dS
+# blocks that the dq stage of the same call then reads, so dkdv goes first.
+
+
+def stage_order(q, k, v, **kw):
+    """The dq / dkdv stages of one attn_bwd call in the order its path needs."""
+    return ("dkdv", "dq") if attn.bwd_path(q, k, v, **kw) == attn.BWD_DS else ("dq", "dkdv")
 
 
 @dataclasses.dataclass
@@ -146,12 +151,17 @@ class CPRing:
         # all of its rows and once for its second chunk, and every ring step
         # then runs only the dq and dkdv stages on the matching workspace
         c = self.chunk
+        shapes = (((0, 2 * c), (0, 2 * c), True), ((0, 2 * c), (0, c), False),
+                  ((c, c), (0, 2 * c), False))
         need = max(256, *(attn.workspace_size("bwd", self.q[0][:, q0:q0 + nq],
                                               self.k[0][:, k0:k0 + nk], self.v[0][:, k0:k0 + nk],
-                                              causal=cz, bwd_ds=RECOMPUTE)
-                          for (q0, nq), (k0, nk), cz in (((0, 2 * c), (0, 2 * c), True),
-                                                         ((0, 2 * c), (0, c), False),
-                                                         ((c, c), (0, 2 * c), False))))
+                                              causal=cz) for (q0, nq), (k0, nk), cz in shapes))
+        order = {(qr, kr[1], cz): stage_order(self.q[0][:, qr[0]:qr[0] + qr[1]],
+                                              self.k[0][:, kr[0]:kr[0] + kr[1]],
+                                              self.v[0][:, kr[0]:kr[0] + kr[1]], causal=cz)
+                 for qr, kr, cz in shapes}
+        self.order = [[order[(pc.q_rows, pc.k_rows[1], pc.causal)] for pc in pcs]
+                      for pcs in self.pieces]
         self.bwd_ws = [{rq: torch.empty(need, dtype=torch.uint8, device=dev)
                         for rq in ((0, 2 * c), (c, c))} for _ in range(cp)]
         self.streams = _Streams(cp, dev)
@@ -219,8 +229,7 @@ class CPRing:
                      dq=self.dq[r][:, q0:q0 + nq], dk=self.dk[pc.src][:, k0:k0 + nk],
                      dv=self.dv[pc.src][:, k0:k0 + nk], grad_dtype=torch.float32,
                      accumulate=accumulate, lse_strides=(0, rows),
-                     workspace=self.bwd_ws[r][pc.q_rows], stream=self.streams.s[r], stage=stage,
-                     bwd_ds=RECOMPUTE)
+                     workspace=self.bwd_ws[r][pc.q_rows], stream=self.streams.s[r], stage=stage)
             return attn.last_launch_count()
 
         for r in range(cp):  # D of every query-row set the rank's steps use, once
@@ -235,10 +244,11 @@ class CPRing:
                 if s > 0:
                     st.wait_event(done[s - 1][(r - 1) % cp])
                 pc = self.pieces[r][s]
-                n += call(r, pc, "dq", s > 0)
-                n += call(r, pc, "dkdv", s > 0)
-                done[s][r] = torch.cuda.Event()
-                done[s][r].record(st)
+                for stage in self.order[r][s]:
+                    n += call(r, pc, stage, s > 0)
+                    if stage == "dkdv":  # the next step's writer of this shard waits here
+                        done[s][r] = torch.cuda.Event()
+                        done[s][r].record(st)
         self.streams.join()
         self.launches += n
         return self.dq, self.dk, self.dv
@@ -298,13 +308,16 @@ class CPAllGather:
         self.dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
         self.dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
         self.fwd_ws = [torch.empty(256, dtype=torch.uint8, device=dev) for _ in range(cp)]
-        need = max(attn.workspace_size("bwd", self.q[0][:, :self.chunk], k[:, k0:k1],
-                                       v[:, k0:k1], causal=True, bottom_right=True,
-                                       window=self.window, bwd_ds=RECOMPUTE)
-                   for pcs in self.pieces for _, _, (k0, k1) in pcs)
-        # one workspace per call: the calls' preprocess and dq stages overlap
-        self.bwd_ws = [[torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-                        for _ in pcs] for pcs in self.pieces]
+        kw = dict(causal=True, bottom_right=True, window=self.window)
+        qc = self.q[0][:, :self.chunk]
+        # one workspace per call, sized for its own key range: the calls'
+        # preprocess and dq stages overlap
+        self.bwd_ws = [[torch.empty(max(attn.workspace_size("bwd", qc, k[:, k0:k1], v[:, k0:k1],
+                                                            **kw), 256),
+                                    dtype=torch.uint8, device=dev)
+                        for _, _, (k0, k1) in pcs] for pcs in self.pieces]
+        self.order = [[stage_order(qc, k[:, k0:k1], v[:, k0:k1], **kw) for _, _, (k0, k1) in pcs]
+                      for pcs in self.pieces]
         self.streams = _Streams(cp, dev)
         self.launches = 0
 
@@ -349,18 +362,29 @@ class CPAllGather:
                          window=self.window, scale=self.scale, dq=self.dq[r][:, q0:q0 + nq],
                          dk=self.dk[:, k0:k1], dv=self.dv[:, k0:k1], grad_dtype=torch.float32,
                          accumulate=True, lse_strides=(0, rows), workspace=self.bwd_ws[r][i],
-                         stream=st, stage=stage, bwd_ds=RECOMPUTE)
+                         stream=st, stage=stage)
                 return attn.last_launch_count()
 
-            for i in range(len(pcs)):  # independent: every call has its own rows
-                n += call(i, "preprocess")
-                n += call(i, "dq")
-            for i in range(len(pcs)):  # shared dK/dV: one after another
+            def dkdv(i):  # shared dK/dV: one call after another
+                nonlocal prev
                 if prev is not None:
                     st.wait_event(prev)
-                n += call(i, "dkdv")
+                launched = call(i, "dkdv")
                 prev = torch.cuda.Event()
                 prev.record(st)
+                return launched
+
+            late = []
+            for i in range(len(pcs)):  # independent: every call has its own rows
+                n += call(i, "preprocess")
+                if self.order[r][i][0] == "dkdv":  # dS path: its dq stage reads the blocks
+                    n += dkdv(i)
+                    n += call(i, "dq")
+                else:
+                    n += call(i, "dq")
+                    late.append(i)
+            for i in late:
+                n += dkdv(i)
         self.streams.join()
         self.launches += n
         return self.dq, self.dk, self.dv

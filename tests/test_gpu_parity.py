@@ -409,9 +409,13 @@ def test_backward_stages_equal_full_call(dims):
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     o, lse = attn.fwd(qd, kd, vd)
     g1 = attn.bwd(qd, kd, vd, o, dod, lse)
-    ws = torch.empty(attn.workspace_size("bwd", qd, kd, vd), dtype=torch.uint8, device="cuda")
+    # poisoned, so that no stage can pass on what an earlier call left behind
+    ws = torch.full((attn.workspace_size("bwd", qd, kd, vd),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
     dq, dk, dv = (torch.empty_like(t) for t in (qd, kd, vd))
-    for stage in ("preprocess", "dq", "dkdv"):
+    # on the dS path the dkdv stage writes the blocks that the dq stage reads
+    order = ("dkdv", "dq") if attn.bwd_path(qd, kd, vd) == attn.BWD_DS else ("dq", "dkdv")
+    for stage in ("preprocess", *order):
         attn.bwd(qd, kd, vd, o, dod, lse, dq=dq, dk=dk, dv=dv, workspace=ws, stage=stage)
     torch.cuda.synchronize()
     for a, b in zip(g1, (dq, dk, dv)):
