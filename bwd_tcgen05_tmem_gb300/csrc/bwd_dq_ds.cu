@@ -12,12 +12,20 @@
 // it by a K tile that the CTAs working on the same head share through L2:
 // per block, 128 x DQK x 128 MACs against 32 KiB, so it is bound by HBM
 // bandwidth (at DQK = 192, about 1.3 PFLOP/s at the measured copy bandwidth).
-// Four dS stages keep 128 KiB in flight per SM; the kernel is persistent, so
-// the stream does not pause between query tiles.
+// Four dS stages keep up to 128 KiB in flight per SM; the kernel is
+// persistent, so the stream does not pause between query tiles.  At DQK = 128
+// (three 32 KiB K stages) dS and K have producers of their own and the dS
+// stream runs four blocks ahead of the MMAs; at DQK = 192 (two 48 KiB K
+// stages) one producer issues each block's dS and K in turn, which keeps the
+// K copies, which gate the MMAs, behind at most one dS copy (measured on one
+// GB300, same results bit for bit: a separate K producer took the 32K
+// DQK = 192 GEMM from 6.37 to 6.41 ms, and at DQK = 128 the 65K-token packed
+// one from 1.75 to 1.70 ms).
 //
-// Warp roles (192 threads): warp 0 producer (dS by bulk copy, K by TMA),
-// warp 1 TMEM owner and MMA issuer, warps 2..5 epilogue (TMEM lane quarter
-// warp & 3).  MMA per K-step of 16 keys: M = 128 queries, N = DQK, A = dS
+// Warp roles: warp 0 dS producer (it also takes the items from the work
+// queue, and issues the K copies too at DQK = 192), warp 1 TMEM owner and MMA
+// issuer, warps 2..5 epilogue (TMEM lane quarter warp & 3), warp 6 K producer
+// (DQK = 128 only).  MMA per K-step of 16 keys: M = 128 queries, N = DQK, A = dS
 // (MN-major, unswizzled: 8-query groups SBO = 2 KiB apart, 8-key groups LBO =
 // 128 bytes apart), B = K (MN-major: head-dim contiguous, 128-byte swizzle,
 // 64-column chunks LBO apart).
@@ -35,12 +43,14 @@ struct DqDsCfg {
   static constexpr int kKStages = kKStagesRaw > 4 ? 4 : kKStagesRaw;
   static constexpr int kSmem = kDsStages * kDsBlock + kKStages * kKTile + 1024;
   static constexpr int kAccCols = DQK <= 128 ? 128 : 256;  // one accumulator buffer
+  static constexpr bool kSplitK = kKStages >= 3;  // a K producer warp of its own
+  static constexpr int kThreads = kSplitK ? 224 : 192;
   static_assert(DQK % 64 == 0 && DQK <= 256, "head dim");
   static_assert(kKStages >= 2, "K stages");
 };
 
 template <int DQK, bool BF16, bool G_F32>
-__global__ void __launch_bounds__(192, 1) attn_bwd_dq_ds_kernel(const __grid_constant__ DqDsParams p) {
+__global__ void __launch_bounds__(DqDsCfg<DQK>::kThreads, 1) attn_bwd_dq_ds_kernel(const __grid_constant__ DqDsParams p) {
   using C = DqDsCfg<DQK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -105,7 +115,7 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_ds_kernel(const __grid_con
       mbar_init(&acc_free[i], 4);  // one arrival per epilogue warp
     }
     mbar_init(&drain_bar, 1);
-    item_ring_init(iring, 5);  // consumers: the MMA warp, four epilogue warps
+    item_ring_init(iring, C::kSplitK ? 6 : 5);  // MMA, four epilogue warps (, K producer)
     fence_barrier_init();
     tma_prefetch_desc(&p.tm_k);
     skip_sh = status != 0;
@@ -123,10 +133,10 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_ds_kernel(const __grid_con
   }
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // per key block: its dS block (one 32 KiB bulk copy, read once: L2
-    // evict-first), then the K tile; the whole warp runs the loop, one
-    // elected lane issues the copies; n counts the blocks of all items
+    // ------------------------------------------------------------ dS producer
+    // per key block its dS block (one 32 KiB bulk copy, read once: L2
+    // evict-first), then (DQK = 192) its K tile; the whole warp runs the
+    // loop, one elected lane issues the copies; n counts the blocks of all items
     const uint64_t pol = l2_evict_first();
     bool ok = true;
     int n = 0, nk = 0;  // dS and K copies issued
@@ -148,8 +158,6 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_ds_kernel(const __grid_con
         ok = false;
         break;
       }
-      const int g = it.h / (p.hq / p.hkv);
-      const int tb = p.geo.cu_q ? 0 : it.b;
       for (int j = 0; j < it.n_kb && ok; ++j, ++n) {
         const int s = n % C::kDsStages;
         if (!mbar_wait_warp(&ds_empty[s], ((n / C::kDsStages) & 1) ^ 1, ab)) {
@@ -162,10 +170,49 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_ds_kernel(const __grid_con
                          &ds_full[s], pol);
         }
         __syncwarp();
+        if constexpr (!C::kSplitK) {
+          const int ks = n % C::kKStages;
+          if (!mbar_wait_warp(&k_empty[ks], ((n / C::kKStages) & 1) ^ 1, ab)) {
+            ok = false;
+            ++n;  // its dS copy is in flight
+            break;
+          }
+          int c1, c2, c3;
+          map_coords(p.ok, 0, it.h / (p.hq / p.hkv), it.sq.k_start + (it.kb0 + j) * kBlockN,
+                     p.geo.cu_q ? 0 : it.b, c1, c2, c3);
+          if (elect_sync()) {
+            mbar_arrive_tx(&k_full[ks], C::kKTile);
+#pragma unroll
+            for (int c = 0; c < C::kKCh; ++c)
+              tma_load_4d(sK + ks * C::kKTile + c * kSlotBytes, &p.tm_k, &k_full[ks], c * 64, c1, c2,
+                          c3);
+          }
+          __syncwarp();
+          nk = n + 1;
+        }
+      }
+    }
+    // let the copies in flight land before the CTA can exit
+    for (int v = n > C::kDsStages ? n - C::kDsStages : 0; v < n; ++v)
+      mbar_wait_quiet(&ds_full[v % C::kDsStages], (v / C::kDsStages) & 1, lim);
+    for (int v = nk > C::kKStages ? nk - C::kKStages : 0; v < nk; ++v)
+      mbar_wait_quiet(&k_full[v % C::kKStages], (v / C::kKStages) & 1, lim);
+  } else if (C::kSplitK && warp == 6) {
+    // ------------------------------------------------------------ K producer
+    // (DQK = 128) the K tile of every block, in the dS producer's order
+    bool ok = true;
+    int n = 0;  // K copies issued
+    for (int q = 0; ok; ++q) {
+      const int li = item_ring_pop(iring, q, ab, ok);
+      if (li < 0) break;
+      const Item it = item(li);
+      if (it.n_kb == 0) continue;
+      const int g = it.h / (p.hq / p.hkv);
+      const int tb = p.geo.cu_q ? 0 : it.b;
+      for (int j = 0; j < it.n_kb && ok; ++j, ++n) {
         const int ks = n % C::kKStages;
         if (!mbar_wait_warp(&k_empty[ks], ((n / C::kKStages) & 1) ^ 1, ab)) {
           ok = false;
-          ++n;  // its dS copy is in flight
           break;
         }
         int c1, c2, c3;
@@ -177,13 +224,9 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_ds_kernel(const __grid_con
             tma_load_4d(sK + ks * C::kKTile + c * kSlotBytes, &p.tm_k, &k_full[ks], c * 64, c1, c2, c3);
         }
         __syncwarp();
-        nk = n + 1;
       }
     }
-    // let the copies in flight land before the CTA can exit
-    for (int v = n > C::kDsStages ? n - C::kDsStages : 0; v < n; ++v)
-      mbar_wait_quiet(&ds_full[v % C::kDsStages], (v / C::kDsStages) & 1, lim);
-    for (int v = nk > C::kKStages ? nk - C::kKStages : 0; v < nk; ++v)
+    for (int v = n > C::kKStages ? n - C::kKStages : 0; v < n; ++v)
       mbar_wait_quiet(&k_full[v % C::kKStages], (v / C::kKStages) & 1, lim);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -236,7 +279,7 @@ __global__ void __launch_bounds__(192, 1) attn_bwd_dq_ds_kernel(const __grid_con
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (warps 2..5)
     const int wq = warp & 3;  // TMEM lane quarter this warp may access
     const int r = wq * 32 + (threadIdx.x & 31);
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -334,7 +377,7 @@ cudaError_t launch_dq_ds_t(const DqDsParams& p, unsigned ctas, cudaStream_t st) 
   auto k = attn_bwd_dq_ds_kernel<DQK, BF16, G_F32>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  k<<<ctas, 192, C::kSmem, st>>>(p);
+  k<<<ctas, C::kThreads, C::kSmem, st>>>(p);
   return cudaGetLastError();
 }
 
