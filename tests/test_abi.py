@@ -295,3 +295,17 @@ def test_bwd_path_selection(lib, b, s, dims, mode, path):
         base = 256 + -(-(b * s * hq * 8) // 256) * 256
         blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
         assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == blk_off + blocks * 32768
+
+
+@pytest.mark.parametrize("dims,causal,order", [
+    ((192, 128), True, ("dkdv", "dq")),    # dS path: the dkdv stage writes the blocks
+    ((128, 128), False, ("dkdv", "dq")),
+    ((64, 64), True, ("dq", "dkdv")),      # recompute
+    ((512, 512), False, ("dq", "dkdv")),   # P/dS: the scores kernel runs in the dq stage
+])
+def test_cp_stage_order_follows_the_path(lib, dims, causal, order):
+    """The CP schedules run each call's stages in the order its path needs."""
+    from bwd_tcgen05_tmem_gb300 import cp as cpmod
+    q, k = fake((1, 4096, 8, dims[0])), fake((1, 2048, 8, dims[0]))
+    v = fake((1, 2048, 8, dims[1]))
+    assert cpmod.stage_order(q, k, v, causal=causal) == order
