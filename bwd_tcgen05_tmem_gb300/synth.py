@@ -92,6 +92,8 @@ class Workload:
 WORKLOADS = {
     w.name: w for w in [
         Workload("tiny_b1_h2_s256_d64", 1, 256, 2, 2, 64, 64),
+        # the benchmark's head dims at a size the oracle checks in a moment
+        Workload("tiny_b1_h2_s256_d192_128", 1, 256, 2, 2, 192, 128),
         Workload("b2_h32_s4096_d192_128", 2, 4096, 32, 32, 192, 128),
         Workload("b1_h32_s32768_d192_128", 1, 32768, 32, 32, 192, 128),
         # the same heads at 8K: a profiling case (64 tiles per head, so the
