@@ -37,6 +37,9 @@ CASES = [
     ("dq-192", (192, 128), 2, 2, 300, attn.DEBUG_DQ, 1, -1),
     ("dkdv-192", (192, 128), 2, 2, 300, attn.DEBUG_DKDV, 1, -1),
     ("ds-dkdv-128-gqa", (128, 128), 4, 2, 300, attn.DEBUG_DKDV, 3, 1),
+    # at head dim 128 the dQ GEMM has a K producer warp of its own, which must
+    # unwind too when a dS copy is missing
+    ("ds-dq-gemm-128-gqa", (128, 128), 4, 2, 300, attn.DEBUG_DQ, 1, 1),
     ("dkdv-128-gqa", (128, 128), 4, 2, 300, attn.DEBUG_DKDV, 3, -1),
     ("fwd-512", (512, 512), 4, 1, 300, attn.DEBUG_FWD, 1, 0),
     ("scores-512", (512, 512), 4, 1, 300, attn.DEBUG_SCORES, 5, 0),
