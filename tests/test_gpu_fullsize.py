@@ -17,7 +17,6 @@ implementation run on the same sub-problem (or key subset), and gradients by
 relative L2.  The GPU results come from one call at the full size, in the
 launch configuration the benchmark uses.
 """
-import math
 
 import numpy as np
 import pytest
@@ -25,7 +24,7 @@ import torch
 
 import oracle
 from bwd_tcgen05_tmem_gb300 import attn, synth
-from parity import GRAD_REL_L2, check_lse, gate, rel_l2
+from parity import check_lse, gate, rel_l2
 
 pytestmark = pytest.mark.gpu
 
