@@ -60,3 +60,36 @@ def test_flop_attribution_sums_to_total(name):
     assert f["fwd"] == 2 * nv * (w.d_qk + w.d_v)
     assert f["bwd"] == 2 * nv * (3 * w.d_qk + 2 * w.d_v)
     assert sum(f["kernel"].values()) == f["total"] == f["fwd"] + f["bwd"]
+
+
+@pytest.mark.parametrize("b,s,window", [(1, 1, (-1, 0)), (2, 300, (-1, 0)), (1, 1000, (200, 0)),
+                                        (3, 256, (127, 0)), (1, 4096, (-1, 0))])
+def test_score_blocks_match_the_library_plan(b, s, window):
+    """``bench.score_blocks`` (the dS bytes the benchmark credits to the dK/dV
+    kernel and the dQ GEMM) counts the 128 x 128 blocks the library sizes its
+    dS workspace for, and every block it counts holds a visible pair."""
+    import ctypes
+    import torch
+    from bwd_tcgen05_tmem_gb300 import attn, build
+    build.build()
+    lib = attn.load()
+    hq = 4
+    w = BASE.with_(batch=b, seqlen=s, heads_q=hq, heads_kv=2, d_qk=192, d_v=128, window=window)
+    meta = lambda *shape: torch.empty(shape, dtype=torch.bfloat16, device="meta")  # noqa: E731
+    q, k, v = meta(b, s, hq, 192), meta(b, s, 2, 192), meta(b, s, 2, 128)
+    p = attn.make_params(q, k, v, o=meta(b, s, hq, 128), causal=True, window=window, bwd_ds=1)
+    assert lib.attn_bwd_path(ctypes.byref(p)) == attn.BWD_DS
+    base = 256 + -(-(b * s * hq * 8) // 256) * 256
+    blk_off = -(-(base + (b + 1) * 8) // 1024) * 1024
+    blocks = (lib.attn_bwd_workspace_size(ctypes.byref(p)) - blk_off) // 32768
+    assert bench.score_blocks(w) == blocks
+    # brute force over the blocks of one sequence and head: a block counts iff
+    # some query row of its tile sees some key of it (causal, left window)
+    wl = window[0]
+    n = 0
+    for qt in range((s + 127) // 128):
+        for kb in range((s + 127) // 128):
+            n += any(kb * 128 <= j <= min(kb * 128 + 127, i) and (wl < 0 or j >= i - wl)
+                     for i in range(qt * 128, min(qt * 128 + 128, s))
+                     for j in range(kb * 128, min(kb * 128 + 128, s)))
+    assert bench.score_blocks(w) == n * b * hq
