@@ -19,18 +19,17 @@
 // that GEMM to 5.56 ms (same GPU, bit-identical dQ).
 //
 // Four dS stages keep up to 128 KiB in flight per SM; the kernel is
-// persistent, so the stream does not pause between items.  At DQK = 128
-// (three 32 KiB K stages) dS and K have producers of their own; at DQK = 192
-// (two 48 KiB K stages) one producer issues each key block's dS copies and
-// then its K copy, so a K copy, which gates the MMAs, never queues behind
-// more than one key block's dS.  TMEM holds two accumulator pairs at
+// persistent, so the stream does not pause between items.  dS and K have
+// producers of their own (three 32 KiB K stages at DQK = 128, two 48 KiB ones
+// at 192), so the dS copies run up to four blocks ahead of the MMAs (with one
+// producer issuing each block's dS and then its K copy the 32K GEMM took
+// 5.54 instead of 5.41 ms, same GPU).  TMEM holds two accumulator pairs at
 // DQK = 128 (an item's epilogue overlaps the next item's MMAs) and one at
 // DQK = 192 (two 192-column accumulators in the 512 columns).
 //
-// Warp roles: warp 0 dS producer (it also takes the items from the work
-// queue, and issues the K copies too at DQK = 192), warp 1 TMEM owner and MMA
-// issuer, warps 2..5 epilogue (TMEM lane quarter warp & 3), warp 6 K producer
-// (DQK = 128 only).  MMA per K-step of 16 keys: M = 128 queries, N = DQK, A = dS
+// Warp roles (224 threads): warp 0 dS producer (it also takes the items from
+// the work queue), warp 1 TMEM owner and MMA issuer, warps 2..5 epilogue (TMEM
+// lane quarter warp & 3), warp 6 K producer.  MMA per K-step of 16 keys: M = 128 queries, N = DQK, A = dS
 // (MN-major, unswizzled: 8-query groups SBO = 2 KiB apart, 8-key groups LBO =
 // 128 bytes apart), B = K (MN-major: head-dim contiguous, 128-byte swizzle,
 // 64-column chunks LBO apart).
@@ -50,8 +49,7 @@ struct DqDsCfg {
   static constexpr int kTileCols = DQK <= 128 ? 128 : 256;  // TMEM columns of one tile's dQ
   static constexpr int kTmemCols = 512;
   static constexpr int kAccBufs = 4 * kTileCols <= kTmemCols ? 2 : 1;  // accumulator pairs
-  static constexpr bool kSplitK = kKStages >= 3;  // a K producer warp of its own
-  static constexpr int kThreads = kSplitK ? 224 : 192;
+  static constexpr int kThreads = 224;
   static_assert(DQK % 64 == 0 && DQK <= 256, "head dim");
   static_assert(kKStages >= 2, "K stages");
 };
@@ -137,7 +135,7 @@ __global__ void __launch_bounds__(DqDsCfg<DQK>::kThreads, 1) attn_bwd_dq_ds_kern
       mbar_init(&acc_free[i], 4);  // one arrival per epilogue warp
     }
     mbar_init(&drain_bar, 1);
-    item_ring_init(iring, C::kSplitK ? 6 : 5);  // MMA, four epilogue warps (, K producer)
+    item_ring_init(iring, 6);  // consumers: MMA, four epilogue warps, K producer
     fence_barrier_init();
     tma_prefetch_desc(&p.tm_k);
     skip_sh = status != 0;
@@ -157,12 +155,11 @@ __global__ void __launch_bounds__(DqDsCfg<DQK>::kThreads, 1) attn_bwd_dq_ds_kern
   if (warp == 0) {
     // ------------------------------------------------------------ dS producer
     // per key block the dS block of each tile that sees it (one 32 KiB bulk
-    // copy each, read once: L2 evict-first), then (DQK = 192) the K tile; the
-    // whole warp runs the loop, one elected lane issues the copies; the
-    // counts run over all items
+    // copy each, read once: L2 evict-first); the whole warp runs the loop, one
+    // elected lane issues the copies; the count runs over all items
     const uint64_t pol = l2_evict_first();
     bool ok = true;
-    int nd = 0, nk = 0;  // dS and K copies issued
+    int nd = 0;  // dS copies issued
     for (int q = 0; ok; ++q) {
       const int li = item_ring_push(iring, q, p.counter, n_items, ab, ok);
       if (li < 0) break;
@@ -185,10 +182,8 @@ __global__ void __launch_bounds__(DqDsCfg<DQK>::kThreads, 1) attn_bwd_dq_ds_kern
       }
       int jc = 0;  // dS copies of this item
       for (int kb = it.lo; kb < it.hi && ok; ++kb) {
-        bool any = false;
         for (int u = 0; u < 2; ++u) {
           if (!active(it, u, kb)) continue;
-          any = true;
           const int s = nd % C::kDsStages;
           if (!mbar_wait_warp(&ds_empty[s], ((nd / C::kDsStages) & 1) ^ 1, ab)) {
             ok = false;
@@ -204,37 +199,15 @@ __global__ void __launch_bounds__(DqDsCfg<DQK>::kThreads, 1) attn_bwd_dq_ds_kern
           ++nd;
           ++jc;
         }
-        if constexpr (!C::kSplitK) {
-          if (!ok || !any) continue;
-          const int ks = nk % C::kKStages;
-          if (!mbar_wait_warp(&k_empty[ks], ((nk / C::kKStages) & 1) ^ 1, ab)) {
-            ok = false;
-            break;
-          }
-          int c1, c2, c3;
-          map_coords(p.ok, 0, it.h / (p.hq / p.hkv), it.sq.k_start + kb * kBlockN,
-                     p.geo.cu_q ? 0 : it.b, c1, c2, c3);
-          if (elect_sync()) {
-            mbar_arrive_tx(&k_full[ks], C::kKTile);
-#pragma unroll
-            for (int c = 0; c < C::kKCh; ++c)
-              tma_load_4d(sK + ks * C::kKTile + c * kSlotBytes, &p.tm_k, &k_full[ks], c * 64, c1, c2,
-                          c3);
-          }
-          __syncwarp();
-          ++nk;
-        }
       }
     }
     // let the copies in flight land before the CTA can exit
     for (int v = nd > C::kDsStages ? nd - C::kDsStages : 0; v < nd; ++v)
       mbar_wait_quiet(&ds_full[v % C::kDsStages], (v / C::kDsStages) & 1, lim);
-    for (int v = nk > C::kKStages ? nk - C::kKStages : 0; v < nk; ++v)
-      mbar_wait_quiet(&k_full[v % C::kKStages], (v / C::kKStages) & 1, lim);
-  } else if (C::kSplitK && warp == 6) {
+  } else if (warp == 6) {
     // ------------------------------------------------------------ K producer
-    // (DQK = 128) the K tile of every key block either tile sees, in the dS
-    // producer's order
+    // the K tile of every key block either tile sees, in the dS producer's
+    // order
     bool ok = true;
     int nk = 0;  // K copies issued
     for (int q = 0; ok; ++q) {
