@@ -112,7 +112,7 @@ constexpr int kDsBlock = 16 * kDsChunk;
 // kernels) while its blocks take at most kDsCap bytes; ds_mode (the params'
 // bwd_ds field) forces it off (-1) or on (1).  The trade, measured on GB300:
 // the dK/dV kernel slows by about a fifth with 32 KiB of dS stores per tile,
-// the dQ GEMM streams them at 0.98 of the copy bandwidth, and dQ no longer
+// the dQ GEMM streams them at the copy bandwidth, and dQ no longer
 // recomputes S and dP per pair: B1 H32 S32K 192/128 fwd+bwd 33.0 -> 28.9 ms,
 // THD 65K tokens 128/128 9.39 -> 8.99 ms.  At 64/64 recomputing is cheaper
 // than streaming 32 KiB per 128 x 128 tile.
